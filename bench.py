@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of the block-batched MXFP4 MoE layer on GB300.
+
+Workload (one GPU): the Kimi K3.1-shaped MoE layer in decode, one row per step:
+d=7168, f=1536, all 896 MXFP4 experts resident in HBM (15.7 GB), top-16 softmax
+routing through the bf16 router GEMV, plus the 2 Q8_0 shared experts; 100
+seeded N(0,1) rows, timed one at a time.  A step is one whole layer
+(moe_route -> moe_expert_block -> moe_combine) on one row.
+
+Metric: HBM GB/s on the unique MXFP4 expert bytes the layer reads (16 experts x
+17,547,264 B per row), i.e. unique expert bytes / layer time.  Inputs are
+resident in HBM; L2 is flushed (256 MB write) before every timed step, outside
+the timed events.  Extra keys report 8- and 16-row verification blocks and the
+roofline of the expert kernel.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+With --gpus N > 1 (under torchrun) every rank runs the same single-GPU layer on
+its own GPU (replicas: the layer has no cross-GPU step); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as syn  # noqa: E402
+
+SEED = 0
+N_ROWS_SEEDED = 100
+SLAB = 17547264
+Q8_SLAB = 35094528
+ROUTER_BYTES = 896 * 7168 * 2
+METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
+UNIT = "GB/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; read-only queries)
+# ---------------------------------------------------------------------------
+
+_REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+            0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class ClockSampler:
+    def __init__(self, pci_bus_id: str | None):
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thr = None
+        self.ok = False
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if pci_bus_id is None or nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                    return
+            m = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(m)) == 0:
+                self.max_mhz = m.value
+            self.nv, self.h = nv, h
+            self.ok = True
+        except OSError:
+            pass
+
+    def _run(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            a = self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))
+            b = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+            if a == 0:
+                self.samples.append((clk.value, rs.value if b == 0 else 0))
+            time.sleep(0.002)
+
+    def start(self):
+        if self.ok:
+            self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr.start()
+
+    def stop(self):
+        if self._thr:
+            self._stop.set()
+            self._thr.join()
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        reasons = set()
+        for _, r in busy:
+            for bit, name in _REASONS.items():
+                if r & bit and bit != 0x1:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(c for c, _ in busy), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle sample (the baseline), run in a single-threaded subprocess
+# ---------------------------------------------------------------------------
+
+def oracle_pairs(n_pairs: int, start: int = 0):
+    """(row, expert) pairs of the workload in order: the experts each seeded row's
+    oracle routing selects."""
+    from oracle import moe_oracle as orc
+    router = syn.router_weight(SEED, syn.KIMI)
+    pairs = []
+    r = 0
+    while len(pairs) < start + n_pairs:
+        x = syn.x_rows(SEED, [r % N_ROWS_SEEDED], syn.KIMI.d_model)
+        lo = orc.router_logits(x, router)
+        for e in orc.select_topk(lo.astype(np.float32).astype(np.float64), syn.KIMI.top_k)[0]:
+            pairs.append((r % N_ROWS_SEEDED, int(e)))
+        r += 1
+    return pairs[start:start + n_pairs]
+
+
+def oracle_step_seconds(pairs):
+    """Times the oracle's expert MLP (slab decode + SwiGLU MLP in float64) on each
+    (row, expert) pair; slab generation is input creation and is not timed."""
+    from oracle import moe_oracle as orc
+    times = []
+    for r, e in pairs:
+        x = orc.bf16_bits_to_float(syn.x_rows(SEED, [r], syn.KIMI.d_model))
+        slab = syn.mxfp4_expert_slab(SEED, e, syn.KIMI)
+        t0 = time.perf_counter()
+        wg, wu, wd = orc.mxfp4_expert_mats(slab, syn.KIMI.d_model, syn.KIMI.d_ff)
+        orc.swiglu_expert(x, wg, wu, wd)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def cpu_baseline(n_pairs: int = 16):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(n_pairs)],
+                       capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
+    secs = json.loads(r.stdout.strip().splitlines()[-1])["seconds"]
+    return {"value": n_pairs * SLAB / sum(secs) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_pairs} (row, expert) pairs of the 1-row Kimi decode workload: fp64 slab decode + "
+                      f"SwiGLU expert MLP per pair, {sum(secs):.1f} s; router, shared experts and combine "
+                      f"(<25% of the bytes) not in the sample"}
+
+
+# ---------------------------------------------------------------------------
+# GPU layer
+# ---------------------------------------------------------------------------
+
+def build_layer(torch, dev):
+    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+    sh = syn.KIMI
+    lay = MoeLayer(sh.d_model, sh.d_ff, sh.n_experts, sh.top_k, n_rows_max=16, n_shared=2, device=dev)
+    router = syn.router_weight(SEED, sh)
+    lay.set_router(torch.from_numpy(router.view(np.int16)).view(torch.uint16))
+    lay.alloc_pool(sh.n_experts)
+    threads = max(2, min(16, os.cpu_count() or 2))
+    for e, slab in syn.mxfp4_slabs_parallel(SEED, range(sh.n_experts), sh, threads=threads):
+        lay.put_slab(e, slab)
+    lay.set_expert_slots(np.arange(sh.n_experts, dtype=np.int32))
+    lay.set_shared([syn.q8_0_shared_slab(SEED, s, sh) for s in range(2)])
+    return lay
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_mod.build()
+    lay = build_layer(torch, dev)
+    stream = torch.cuda.current_stream()
+    xs = syn.x_rows(SEED, range(N_ROWS_SEEDED), syn.KIMI.d_model)
+    X = torch.from_numpy(xs.view(np.int16)).to(dev).view(torch.uint16)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    K, W = args.steps, args.warmup
+
+    def layer_step(i, kev=None):
+        x = X[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1]
+        lay.route(1, x)
+        if kev:
+            kev[0].record()
+        lay.experts(1)
+        if kev:
+            kev[1].record()
+        lay.combine(1, x)
+
+    for i in range(W):
+        flush.zero_()
+        layer_step(i)
+    torch.cuda.synchronize()
+    assert lay.error_bits() == 0
+
+    props = torch.cuda.get_device_properties(dev)
+    bus = getattr(props, "pci_bus_id", None)
+    sampler = ClockSampler(bus if isinstance(bus, str) else None)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record()
+        layer_step(W + i, kev[i])
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    assert lay.error_bits() == 0
+    layer_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    total_ms = sum(layer_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    U = syn.KIMI.top_k  # a single row selects 16 distinct experts
+    unique_bytes = U * SLAB
+    value = world * K * unique_bytes / (total_ms * 1e-3) / 1e9
+    all_bytes = unique_bytes + 2 * Q8_SLAB + ROUTER_BYTES + 3 * syn.KIMI.d_model * 2
+    kern_bytes = unique_bytes + 2 * Q8_SLAB + syn.KIMI.d_model * 2 + (16 + 2) * syn.KIMI.d_model * 4
+    kern_avg_s = statistics.mean(kern_ms) * 1e-3
+    peak, peak_kind = load_peaks()
+    achieved = kern_bytes / kern_avg_s / 1e9
+
+    # end to end through the public API: pinned host input -> layer -> pinned host output
+    xh = torch.from_numpy(xs.view(np.int16)).view(torch.uint16).pin_memory()
+    oh = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16).pin_memory()
+    xd = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
+    e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K + W):
+        flush.zero_()
+        if i >= W:
+            e2e[i - W][0].record()
+        xd.copy_(xh[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1], non_blocking=True)
+        out = lay.forward(xd, xd, n_rows=1)
+        oh.copy_(out, non_blocking=True)
+        if i >= W:
+            e2e[i - W][1].record()
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * K * unique_bytes / (e2e_ms * 1e-3) / 1e9
+
+    blocks = {}
+    if not args.no_blocks:
+        blocks["1"] = {"us_median": statistics.median(layer_ms) * 1e3, "unique_experts": U,
+                       "gbs_unique": unique_bytes / statistics.median(layer_ms) / 1e6,
+                       "gbs_all_bytes": all_bytes / statistics.median(layer_ms) / 1e6,
+                       "routing": "router GEMV"}
+        for n in (8, 16):
+            blocks[str(n)] = time_blocks(torch, lay, X, flush, n, reps=max(5, min(K, 20)))
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 weights x f16 activations, fp32 accumulate, bf16 out", "data": "synthetic",
+        "config": {"workload": "Kimi K3.1 MoE layer decode, 1 row/step: d=7168 f=1536 E=896 top-16 + 2 Q8_0 "
+                               "shared, all experts resident, 100 seeded rows",
+                   "rows_per_step": 1, "l2": "flushed before every step (256 MB write), outside the events",
+                   "parallelism": f"replicas x{world}", "blocks_sigma0.5": blocks},
+        "layer_us_p10_p50_p90": [float(np.percentile(layer_ms, q)) * 1e3 for q in (10, 50, 90)],
+        "all_bytes_gbs": world * K * all_bytes / (total_ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "moe::expert_kernel", "peak_kind": peak_kind,
+                     "bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_s * 1e6},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
+                "d2h_bytes_per_step": syn.KIMI.d_model * 2},
+        "gpu_launches": K * 3,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    return line
+
+
+def time_blocks(torch, lay, X, flush, n, reps):
+    """Verification blocks of n rows: shared N(0,1) base logits + N(0, 0.5) per-row noise."""
+    ts, us = [], []
+    for b in range(reps + 3):
+        lg = torch.from_numpy(syn.block_logits(SEED, n, syn.KIMI.n_experts, 0.5, block=b)).to(X.device)
+        x = X[(b * n) % (N_ROWS_SEEDED - n): (b * n) % (N_ROWS_SEEDED - n) + n]
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        lay.forward(x, x, logits_in=lg)
+        e1.record()
+        torch.cuda.synchronize()
+        if b >= 3:
+            ts.append(e0.elapsed_time(e1))
+            us.append(int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item()))
+    t = statistics.median(ts)
+    u = statistics.mean(us)
+    allb = u * SLAB + 2 * Q8_SLAB + 3 * n * syn.KIMI.d_model * 2
+    return {"us_median": t * 1e3, "unique_experts": u, "gbs_unique": u * SLAB / t / 1e6,
+            "gbs_all_bytes": allb / t / 1e6, "routing": "caller logits"}
+
+
+def run_reference(args):
+    """The CPU oracle timed on this host's cores: each step is the oracle's expert MLP
+    of one (row, selected expert) pair of the workload (17,547,264 expert bytes)."""
+    K, W = args.steps, args.warmup
+    pairs = oracle_pairs(K + W)
+    secs = oracle_step_seconds(pairs)[W:]
+    total = sum(secs)
+    value = K * SLAB / total / 1e9
+    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else (os.cpu_count() or 1)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
+            "steps": K, "warmup": W, "ms_per_step": total / K * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "Kimi K3.1 MoE layer decode, 1 row/step (oracle sample)", "rows_per_step": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "one (row, selected expert) fp64 expert MLP per step"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-blocks", action="store_true")
+    ap.add_argument("--_oracle-sample", type=int, default=0, dest="oracle_sample")
+    args = ap.parse_args()
+
+    if args.oracle_sample:
+        print(json.dumps({"seconds": oracle_step_seconds(oracle_pairs(args.oracle_sample))}))
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) block-batched MXFP4 mixture-of-experts layer.
+ *
+ * The layer is the one described on "Run Kimi 3.1 locally on one GPU"
+ * (argonautlabs.ai): each MoE layer has 896 experts, 16 are selected per token
+ * (section "Read the experts the router needs"); experts are MXFP4, one
+ * 17,547,264-byte file per expert, and the rest of the model is Q8_0 (section
+ * "One GPU, three storage tiers"); a verification block of up to 16 rows reads
+ * each expert once for all its rows and its rows run the same arithmetic as
+ * plain single-row steps (section "A drafter that leaves the answer
+ * unchanged").  "Run Kimi K3 and K3.1 Pro Locally" (computingforgeeks.com),
+ * table in "Kimi K3 and K3.1 Pro in numbers", adds the 2 shared experts.
+ *
+ * One layer for a block of N rows is four calls on one stream:
+ *   moe_route         router GEMV (or caller logits), top-k, weights, grouping
+ *   moe_expert_block  every selected expert's SwiGLU MLP on its rows, each
+ *                     expert's weights streamed from HBM once per block, plus
+ *                     the shared Q8_0 experts
+ *   moe_combine       out = bf16(residual + sum_j w_j y_j + sum_s shared_s)
+ * and q8_0_block_matmul is the stand-alone Q8_0 N-row matmul.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every pointer argument is a DEVICE pointer unless it is documented as a
+ *   host pointer (descriptors and pools are host structs).
+ * - The caller owns every buffer.  No call allocates device memory.
+ * - Every compute call is asynchronous on the given stream (a cudaStream_t
+ *   passed as void*; NULL means the legacy default stream) and returns a
+ *   status.  Argument errors are detected on the host before any launch and
+ *   return MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED with nothing enqueued.
+ * - Device-side failures (a bounded wait that ran out, a NaN logit) never trap:
+ *   the kernel records a bit in the workspace's error word and finishes.  Read
+ *   and clear it with moe_get_error().
+ * - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef MOE_API
+#define MOE_API __attribute__((visibility("default")))
+#endif
+
+/* status codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1   /* NULL / misaligned pointer, bad size */
+#define MOE_ERR_UNSUPPORTED 2   /* shape, row count or device not supported */
+#define MOE_ERR_CUDA 3          /* a CUDA runtime call failed */
+#define MOE_ERR_TIMEOUT 4       /* device error word: a bounded wait ran out */
+#define MOE_ERR_NAN 5           /* device error word: a NaN logit was seen */
+
+/* bits of the device error word returned by moe_get_error */
+#define MOE_EBIT_TIMEOUT 0x1u
+#define MOE_EBIT_NAN 0x2u
+#define MOE_EBIT_BAD_SLOT 0x4u
+
+/* moe_expert_block modes */
+#define MOE_MODE_DECODE 0       /* N <= 16: one arithmetic path for every N (row results
+                                   do not depend on the other rows of the block) */
+#define MOE_MODE_PREFILL 1      /* any N: block-scaled tensor-core path */
+#define MOE_MODE_DEBUG_GU 0x100 /* also write g and u (before SwiGLU) to the workspace */
+
+/* weight formats of a pool */
+#define MOE_FMT_MXFP4 0
+#define MOE_FMT_Q8_0 1
+
+/* q8_0_block_matmul epilogues and input types */
+#define MOE_EPI_NONE 0          /* y  = x W^T */
+#define MOE_EPI_ACCUM 1         /* y += x W^T */
+#define MOE_EPI_SWIGLU 2        /* y  = silu(x Wg^T) * (x Wu^T) */
+#define MOE_DTYPE_BF16 0
+#define MOE_DTYPE_F32 1
+
+/*
+ * Layer shape.  d_model = hidden size d, d_ff = expert width f, n_experts = E
+ * routed experts, top_k = k experts per row, group = elements per scale.
+ * Kimi K3.1: {7168, 1536, 896, 16, 32}.  Requirements: group == 32,
+ * 1 <= top_k <= min(n_experts, 32), n_experts <= 1024, d_model % 256 == 0,
+ * d_ff % 64 == 0, d_model % 64 == 0.
+ */
+typedef struct moe_desc {
+    int32_t d_model;
+    int32_t d_ff;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t group;
+} moe_desc;
+
+/*
+ * Expert slabs resident in ONE device allocation (host struct).
+ *
+ * Slot s starts at base + s * slot_bytes.  A slab is the expert's three
+ * matrices in this order: gate [f][d], up [f][d], down [d][f], each stored as
+ * its codes plane followed by its scales plane:
+ *   MXFP4: codes [rows][K/2] bytes, two E2M1 codes per byte, the even-K element
+ *          in the low nibble; scales [rows][K/32] E8M0 bytes (2^(s-127)).
+ *          One slab is 3*d*f*(1/2 + 1/32) bytes (17,547,264 at d=7168, f=1536,
+ *          the expert file size on "Run Kimi 3.1 locally on one GPU").
+ *   Q8_0:  codes [rows][K] int8; scales [rows][K/32] fp16; 3*d*f*(1 + 2/32) bytes.
+ * base must be 32-byte aligned and slot_bytes a multiple of 32 that is at
+ * least the slab size.  The pool is read through TMA tensor maps that the
+ * library encodes on the host from these fields.
+ */
+typedef struct moe_pool {
+    const void* base;
+    int64_t slot_bytes;
+    int32_t n_slots;
+    int32_t format;
+} moe_pool;
+
+/* Bytes of one slab of the given format for this shape. */
+MOE_API size_t moe_slab_bytes(const moe_desc* desc, int32_t format);
+
+/*
+ * Workspace.  moe_workspace_size() gives the bytes a workspace for blocks of
+ * up to n_rows_max rows needs (n_shared shared experts).  The caller
+ * allocates it (256-byte aligned) and must zero it once before first use
+ * (cudaMemset 0); the kernels leave it in that state after every layer.  A
+ * workspace serves one layer at a time: layers that run concurrently need
+ * their own.  The layout is opaque; moe_workspace_offsets() exposes the
+ * parts tests inspect.
+ */
+MOE_API size_t moe_workspace_size(const moe_desc* desc, int32_t n_rows_max, int32_t n_shared);
+
+typedef struct moe_ws_offsets {
+    int64_t error_word;   /* uint32 */
+    int64_t n_unique;     /* int32 U */
+    int64_t uexp;         /* int32 [U] selected experts, ascending */
+    int64_t off;          /* int32 [U+1] */
+    int64_t pair;         /* int32 [N*k] row*k + slot, grouped by expert */
+    int64_t dbg_g;        /* float [pairs][f] gate projection (MOE_MODE_DEBUG_GU) */
+    int64_t dbg_u;        /* float [pairs][f] up projection   (MOE_MODE_DEBUG_GU) */
+    int64_t h;            /* float [pairs][f] SwiGLU activations */
+    int64_t shared_y;     /* float [n_shared][N][d] shared-expert outputs */
+} moe_ws_offsets;
+
+MOE_API int moe_workspace_offsets(const moe_desc* desc, int32_t n_rows_max, int32_t n_shared,
+                          moe_ws_offsets* out /* host */);
+
+/*
+ * Routing (router GEMV -> top-k -> renormalised weights -> grouping).
+ *
+ * Pages: "Run Kimi 3.1 locally on one GPU", "Read the experts the router
+ * needs" (16 of 896 selected); the router is BF16 ("Run Kimi K3 and K3.1 Pro
+ * Locally", "Confirm the checkpoint format and size").  The routing function
+ * itself is not on the pages; this library takes the plainest reading:
+ *   logit[n][e] = sum_c x[n][c] * Wr[e][c]              (fp32 accumulate)
+ *   idx[n][0..k)  = the k largest logits, larger first, equal logits by lower
+ *                   index, NaN after every number (and MOE_EBIT_NAN is set)
+ *   w[n][j]       = exp(l_j - l_0) / sum_i exp(l_i - l_0)  (softmax over the
+ *                   selected k, i.e. softmax then renormalise; fp32)
+ * and groups the block's (row, slot) pairs by expert for moe_expert_block.
+ *
+ *  n_rows      1..n_rows_max of the workspace; the GEMV path needs n_rows <= 32
+ *  x           bf16 [n_rows][d] activations, row-major; may be NULL only when
+ *              logits_in is given and no moe_expert_block call follows
+ *  w_router    bf16 [E][d] router matrix, row-major (ignored with logits_in)
+ *  logits_in   fp32 [n_rows][E] logits to route on instead of the GEMV, or NULL
+ *  logits_out  fp32 [n_rows][E] receives the GEMV logits, or NULL
+ *  topk_idx    int32 [n_rows][k] selected experts in rank order (output)
+ *  topk_w      fp32 [n_rows][k] their weights (output)
+ *  ws          workspace (receives the grouping and prepared activations)
+ */
+MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
+              const uint16_t* x, const uint16_t* w_router,
+              const float* logits_in, float* logits_out,
+              int32_t* topk_idx, float* topk_w,
+              void* ws, int32_t n_rows_max, int32_t n_shared, void* stream);
+
+/*
+ * Every selected expert's SwiGLU MLP on the rows routed to it, plus the shared
+ * experts on every row.  Pages: MXFP4 experts ("Run Kimi 3.1 locally on one
+ * GPU", "One GPU, three storage tiers"), a block reads each expert once for
+ * all its rows ("A drafter that leaves the answer unchanged"):
+ *   g = x Wg^T, u = x Wu^T, h = silu(g) * u, y = h Wd^T   per (row, slot)
+ * Each expert's slab is streamed from HBM once per call.  Must follow
+ * moe_route on the same workspace and stream.
+ *
+ *  mode         MOE_MODE_DECODE (n_rows <= 16) or MOE_MODE_PREFILL, optionally
+ *               | MOE_MODE_DEBUG_GU
+ *  routed       pool holding the routed experts (host struct, MXFP4)
+ *  expert_slot  int32 [E] slot of each expert in `routed` (device)
+ *  slot_ready   uint32 [routed->n_slots] flags, or NULL when every slot is
+ *               resident: an expert's slab is read only after its flag is
+ *               non-zero (bounded wait; MOE_EBIT_TIMEOUT when it runs out)
+ *  shared       pool of n_shared Q8_0 shared experts in slots 0..n_shared-1,
+ *               or NULL with n_shared == 0
+ *  y_part       fp32 [n_rows][k][d] output of each (row, slot)
+ *  The shared experts' outputs go to the workspace (moe_ws_offsets.shared_y).
+ */
+MOE_API int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mode,
+                     const moe_pool* routed, const int32_t* expert_slot,
+                     const uint32_t* slot_ready,
+                     const moe_pool* shared, int32_t n_shared,
+                     void* ws, int32_t n_rows_max, float* y_part, void* stream);
+
+/*
+ * Weighted combine into the residual, in a fixed order per element:
+ *   acc = 0; for j in 0..k-1: acc = fma(w[n][j], y[n][j][c], acc);
+ *   for s in 0..n_shared-1: acc += shared_y[s][n][c];
+ *   out[n][c] = bf16_rne(residual[n][c] + acc)
+ *  residual  bf16 [n_rows][d];  y_part fp32 [n_rows][k][d];  topk_w fp32 [n_rows][k]
+ *  shared_y  fp32 [n_shared][n_rows][d] or NULL;  out bf16 [n_rows][d]
+ */
+MOE_API int moe_combine(const moe_desc* desc, int32_t n_rows, const uint16_t* residual,
+                const float* y_part, const float* topk_w,
+                const float* shared_y, int32_t n_shared,
+                uint16_t* out, void* stream);
+
+/*
+ * Stand-alone Q8_0 matmul of an N-row block: every weight is loaded from HBM
+ * once for all rows ("Run Kimi 3.1 locally on one GPU": the spine's matrix
+ * multiplies load each weight once for up to eight rows).  W[o][c] = q[o][c] *
+ * fp16(d[o][c/32]).
+ *  n_rows 1..16; k_in % 256 == 0; n_out % 64 == 0
+ *  x       [n_rows][k_in], bf16 (x_dtype MOE_DTYPE_BF16) or fp32 (MOE_DTYPE_F32)
+ *  q, d    int8 [n_out][k_in] and fp16 [n_out][k_in/32]; 32-byte aligned
+ *  q2, d2  the up matrix for MOE_EPI_SWIGLU (same shape), else NULL
+ *  y       fp32 [n_rows][n_out]
+ *  ws      scratch of q8_0_workspace_size() bytes, zeroed once before first use
+ * MOE_EPI_SWIGLU requires bf16 x.
+ */
+MOE_API size_t q8_0_workspace_size(int32_t n_rows, int32_t k_in, int32_t n_out);
+MOE_API int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out,
+                      const void* x, int32_t x_dtype,
+                      const int8_t* q, const uint16_t* d,
+                      const int8_t* q2, const uint16_t* d2,
+                      int32_t epilogue, float* y, void* ws, void* stream);
+
+/*
+ * Reads the workspace's device error word (synchronising `stream`), clears it,
+ * and returns it through *bits (host).  Returns MOE_OK, or MOE_ERR_CUDA.
+ */
+MOE_API int moe_get_error(void* ws, void* stream, uint32_t* bits);
+
+/* Number of SMs the persistent kernels size their grids for (0 if no device). */
+MOE_API int32_t moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,179 @@
+"""Thin ctypes binding of the C ABI in ``include/moe.h``.
+
+Argument marshalling only: every function here takes torch tensors (or raw
+device pointers as ints, or None) and forwards their addresses to the function
+of the same name in ``_moe_gb300.so``.  All arithmetic happens in the CUDA
+kernels.  There is no CPU fallback: if the library is missing, every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_EBIT_TIMEOUT = 0x1
+MOE_EBIT_NAN = 0x2
+MOE_EBIT_BAD_SLOT = 0x4
+MOE_MODE_DECODE = 0
+MOE_MODE_PREFILL = 1
+MOE_MODE_DEBUG_GU = 0x100
+MOE_FMT_MXFP4 = 0
+MOE_FMT_Q8_0 = 1
+MOE_EPI_NONE = 0
+MOE_EPI_ACCUM = 1
+MOE_EPI_SWIGLU = 2
+MOE_DTYPE_BF16 = 0
+MOE_DTYPE_F32 = 1
+
+EXPORTED = [
+    "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
+    "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
+]
+
+
+class MoeDesc(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("n_experts", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("group", ctypes.c_int32)]
+
+
+class MoePool(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("slot_bytes", ctypes.c_int64), ("n_slots", ctypes.c_int32),
+                ("format", ctypes.c_int32)]
+
+
+class MoeWsOffsets(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in
+                ("error_word", "n_unique", "uexp", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y")]
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise MoeError("CUDA library not built: call __graft_entry__.build() or "
+                           "python -m mxfp4_mixture_experts_router_gb300.build")
+        L = ctypes.CDLL(_build.LIB)
+        P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(MoeDesc)
+        PL = ctypes.POINTER(MoePool)
+        L.moe_slab_bytes.argtypes = [D, I32]
+        L.moe_slab_bytes.restype = SZ
+        L.moe_workspace_size.argtypes = [D, I32, I32]
+        L.moe_workspace_size.restype = SZ
+        L.moe_workspace_offsets.argtypes = [D, I32, I32, ctypes.POINTER(MoeWsOffsets)]
+        L.moe_route.argtypes = [D, I32, P, P, P, P, P, P, P, I32, I32, P]
+        L.moe_expert_block.argtypes = [D, I32, I32, PL, P, P, PL, I32, P, I32, P, P]
+        L.moe_combine.argtypes = [D, I32, P, P, P, P, I32, P, P]
+        L.q8_0_workspace_size.argtypes = [I32, I32, I32]
+        L.q8_0_workspace_size.restype = SZ
+        L.q8_0_block_matmul.argtypes = [I32, I32, I32, P, I32, P, P, P, P, I32, P, P, P]
+        L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+        L.moe_device_sm_count.restype = I32
+        _LIB = L
+    return _LIB
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(f"{what} failed with status {status}")
+
+
+def desc(d_model: int, d_ff: int, n_experts: int, top_k: int, group: int = 32) -> MoeDesc:
+    return MoeDesc(d_model, d_ff, n_experts, top_k, group)
+
+
+def pool(base, slot_bytes: int, n_slots: int, fmt: int) -> MoePool:
+    return MoePool(_ptr(base), slot_bytes, n_slots, fmt)
+
+
+def moe_slab_bytes(d: MoeDesc, fmt: int) -> int:
+    return lib().moe_slab_bytes(ctypes.byref(d), fmt)
+
+
+def moe_workspace_size(d: MoeDesc, n_rows_max: int, n_shared: int) -> int:
+    return lib().moe_workspace_size(ctypes.byref(d), n_rows_max, n_shared)
+
+
+def moe_workspace_offsets(d: MoeDesc, n_rows_max: int, n_shared: int) -> MoeWsOffsets:
+    o = MoeWsOffsets()
+    _check(lib().moe_workspace_offsets(ctypes.byref(d), n_rows_max, n_shared, ctypes.byref(o)),
+           "moe_workspace_offsets")
+    return o
+
+
+def moe_route(d: MoeDesc, n_rows: int, x, w_router, logits_in, logits_out, topk_idx, topk_w, ws,
+              n_rows_max: int, n_shared: int, stream=None):
+    _check(lib().moe_route(ctypes.byref(d), n_rows, _ptr(x), _ptr(w_router), _ptr(logits_in),
+                           _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), n_rows_max,
+                           n_shared, _stream(stream)), "moe_route")
+
+
+def moe_expert_block(d: MoeDesc, n_rows: int, mode: int, routed: MoePool, expert_slot, slot_ready,
+                     shared: MoePool | None, n_shared: int, ws, n_rows_max: int, y_part, stream=None):
+    _check(lib().moe_expert_block(ctypes.byref(d), n_rows, mode, ctypes.byref(routed), _ptr(expert_slot),
+                                  _ptr(slot_ready), ctypes.byref(shared) if shared is not None else None,
+                                  n_shared, _ptr(ws), n_rows_max, _ptr(y_part), _stream(stream)),
+           "moe_expert_block")
+
+
+def moe_combine(d: MoeDesc, n_rows: int, residual, y_part, topk_w, shared_y, n_shared: int, out,
+                stream=None):
+    _check(lib().moe_combine(ctypes.byref(d), n_rows, _ptr(residual), _ptr(y_part), _ptr(topk_w),
+                             _ptr(shared_y), n_shared, _ptr(out), _stream(stream)), "moe_combine")
+
+
+def q8_0_workspace_size(n_rows: int, k_in: int, n_out: int) -> int:
+    return lib().q8_0_workspace_size(n_rows, k_in, n_out)
+
+
+def q8_0_block_matmul(n_rows: int, k_in: int, n_out: int, x, x_dtype: int, q, dq, q2, d2, epilogue: int,
+                      y, ws, stream=None):
+    _check(lib().q8_0_block_matmul(n_rows, k_in, n_out, _ptr(x), x_dtype, _ptr(q), _ptr(dq), _ptr(q2),
+                                   _ptr(d2), epilogue, _ptr(y), _ptr(ws), _stream(stream)),
+           "q8_0_block_matmul")
+
+
+def moe_get_error(ws, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(lib().moe_get_error(_ptr(ws), _stream(stream), ctypes.byref(bits)), "moe_get_error")
+    return bits.value
+
+
+def moe_device_sm_count() -> int:
+    return lib().moe_device_sm_count()

@@ -1,0 +1,243 @@
+// Internal helpers of the GB300 MoE library: inline PTX wrappers (mbarrier, TMA,
+// tensor-core MMA, E2M1 conversion), bounded waits, and the workspace layout.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// workspace layout (shared by host and device code)
+// ---------------------------------------------------------------------------
+
+// control words at the start of the workspace
+enum Ctrl : int {
+    CTRL_ERROR = 0,      // device error word (MOE_EBIT_*)
+    CTRL_WORK = 1,       // next work item of the expert kernel
+    CTRL_EXIT = 2,       // CTAs of the expert kernel that finished
+    CTRL_TICKET = 3,     // CTAs of the route kernel that finished
+    CTRL_UNIQUE = 4,     // U: experts selected by the block
+    CTRL_ROWS = 5,       // rows of the routed block
+    CTRL_WORDS = 64
+};
+
+struct WsLayout {
+    size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
+        total;
+    int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shared) {
+    WsLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    const int64_t N = n_rows_max;
+    L.pairs = (int64_t)n_shared * N + N * k;
+    const int64_t V = n_shared + (N * k < E ? N * k : E);
+    L.ctrl = take(CTRL_WORDS * 4);
+    L.uexp = take((size_t)E * 4);
+    L.off = take((size_t)(E + 1) * 4);
+    L.pair = take((size_t)N * k * 4);
+    L.x16 = take((size_t)N * d * 2);
+    L.xexp = take((size_t)N * 4);
+    L.gu_done = take((size_t)V * 4);
+    L.hmax = take((size_t)L.pairs * 4);
+    L.h = take((size_t)L.pairs * f * 4);
+    L.dbg_g = take((size_t)L.pairs * f * 4);
+    L.dbg_u = take((size_t)L.pairs * f * 4);
+    L.shared_y = take((size_t)n_shared * N * d * 4);
+    L.logits = take((size_t)N * E * 4);
+    L.total = o;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+
+// Upper bound of every spin in device code: 2 s of %globaltimer.
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void set_error(uint32_t* ctrl, uint32_t bits) {
+    atomicOr(ctrl + CTRL_ERROR, bits);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ bool timed_out(const uint32_t* ctrl) {
+    return (ld_acquire(ctrl + CTRL_ERROR) & MOE_EBIT_TIMEOUT) != 0u;
+}
+
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// --- mbarrier ---------------------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits until the phase with the given parity of `bar` has completed; gives up
+// after WAIT_LIMIT_NS and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_test(bar, parity)) return true;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+
+// --- TMA ------------------------------------------------------------------
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
+                                            int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// --- named barrier among the consumer warps -------------------------------
+
+template <int NTHREADS>
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(NTHREADS) : "memory");
+}
+
+// --- numeric conversions ----------------------------------------------------
+
+// Two E2M1 codes (one byte, even element in the low nibble) -> f16x2 (low half = even).
+// The conversion is exact: every E2M1 value is an f16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& d0, uint32_t& d1, uint32_t& d2,
+                                                uint32_t& d3) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "  mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "  cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "  cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "  cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "  cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+        : "r"(w));
+}
+
+// Four int8 values -> two f16x2 (exact): place (v + 128) in the mantissa of
+// 1024.0 and subtract 1152.
+__device__ __forceinline__ void s8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t t = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(t), "r"(0x64646464u), "r"(0x4140u));
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(t), "r"(0x64646464u), "r"(0x4342u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+}
+
+// E8M0 scale byte -> 2^(s-127) as fp32 (s = 0 is the subnormal 2^-127, 255 is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+    uint32_t b = s << 23;
+    b = (s == 0u) ? 0x00400000u : b;
+    b = (s == 255u) ? 0x7fc00000u : b;
+    return __uint_as_float(b);
+}
+
+// 2^e as fp32 for e in [-126, 127].
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// Scale exponent p for a row whose largest magnitude has bit pattern `maxbits`:
+// max * 2^-p lands in [2^14, 2^15), inside the f16 range with room for rounding.
+__device__ __forceinline__ int f16_scale_exponent(uint32_t maxbits) {
+    if (maxbits == 0u) return 0;
+    int e = (int)((maxbits >> 23) & 0xFFu) - 127;
+    int p = e - 14;
+    p = p < -100 ? -100 : p;
+    p = p > 100 ? 100 : p;
+    return p;
+}
+
+// D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds8(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds16(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+}  // namespace moe

@@ -1,0 +1,939 @@
+// Expert contractions of a block: every selected expert's SwiGLU MLP on the
+// rows routed to it, the shared experts on every row, and the stand-alone Q8_0
+// block matmul, all through one persistent kernel.
+//
+// Pages: "Run Kimi 3.1 locally on one GPU": MXFP4 experts, one file per expert
+// (section "One GPU, three storage tiers"); a block reads each expert once for
+// all its rows, and its rows run the same arithmetic as plain steps (section
+// "A drafter that leaves the answer unchanged").  The spine (here: the shared
+// experts) is Q8_0 and its matmuls load each weight once for all rows.
+//
+// Design (GB300):
+// * One CTA per SM, 8 consumer warps + 1 producer warp.  The producer claims
+//   work items from a global counter in order, and streams each item's weight
+//   tiles HBM -> shared memory with TMA (3-D tensor maps over the slab pool,
+//   128-byte swizzle) into an 8-stage mbarrier ring.  Every weight byte of a
+//   block is read from HBM exactly once.
+// * Work items: gate/up items (16 output rows of both matrices, full K) and
+//   down items (64 output rows, full K).  Items are ordered gate/up of expert
+//   v, then down of expert v-2, so a down item rarely waits; it waits (bounded)
+//   on a per-expert counter of finished gate/up items.
+// * Consumers convert E2M1 codes to f16 with cvt.rn.f16x2.e2m1x2 (exact) and
+//   int8 with a mantissa trick (exact), and multiply with warp-level tensor-core
+//   MMAs (m16n8k16, fp32 accumulate) against the block's rows: x pre-scaled to
+//   f16 by a power of two, h split into f16 hi + lo parts.  Each K group of 32
+//   forms its own MMA partial, which is then scaled by that group's E8M0 or
+//   fp16 scale, so the weights enter exactly.
+// * A row's arithmetic never depends on the other rows of the block: K is
+//   always reduced in the same order, the row's tensor-core column does not
+//   change its result, and scale exponents are per row.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int EX_CW = 8;                      // consumer warps
+constexpr int EX_CT = EX_CW * 32;             // consumer threads
+constexpr int EX_THREADS = EX_CT + 32;        // + producer warp
+constexpr int EX_NST = 8;                     // ring stages
+constexpr int EX_CODE_BYTES = 16384;
+constexpr int EX_STAGE = 17408;               // codes + scales
+constexpr int EX_NT = 2;                      // n-tiles of 8 rows: up to 16 rows per expert
+constexpr int EX_RED_FLOATS = EX_CW * 4 * EX_NT * 4 * 32;
+constexpr size_t EX_SMEM = (size_t)EX_NST * EX_STAGE + EX_RED_FLOATS * 4 + 1024 + 1024;
+
+enum { IT_GU = 0, IT_DN = 1 };
+enum { J_LAYER = 0, J_Q8_SWIGLU = 1, J_Q8_PLAIN = 2 };
+
+struct Geom {
+    int row_bytes, bi, cb, nbox, sb, flat, chunks, gps, rows_item;
+    uint32_t tx;
+};
+
+struct ExParams {
+    CUtensorMap map[12];  // routed then shared: gate codes, gate scales, up codes, up scales, down codes, down scales
+    Geom geom[4];         // routed gate/up, routed down, shared gate/up, shared down
+    int job, fmt_routed, fmt_shared;
+    int k_gu, m_gu, k_dn, m_dn;
+    int top_k, n_rows, n_shared;
+    int n_gu, n_dn, lag;
+    int debug_gu, accum;
+    const int* expert_slot;
+    const uint32_t* slot_ready;
+    int n_slots;
+    uint32_t* ctrl;
+    const int* uexp;
+    const int* off;
+    const int* pair;
+    const __half* x16;
+    const int* xexp;
+    uint32_t* gu_done;
+    uint32_t* hmax;
+    float* h;
+    float* dbg_g;
+    float* dbg_u;
+    float* out_shared;
+    float* y_part;
+    int64_t pairs_cap;
+};
+
+struct Meta {
+    int item, type, v, blk, chunk, nchunks, slot, pad;
+};
+
+__device__ __forceinline__ void item_counts(const ExParams& p, bool& has_gu, bool& has_dn, int& lag) {
+    has_gu = p.job != J_Q8_PLAIN;
+    has_dn = p.job != J_Q8_SWIGLU;
+    lag = (has_gu && has_dn) ? p.lag : 0;
+}
+
+__device__ __forceinline__ int total_items(const ExParams& p, int V) {
+    bool g, d;
+    int lag;
+    item_counts(p, g, d, lag);
+    return V * ((g ? p.n_gu : 0) + (d ? p.n_dn : 0));
+}
+
+// Item order: round i holds the gate/up items of expert i, then the down items
+// of expert i - lag.
+__device__ void decode_item(const ExParams& p, int V, int item, int& type, int& v, int& blk) {
+    bool has_gu, has_dn;
+    int lag;
+    item_counts(p, has_gu, has_dn, lag);
+    int rest = item;
+    for (int i = 0; i < V + lag; i++) {
+        if (has_gu && i < V) {
+            if (rest < p.n_gu) {
+                type = IT_GU;
+                v = i;
+                blk = rest;
+                return;
+            }
+            rest -= p.n_gu;
+        }
+        const int vd = i - lag;
+        if (has_dn && vd >= 0 && vd < V) {
+            if (rest < p.n_dn) {
+                type = IT_DN;
+                v = vd;
+                blk = rest;
+                return;
+            }
+            rest -= p.n_dn;
+        }
+    }
+    type = IT_GU;
+    v = 0;
+    blk = 0;
+}
+
+// shared-memory address of the code bytes at byte offset `ob` of row `row`
+// inside a matrix region of `rows` rows laid out as TMA boxes of `bi` bytes.
+__device__ __forceinline__ uint32_t code_addr(uint32_t base, const Geom& g, int rows, int row, int ob) {
+    const int box = ob / g.bi;
+    const int in = ob - box * g.bi;
+    const int swm = (g.bi == 128) ? 7 : 0;
+    return base + (uint32_t)(box * g.bi * rows + row * g.bi + ((((in >> 4) ^ (row & swm)) << 4) | (in & 15)));
+}
+
+// A-fragment words of rows r0 (= lane/4) and r1 (= r0+8) for this thread's 8
+// K values of group q: four f16x2 for the first MMA of the group, four for the second.
+template <int FMT>
+__device__ __forceinline__ void load_a(uint32_t cbase, const Geom& g, int rows, int r0, int r1, int q, int i,
+                                       uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+    if (FMT == MOE_FMT_MXFP4) {
+        const int ob = 16 * q + 4 * i;
+        const uint32_t w0 = lds32(code_addr(cbase, g, rows, r0, ob));
+        const uint32_t w1 = lds32(code_addr(cbase, g, rows, r1, ob));
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        e2m1x8_to_f16x2(w0, x0, x1, x2, x3);
+        e2m1x8_to_f16x2(w1, y0, y1, y2, y3);
+        a0[0] = x0; a0[1] = y0; a0[2] = x1; a0[3] = y1;
+        a1[0] = x2; a1[1] = y2; a1[2] = x3; a1[3] = y3;
+    } else {
+        const int ob = 32 * q + 8 * i;
+        const uint2 w0 = lds64(code_addr(cbase, g, rows, r0, ob));
+        const uint2 w1 = lds64(code_addr(cbase, g, rows, r1, ob));
+        uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+        s8x4_to_f16x2(w0.x, x0, x1);
+        s8x4_to_f16x2(w0.y, x2, x3);
+        s8x4_to_f16x2(w1.x, y0, y1);
+        s8x4_to_f16x2(w1.y, y2, y3);
+        a0[0] = x0; a0[1] = y0; a0[2] = x1; a0[3] = y1;
+        a1[0] = x2; a1[1] = y2; a1[2] = x3; a1[3] = y3;
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ float load_scale(uint32_t sbase, const Geom& g, int row, int q) {
+    if (FMT == MOE_FMT_MXFP4) return e8m0_to_f32(lds8(sbase + row * g.sb + q));
+    return __half2float(__ushort_as_half((unsigned short)lds16(sbase + row * g.sb + 2 * q)));
+}
+
+__device__ __forceinline__ void fma4(float (&acc)[4], float s0, float s1, const float (&pp)[4]) {
+    acc[0] = fmaf(s0, pp[0], acc[0]);
+    acc[1] = fmaf(s0, pp[1], acc[1]);
+    acc[2] = fmaf(s1, pp[2], acc[2]);
+    acc[3] = fmaf(s1, pp[3], acc[3]);
+}
+
+// one stage of a gate/up item
+template <int FMT>
+__device__ __forceinline__ void gu_stage(uint32_t st, const Geom& g, int chunk, int cw, int lane, int NT,
+                                         const __half* const (&xrow)[EX_NT], const bool (&bval)[EX_NT],
+                                         float (&ag)[EX_NT][4], float (&au)[EX_NT][4]) {
+    const int gq = lane >> 2, i = lane & 3;
+    const uint32_t gateC = st, upC = st + g.nbox * g.bi * 16;
+    const uint32_t gateS = st + EX_CODE_BYTES, upS = st + EX_CODE_BYTES + 512;
+    for (int q = cw; q < g.gps; q += EX_CW) {
+        const int kk = (chunk * g.gps + q) * 32 + 8 * i;
+        uint4 bx[EX_NT];
+#pragma unroll
+        for (int nt = 0; nt < EX_NT; nt++) {
+            bx[nt] = make_uint4(0, 0, 0, 0);
+            if (nt < NT && bval[nt]) bx[nt] = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + kk));
+        }
+        uint32_t g0[4], g1[4], u0[4], u1[4];
+        load_a<FMT>(gateC, g, 16, gq, gq + 8, q, i, g0, g1);
+        load_a<FMT>(upC, g, 16, gq, gq + 8, q, i, u0, u1);
+        const float sg0 = load_scale<FMT>(gateS, g, gq, q), sg1 = load_scale<FMT>(gateS, g, gq + 8, q);
+        const float su0 = load_scale<FMT>(upS, g, gq, q), su1 = load_scale<FMT>(upS, g, gq + 8, q);
+#pragma unroll
+        for (int nt = 0; nt < EX_NT; nt++) {
+            if (nt < NT) {
+                float pg[4] = {0.f, 0.f, 0.f, 0.f}, pu[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(pg, g0[0], g0[1], g0[2], g0[3], bx[nt].x, bx[nt].y);
+                mma_f16(pg, g1[0], g1[1], g1[2], g1[3], bx[nt].z, bx[nt].w);
+                mma_f16(pu, u0[0], u0[1], u0[2], u0[3], bx[nt].x, bx[nt].y);
+                mma_f16(pu, u1[0], u1[1], u1[2], u1[3], bx[nt].z, bx[nt].w);
+                fma4(ag[nt], sg0, sg1, pg);
+                fma4(au[nt], su0, su1, pu);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// one stage of a down item (4 M-tiles of 16 rows)
+template <int FMT>
+__device__ __forceinline__ void dn_stage(uint32_t st, const Geom& g, int chunk, int cw, int lane, int NT,
+                                         const float* const (&hrow)[EX_NT], const float (&hs)[EX_NT],
+                                         const bool (&bval)[EX_NT], float (&acc)[4][EX_NT][4]) {
+    const int gq = lane >> 2, i = lane & 3;
+    const uint32_t C = st, S = st + EX_CODE_BYTES;
+    for (int q = cw; q < g.gps; q += EX_CW) {
+        const int kk = (chunk * g.gps + q) * 32 + 8 * i;
+        uint32_t hi[EX_NT][4], lo[EX_NT][4];
+#pragma unroll
+        for (int nt = 0; nt < EX_NT; nt++) {
+#pragma unroll
+            for (int t = 0; t < 4; t++) hi[nt][t] = lo[nt][t] = 0u;
+            if (nt < NT && bval[nt]) {
+                const float4 va = __ldcg(reinterpret_cast<const float4*>(hrow[nt] + kk));
+                const float4 vb = __ldcg(reinterpret_cast<const float4*>(hrow[nt] + kk + 4));
+                const float v[8] = {va.x * hs[nt], va.y * hs[nt], va.z * hs[nt], va.w * hs[nt],
+                                    vb.x * hs[nt], vb.y * hs[nt], vb.z * hs[nt], vb.w * hs[nt]};
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    const __half2 hh = __floats2half2_rn(v[2 * t], v[2 * t + 1]);
+                    const float2 back = __half22float2(hh);
+                    hi[nt][t] = *reinterpret_cast<const uint32_t*>(&hh);
+                    lo[nt][t] = pack_h2(v[2 * t] - back.x, v[2 * t + 1] - back.y);
+                }
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            const int r0 = mt * 16 + gq, r1 = r0 + 8;
+            uint32_t a0[4], a1[4];
+            load_a<FMT>(C, g, 64, r0, r1, q, i, a0, a1);
+            const float s0 = load_scale<FMT>(S, g, r0, q), s1 = load_scale<FMT>(S, g, r1, q);
+#pragma unroll
+            for (int nt = 0; nt < EX_NT; nt++) {
+                if (nt < NT) {
+                    float pp[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_f16(pp, a0[0], a0[1], a0[2], a0[3], hi[nt][0], hi[nt][1]);
+                    mma_f16(pp, a1[0], a1[1], a1[2], a1[3], hi[nt][2], hi[nt][3]);
+                    mma_f16(pp, a0[0], a0[1], a0[2], a0[3], lo[nt][0], lo[nt][1]);
+                    mma_f16(pp, a1[0], a1[1], a1[2], a1[3], lo[nt][2], lo[nt][3]);
+                    fma4(acc[mt][nt], s0, s1, pp);
+                }
+            }
+        }
+    }
+}
+
+// the block rows behind pair column `col` of expert v
+struct ItemCtx {
+    int v, r, NT, pb, u_off;
+    bool shared;
+};
+
+__device__ __forceinline__ int pair_row(const ExParams& p, const ItemCtx& c, int col) {
+    return c.shared ? col : __ldg(p.pair + c.u_off + col) / p.top_k;
+}
+
+// ---------------------------------------------------------------------------
+
+__device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t* full, uint64_t* empty,
+                         Meta* meta) {
+    for (int m = 0; m < 12; m++) tma_prefetch_desc(&p.map[m]);
+    const int S = p.n_shared;
+    const int total = total_items(p, V);
+    uint32_t stage = 0, phase = 0;
+    uint32_t pending = 0, pending_par = 0;  // stages with copies not yet known to be consumed
+    bool ok = true;
+    while (ok) {
+        const int item = (int)atomicAdd(p.ctrl + CTRL_WORK, 1u);
+        if (item >= total) break;
+        int type, v, blk;
+        decode_item(p, V, item, type, v, blk);
+        const bool shared = v < S;
+        const Geom& G = p.geom[(shared ? 2 : 0) + type];
+        const CUtensorMap* mp = &p.map[shared ? 6 : 0];
+        int z = v;
+        if (!shared) {
+            const int e = __ldg(p.uexp + (v - S));
+            z = __ldg(p.expert_slot + e);
+            if (z < 0 || z >= p.n_slots) {
+                set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
+                z = 0;
+            }
+            if (p.slot_ready != nullptr && ld_acquire(p.slot_ready + z) == 0u) {
+                const uint64_t t0 = global_ns();
+                while (ld_acquire(p.slot_ready + z) == 0u) {
+                    // once any wait of this launch has run out, later ones give up at once
+                    if (timed_out(p.ctrl)) break;
+                    if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                        set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+            }
+        }
+        const int row0 = blk * G.rows_item;
+        for (int c = 0; c < G.chunks; c++) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            pending &= ~(1u << stage);
+            Meta& mt = meta[stage];
+            mt.item = item;
+            mt.type = type;
+            mt.v = v;
+            mt.blk = blk;
+            mt.chunk = c;
+            mt.nchunks = G.chunks;
+            mt.slot = z;
+            mbar_arrive_expect_tx(&full[stage], G.tx);
+            unsigned char* st = ring + (size_t)stage * EX_STAGE;
+            if (type == IT_GU) {
+                for (int m = 0; m < 2; m++) {
+                    for (int b = 0; b < G.nbox; b++)
+                        tma_load_3d(st + m * G.nbox * G.bi * 16 + b * G.bi * 16, mp + 2 * m, &full[stage],
+                                    c * G.cb + b * G.bi, row0, z);
+                    if (G.flat)
+                        tma_load_3d(st + EX_CODE_BYTES + m * 512, mp + 2 * m + 1, &full[stage], 0,
+                                    row0 * G.sb / 16, z);
+                    else
+                        tma_load_3d(st + EX_CODE_BYTES + m * 512, mp + 2 * m + 1, &full[stage], c * G.sb, row0, z);
+                }
+            } else {
+                for (int b = 0; b < G.nbox; b++)
+                    tma_load_3d(st + b * G.bi * 64, mp + 4, &full[stage], c * G.cb + b * G.bi, row0, z);
+                if (G.flat)
+                    tma_load_3d(st + EX_CODE_BYTES, mp + 5, &full[stage], 0, row0 * G.sb / 16, z);
+                else
+                    tma_load_3d(st + EX_CODE_BYTES, mp + 5, &full[stage], c * G.sb, row0, z);
+            }
+            pending |= 1u << stage;
+            pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
+            if (++stage == EX_NST) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (ok) {
+        if (mbar_wait(&empty[stage], phase ^ 1u)) {
+            pending &= ~(1u << stage);
+            meta[stage].item = -1;
+            mbar_arrive(&full[stage]);
+        } else {
+            set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+        }
+    }
+    // never leave the CTA with copies in flight
+    for (int s = 0; s < EX_NST; s++)
+        if (pending & (1u << s)) mbar_wait(&full[s], (pending_par >> s) & 1u);
+}
+
+template <int FR, int FS>
+__device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* red, uint64_t* full,
+                         uint64_t* empty, const Meta* meta) {
+    const int tid = threadIdx.x, cw = tid >> 5, lane = tid & 31;
+    const int S = p.n_shared, N = p.n_rows;
+    uint32_t stage = 0, phase = 0;
+    ItemCtx c{};
+    const __half* xrow[EX_NT];
+    const float* hrow[EX_NT];
+    float hs[EX_NT];
+    bool bval[EX_NT];
+    float ag[EX_NT][4], au[EX_NT][4];
+    float acc[4][EX_NT][4];
+    int type = IT_GU, blk = 0;
+
+    while (true) {
+        if (!mbar_wait(&full[stage], phase)) {
+            if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+            break;
+        }
+        const Meta m = meta[stage];
+        if (m.item < 0) break;
+        if (m.chunk == 0) {
+            type = m.type;
+            blk = m.blk;
+            c.v = m.v;
+            c.shared = m.v < S;
+            if (c.shared) {
+                c.r = N;
+                c.pb = m.v * N;
+                c.u_off = 0;
+            } else {
+                const int u = m.v - S;
+                const int o0 = __ldg(p.off + u), o1 = __ldg(p.off + u + 1);
+                c.r = o1 - o0;
+                c.pb = S * N + o0;
+                c.u_off = o0;
+            }
+            c.NT = (c.r + 7) >> 3;
+            if (c.NT > EX_NT) {
+                if (lane == 0) set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
+                c.NT = EX_NT;
+            }
+#pragma unroll
+            for (int nt = 0; nt < EX_NT; nt++) {
+                const int col = nt * 8 + (lane >> 2);
+                bval[nt] = col < c.r;
+                xrow[nt] = p.x16;
+                hrow[nt] = p.h;
+                hs[nt] = 1.f;
+                if (bval[nt]) {
+                    if (type == IT_GU) {
+                        xrow[nt] = p.x16 + (size_t)pair_row(p, c, col) * p.k_gu;
+                    } else {
+                        hrow[nt] = p.h + (size_t)(c.pb + col) * p.k_dn;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    ag[nt][t] = au[nt][t] = 0.f;
+#pragma unroll
+                    for (int mt = 0; mt < 4; mt++) acc[mt][nt][t] = 0.f;
+                }
+            }
+            if (type == IT_DN) {
+                if (p.job == J_LAYER) {
+                    // the expert's gate/up items must be complete (bounded wait)
+                    if (tid == 0 && ld_acquire(p.gu_done + c.v) < (uint32_t)p.n_gu) {
+                        const uint64_t t0 = global_ns();
+                        while (ld_acquire(p.gu_done + c.v) < (uint32_t)p.n_gu) {
+                            if (timed_out(p.ctrl)) break;
+                            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                                set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                                break;
+                            }
+                            __nanosleep(128);
+                        }
+                    }
+                    consumer_sync<EX_CT>();
+                }
+#pragma unroll
+                for (int nt = 0; nt < EX_NT; nt++)
+                    if (bval[nt]) hs[nt] = exp2i(-f16_scale_exponent(__ldcg(p.hmax + c.pb + nt * 8 + (lane >> 2))));
+            }
+        }
+        const uint32_t st = smem_u32(ring + (size_t)stage * EX_STAGE);
+        if (type == IT_GU) {
+            if (c.shared)
+                gu_stage<FS>(st, p.geom[2], m.chunk, cw, lane, c.NT, xrow, bval, ag, au);
+            else
+                gu_stage<FR>(st, p.geom[0], m.chunk, cw, lane, c.NT, xrow, bval, ag, au);
+        } else {
+            if (c.shared)
+                dn_stage<FS>(st, p.geom[3], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
+            else
+                dn_stage<FR>(st, p.geom[1], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == EX_NST) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        if (m.chunk != m.nchunks - 1) continue;
+
+        // ---- item epilogue: fixed-order reduction over the consumer warps ----
+        consumer_sync<EX_CT>();
+        if (type == IT_GU) {
+#pragma unroll
+            for (int nt = 0; nt < EX_NT; nt++)
+#pragma unroll
+                for (int t = 0; t < 4; t++) {
+                    red[((cw * 2 + 0) * EX_NT + nt) * 128 + t * 32 + lane] = ag[nt][t];
+                    red[((cw * 2 + 1) * EX_NT + nt) * 128 + t * 32 + lane] = au[nt][t];
+                }
+            consumer_sync<EX_CT>();
+            for (int idx = tid; idx < c.NT * 128; idx += EX_CT) {
+                const int nt = idx >> 7, t = (idx >> 5) & 3, ln = idx & 31;
+                float gs = 0.f, us = 0.f;
+                for (int w = 0; w < EX_CW; w++) {
+                    gs += red[((w * 2 + 0) * EX_NT + nt) * 128 + t * 32 + ln];
+                    us += red[((w * 2 + 1) * EX_NT + nt) * 128 + t * 32 + ln];
+                }
+                const int col = nt * 8 + 2 * (ln & 3) + (t & 1);
+                const int j = blk * 16 + (ln >> 2) + 8 * (t >> 1);
+                uint32_t amax = 0;
+                if (col < c.r) {
+                    const int row = pair_row(p, c, col);
+                    const float sc = exp2i(__ldg(p.xexp + row));
+                    gs *= sc;
+                    us *= sc;
+                    const float hv = gs / (1.f + expf(-gs)) * us;
+                    const size_t o = (size_t)(c.pb + col) * p.m_gu + j;
+                    p.h[o] = hv;
+                    if (p.debug_gu) {
+                        p.dbg_g[o] = gs;
+                        p.dbg_u[o] = us;
+                    }
+                    amax = __float_as_uint(hv) & 0x7FFFFFFFu;
+                }
+                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+                amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+                if (ln < 4 && col < c.r) atomicMax(p.hmax + c.pb + col, amax);
+            }
+            __threadfence();
+            consumer_sync<EX_CT>();
+            if (tid == 0) red_release_add(p.gu_done + c.v, 1u);
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < 4; mt++)
+#pragma unroll
+                for (int nt = 0; nt < EX_NT; nt++)
+#pragma unroll
+                    for (int t = 0; t < 4; t++) red[((cw * 4 + mt) * EX_NT + nt) * 128 + t * 32 + lane] = acc[mt][nt][t];
+            consumer_sync<EX_CT>();
+            const int per_mt = c.NT * 128;
+            for (int idx = tid; idx < 4 * per_mt; idx += EX_CT) {
+                const int mt = idx / per_mt, rem = idx - mt * per_mt;
+                const int nt = rem >> 7, t = (rem >> 5) & 3, ln = rem & 31;
+                const int col = nt * 8 + 2 * (ln & 3) + (t & 1);
+                if (col >= c.r) continue;
+                float y = 0.f;
+                for (int w = 0; w < EX_CW; w++) y += red[((w * 4 + mt) * EX_NT + nt) * 128 + t * 32 + ln];
+                y *= exp2i(f16_scale_exponent(__ldcg(p.hmax + c.pb + col)));
+                const int mrow = blk * 64 + mt * 16 + (ln >> 2) + 8 * (t >> 1);
+                if (c.shared) {
+                    float* dst = p.out_shared + (size_t)(c.pb + col) * p.m_dn + mrow;
+                    *dst = p.accum ? (*dst + y) : y;
+                } else {
+                    const int pid = __ldg(p.pair + c.u_off + col);
+                    p.y_part[(size_t)pid * p.m_dn + mrow] = y;
+                }
+            }
+        }
+    }
+}
+
+template <int FR, int FS>
+__global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_constant__ ExParams p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char* ring = smem;
+    float* red = reinterpret_cast<float*>(ring + (size_t)EX_NST * EX_STAGE);
+    uint64_t* full = reinterpret_cast<uint64_t*>(red + EX_RED_FLOATS);
+    uint64_t* empty = full + EX_NST;
+    Meta* meta = reinterpret_cast<Meta*>(empty + EX_NST);
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int s = 0; s < EX_NST; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], EX_CW);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int S = p.n_shared;
+    const int U = (p.job == J_LAYER) ? (int)p.ctrl[CTRL_UNIQUE] : 0;
+    const int V = S + U;
+
+    if (tid >= EX_CT) {
+        if (tid == EX_CT) producer(p, V, ring, full, empty, meta);
+        return;
+    }
+    consumer<FR, FS>(p, V, ring, red, full, empty, meta);
+
+    // the last CTA to finish leaves the workspace clean for the next call
+    consumer_sync<EX_CT>();
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(p.ctrl + CTRL_EXIT, 1u) == gridDim.x - 1;
+    }
+    consumer_sync<EX_CT>();
+    if (s_last) {
+        __threadfence();
+        for (int i = tid; i < V; i += EX_CT) p.gu_done[i] = 0;
+        for (int64_t i = tid; i < p.pairs_cap; i += EX_CT) p.hmax[i] = 0;
+        if (tid == 0) {
+            p.ctrl[CTRL_WORK] = 0;
+            p.ctrl[CTRL_EXIT] = 0;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+static bool make_geom(Geom& g, int fmt, bool gu, int K, int rows_total) {
+    g.rows_item = gu ? 16 : 64;
+    g.row_bytes = fmt == MOE_FMT_MXFP4 ? K / 2 : K;
+    const int cap = gu ? 512 : 256;
+    g.cb = g.row_bytes < cap ? g.row_bytes : cap;
+    if (g.cb <= 0 || g.row_bytes % g.cb) return false;
+    g.bi = (g.cb % 128 == 0) ? 128 : g.cb;
+    if (g.bi % 16 || g.bi > 128) return false;
+    g.nbox = g.cb / g.bi;
+    g.chunks = g.row_bytes / g.cb;
+    g.gps = fmt == MOE_FMT_MXFP4 ? g.cb / 16 : g.cb / 32;
+    g.sb = fmt == MOE_FMT_MXFP4 ? g.gps : 2 * g.gps;
+    g.flat = g.sb < 16;
+    const int rsb = (fmt == MOE_FMT_MXFP4 ? 1 : 2) * (K / 32);
+    if (g.flat && (g.chunks != 1 || (g.rows_item * g.sb) % 16)) return false;
+    if (!g.flat && rsb % 16) return false;
+    if (rows_total % g.rows_item) return false;
+    g.tx = (uint32_t)((gu ? 2 : 1) * (g.nbox * g.bi * g.rows_item + g.rows_item * g.sb));
+    return true;
+}
+
+// codes and scales maps of one [rows][K] matrix stored at `codes`/`scales`
+// in each of n_slots slots slot_bytes apart
+static bool make_maps(CUtensorMap* cm, CUtensorMap* sm, const Geom& g, int fmt, const void* codes,
+                      const void* scales, int rows, int K, int n_slots, int64_t slot_bytes) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    if (((uintptr_t)codes & 15) || ((uintptr_t)scales & 15)) return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)g.row_bytes, (cuuint64_t)rows, (cuuint64_t)n_slots};
+        const cuuint64_t strides[2] = {(cuuint64_t)g.row_bytes, (cuuint64_t)slot_bytes};
+        const cuuint32_t box[3] = {(cuuint32_t)g.bi, (cuuint32_t)g.rows_item, 1};
+        if (enc(cm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(codes), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, g.bi == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    }
+    const int rsb = (fmt == MOE_FMT_MXFP4 ? 1 : 2) * (K / 32);
+    if (g.flat) {
+        const cuuint64_t dims[3] = {16, (cuuint64_t)rows * rsb / 16, (cuuint64_t)n_slots};
+        const cuuint64_t strides[2] = {16, (cuuint64_t)slot_bytes};
+        const cuuint32_t box[3] = {16, (cuuint32_t)(g.rows_item * g.sb / 16), 1};
+        return enc(sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(scales), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+    const cuuint64_t dims[3] = {(cuuint64_t)rsb, (cuuint64_t)rows, (cuuint64_t)n_slots};
+    const cuuint64_t strides[2] = {(cuuint64_t)rsb, (cuuint64_t)slot_bytes};
+    const cuuint32_t box[3] = {(cuuint32_t)g.sb, (cuuint32_t)g.rows_item, 1};
+    return enc(sm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(scales), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// all six maps of a slab pool (gate, up, down)
+static bool pool_maps(CUtensorMap* maps, Geom* gg /*[2]: gate/up, down*/, const moe_pool* pool, int d, int f) {
+    const int fmt = pool->format;
+    if (!make_geom(gg[0], fmt, true, d, f) || !make_geom(gg[1], fmt, false, f, d)) return false;
+    const char* base = static_cast<const char*>(pool->base);
+    const int64_t cpb = fmt == MOE_FMT_MXFP4 ? 1 : 2;  // scale bytes per group
+    const int64_t codes_gu = fmt == MOE_FMT_MXFP4 ? (int64_t)f * d / 2 : (int64_t)f * d;
+    const int64_t scales_gu = (int64_t)f * (d / 32) * cpb;
+    const int64_t per = codes_gu + scales_gu;
+    if (!make_maps(&maps[0], &maps[1], gg[0], fmt, base, base + codes_gu, f, d, pool->n_slots, pool->slot_bytes))
+        return false;
+    if (!make_maps(&maps[2], &maps[3], gg[0], fmt, base + per, base + per + codes_gu, f, d, pool->n_slots,
+                   pool->slot_bytes))
+        return false;
+    return make_maps(&maps[4], &maps[5], gg[1], fmt, base + 2 * per, base + 2 * per + codes_gu, d, f, pool->n_slots,
+                     pool->slot_bytes);
+}
+
+static int sm_count() {
+    static int n = -1;
+    if (n < 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n = 0;
+    }
+    return n;
+}
+
+template <int FR, int FS>
+static int launch_expert_kernel(const ExParams& p, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(expert_kernel<FR, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)EX_SMEM) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr = true;
+    }
+    const int grid = sm_count();
+    if (grid <= 0) return MOE_ERR_CUDA;
+    expert_kernel<FR, FS><<<grid, EX_THREADS, EX_SMEM, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" int32_t moe_device_sm_count(void) { return sm_count(); }
+
+extern "C" size_t moe_slab_bytes(const moe_desc* desc, int32_t format) {
+    if (!desc) return 0;
+    const size_t df = (size_t)desc->d_model * desc->d_ff;
+    if (format == MOE_FMT_MXFP4) return 3 * (df / 2 + df / 32);
+    if (format == MOE_FMT_Q8_0) return 3 * (df + 2 * (df / 32));
+    return 0;
+}
+
+static bool pool_ok(const moe_desc* desc, const moe_pool* pool, int fmt) {
+    if (!pool || !pool->base || pool->format != fmt || pool->n_slots <= 0) return false;
+    if (((uintptr_t)pool->base & 31) || (pool->slot_bytes & 31)) return false;
+    return (size_t)pool->slot_bytes >= moe_slab_bytes(desc, fmt);
+}
+
+extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mode, const moe_pool* routed,
+                                const int32_t* expert_slot, const uint32_t* slot_ready, const moe_pool* shared,
+                                int32_t n_shared, void* ws, int32_t n_rows_max, float* y_part, void* stream) {
+    if (!desc || !ws || !expert_slot || !y_part) return MOE_ERR_INVALID_ARG;
+    const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
+    if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
+        return MOE_ERR_UNSUPPORTED;
+    const int base_mode = mode & 0xFF;
+    if (base_mode != MOE_MODE_DECODE) return MOE_ERR_UNSUPPORTED;
+    if (n_rows < 1 || n_rows > 16 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
+    if (n_shared < 0 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
+    if (!pool_ok(desc, routed, MOE_FMT_MXFP4)) return MOE_ERR_INVALID_ARG;
+    if (n_shared > 0 && (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared)) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 255) return MOE_ERR_INVALID_ARG;
+
+    const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
+    char* base = static_cast<char*>(ws);
+    static ExParams p;  // large (tensor maps); filled per call, copied into the launch
+    memset(&p, 0, sizeof(p));
+    if (!pool_maps(&p.map[0], &p.geom[0], routed, d, f)) return MOE_ERR_UNSUPPORTED;
+    if (n_shared > 0 && !pool_maps(&p.map[6], &p.geom[2], shared, d, f)) return MOE_ERR_UNSUPPORTED;
+    if (n_shared == 0) {
+        for (int i = 0; i < 6; i++) p.map[6 + i] = p.map[i];
+        p.geom[2] = p.geom[0];
+        p.geom[3] = p.geom[1];
+    }
+    p.job = J_LAYER;
+    p.fmt_routed = MOE_FMT_MXFP4;
+    p.fmt_shared = MOE_FMT_Q8_0;
+    p.k_gu = d;
+    p.m_gu = f;
+    p.k_dn = f;
+    p.m_dn = d;
+    p.top_k = k;
+    p.n_rows = n_rows;
+    p.n_shared = n_shared;
+    p.n_gu = f / 16;
+    p.n_dn = d / 64;
+    p.lag = 2;
+    p.debug_gu = (mode & MOE_MODE_DEBUG_GU) ? 1 : 0;
+    p.accum = 0;
+    p.expert_slot = expert_slot;
+    p.slot_ready = slot_ready;
+    p.n_slots = routed->n_slots;
+    p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
+    p.uexp = reinterpret_cast<const int*>(base + L.uexp);
+    p.off = reinterpret_cast<const int*>(base + L.off);
+    p.pair = reinterpret_cast<const int*>(base + L.pair);
+    p.x16 = reinterpret_cast<const __half*>(base + L.x16);
+    p.xexp = reinterpret_cast<const int*>(base + L.xexp);
+    p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done);
+    p.hmax = reinterpret_cast<uint32_t*>(base + L.hmax);
+    p.h = reinterpret_cast<float*>(base + L.h);
+    p.dbg_g = reinterpret_cast<float*>(base + L.dbg_g);
+    p.dbg_u = reinterpret_cast<float*>(base + L.dbg_u);
+    p.out_shared = reinterpret_cast<float*>(base + L.shared_y);
+    p.y_part = y_part;
+    p.pairs_cap = L.pairs;
+    return n_shared > 0 ? launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream))
+                        : launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// stand-alone Q8_0 block matmul
+// ---------------------------------------------------------------------------
+
+struct Q8Ws {
+    size_t ctrl, x16, xexp, hmax, h, gu_done, total;
+};
+
+static Q8Ws q8_layout(int n_rows, int k_in) {
+    Q8Ws L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+    L.ctrl = take(CTRL_WORDS * 4);
+    L.x16 = take((size_t)n_rows * k_in * 2);
+    L.xexp = take((size_t)n_rows * 4);
+    L.hmax = take((size_t)n_rows * 4);
+    L.h = take((size_t)n_rows * k_in * 4);
+    L.gu_done = take(4);
+    L.total = o;
+    return L;
+}
+
+// prepares the rows of a stand-alone Q8_0 matmul: f16 rows (SwiGLU) or fp32
+// rows with their largest magnitude (plain)
+__global__ void q8_prep_kernel(int k_in, const void* x, int x_dtype, int swiglu, __half* x16, int* xexp,
+                               uint32_t* hmax, float* h) {
+    const int n = blockIdx.x, tid = threadIdx.x;
+    __shared__ uint32_t s_max[32];
+    __shared__ int s_p;
+    uint32_t mx = 0;
+    for (int c = tid; c < k_in; c += blockDim.x) {
+        float v;
+        if (x_dtype == MOE_DTYPE_BF16)
+            v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[(size_t)n * k_in + c] << 16);
+        else
+            v = static_cast<const float*>(x)[(size_t)n * k_in + c];
+        mx = max(mx, __float_as_uint(v) & 0x7FFFFFFFu);
+        if (!swiglu) h[(size_t)n * k_in + c] = v;
+    }
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((tid & 31) == 0) s_max[tid >> 5] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t m = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); w++) m = max(m, s_max[w]);
+        s_p = f16_scale_exponent(m);
+        hmax[n] = m;
+        xexp[n] = s_p;
+    }
+    __syncthreads();
+    if (swiglu) {
+        const float s = exp2i(-s_p);
+        for (int c = tid; c < k_in; c += blockDim.x)
+            x16[(size_t)n * k_in + c] =
+                __float2half_rn(__uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[(size_t)n * k_in + c] << 16) * s);
+    }
+}
+
+extern "C" size_t q8_0_workspace_size(int32_t n_rows, int32_t k_in, int32_t n_out) {
+    (void)n_out;
+    if (n_rows <= 0 || k_in <= 0) return 0;
+    return q8_layout(n_rows, k_in).total;
+}
+
+extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, const void* x, int32_t x_dtype,
+                                 const int8_t* q, const uint16_t* dq, const int8_t* q2, const uint16_t* d2,
+                                 int32_t epilogue, float* y, void* ws, void* stream) {
+    if (!x || !q || !dq || !y || !ws) return MOE_ERR_INVALID_ARG;
+    if (n_rows < 1 || n_rows > 16 || k_in <= 0 || k_in % 256 || n_out <= 0) return MOE_ERR_UNSUPPORTED;
+    if (x_dtype != MOE_DTYPE_BF16 && x_dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID_ARG;
+    const bool swiglu = epilogue == MOE_EPI_SWIGLU;
+    if (!swiglu && epilogue != MOE_EPI_NONE && epilogue != MOE_EPI_ACCUM) return MOE_ERR_INVALID_ARG;
+    if (swiglu && (!q2 || !d2 || x_dtype != MOE_DTYPE_BF16)) return MOE_ERR_INVALID_ARG;
+    if (swiglu ? (n_out % 16) : (n_out % 64)) return MOE_ERR_UNSUPPORTED;
+    if (((uintptr_t)q & 31) || ((uintptr_t)dq & 31) || ((uintptr_t)ws & 255)) return MOE_ERR_INVALID_ARG;
+    if (swiglu && (((uintptr_t)q2 & 31) || ((uintptr_t)d2 & 31))) return MOE_ERR_INVALID_ARG;
+
+    const Q8Ws L = q8_layout(n_rows, k_in);
+    char* base = static_cast<char*>(ws);
+    static ExParams p;
+    memset(&p, 0, sizeof(p));
+    Geom g;
+    if (!make_geom(g, MOE_FMT_Q8_0, swiglu, k_in, n_out)) return MOE_ERR_UNSUPPORTED;
+    const int64_t qbytes = align_up((size_t)n_out * k_in, 32);
+    const int64_t dbytes = align_up((size_t)n_out * (k_in / 32) * 2, 32);
+    const int64_t slot = qbytes > dbytes ? qbytes : dbytes;
+    if (swiglu) {
+        if (!make_maps(&p.map[6], &p.map[7], g, MOE_FMT_Q8_0, q, dq, n_out, k_in, 1, slot)) return MOE_ERR_UNSUPPORTED;
+        if (!make_maps(&p.map[8], &p.map[9], g, MOE_FMT_Q8_0, q2, d2, n_out, k_in, 1, slot)) return MOE_ERR_UNSUPPORTED;
+        p.map[10] = p.map[6];
+        p.map[11] = p.map[7];
+        p.geom[2] = g;
+        p.geom[3] = g;
+        p.job = J_Q8_SWIGLU;
+    } else {
+        if (!make_maps(&p.map[10], &p.map[11], g, MOE_FMT_Q8_0, q, dq, n_out, k_in, 1, slot)) return MOE_ERR_UNSUPPORTED;
+        p.map[6] = p.map[8] = p.map[10];
+        p.map[7] = p.map[9] = p.map[11];
+        p.geom[2] = g;
+        p.geom[3] = g;
+        p.job = J_Q8_PLAIN;
+    }
+    for (int i = 0; i < 6; i++) p.map[i] = p.map[6 + i];
+    p.geom[0] = p.geom[2];
+    p.geom[1] = p.geom[3];
+    p.fmt_routed = p.fmt_shared = MOE_FMT_Q8_0;
+    p.k_gu = k_in;
+    p.m_gu = n_out;
+    p.k_dn = k_in;
+    p.m_dn = n_out;
+    p.top_k = 1;
+    p.n_rows = n_rows;
+    p.n_shared = 1;
+    p.n_gu = n_out / 16;
+    p.n_dn = n_out / 64;
+    p.lag = 0;
+    p.accum = epilogue == MOE_EPI_ACCUM;
+    p.n_slots = 1;
+    p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
+    p.x16 = reinterpret_cast<const __half*>(base + L.x16);
+    p.xexp = reinterpret_cast<const int*>(base + L.xexp);
+    p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done);
+    p.hmax = reinterpret_cast<uint32_t*>(base + L.hmax);
+    p.h = swiglu ? y : reinterpret_cast<float*>(base + L.h);
+    p.out_shared = y;
+    p.dbg_g = p.dbg_u = nullptr;
+    p.pairs_cap = 0;  // hmax rows are rewritten by the preparation kernel on every call
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    q8_prep_kernel<<<n_rows, 256, 0, s>>>(k_in, x, x_dtype, swiglu ? 1 : 0, reinterpret_cast<__half*>(base + L.x16),
+                                          reinterpret_cast<int*>(base + L.xexp),
+                                          reinterpret_cast<uint32_t*>(base + L.hmax),
+                                          reinterpret_cast<float*>(base + L.h));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_expert_kernel<MOE_FMT_Q8_0, MOE_FMT_Q8_0>(p, s);
+}

@@ -1,0 +1,115 @@
+"""A MoE layer on one GPU, assembled from the C ABI calls.
+
+``MoeLayer`` owns the device buffers of one layer (router matrix, expert slab
+pool and slot map, shared-expert pool, workspace, per-block outputs) and runs a
+block of rows through ``moe_route`` -> ``moe_expert_block`` -> ``moe_combine``
+on one stream.  PyTorch only allocates memory and provides the stream; every
+step runs in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class MoeLayer:
+    def __init__(self, d_model: int, d_ff: int, n_experts: int, top_k: int, n_rows_max: int = 16,
+                 n_shared: int = 0, device: str | int = "cuda"):
+        self.desc = B.desc(d_model, d_ff, n_experts, top_k)
+        self.d, self.f, self.E, self.k = d_model, d_ff, n_experts, top_k
+        self.n_rows_max = n_rows_max
+        self.n_shared = n_shared
+        self.device = torch.device(device)
+        self.slab_bytes = B.moe_slab_bytes(self.desc, B.MOE_FMT_MXFP4)
+        self.q8_bytes = B.moe_slab_bytes(self.desc, B.MOE_FMT_Q8_0)
+        self.slot_bytes = (self.slab_bytes + 255) // 256 * 256
+        self.q8_slot_bytes = (self.q8_bytes + 255) // 256 * 256
+        ws_bytes = B.moe_workspace_size(self.desc, n_rows_max, n_shared)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=self.device)
+        self.offsets = B.moe_workspace_offsets(self.desc, n_rows_max, n_shared)
+        self.router = None
+        self.pool = None
+        self.n_slots = 0
+        self.expert_slot = torch.zeros(n_experts, dtype=torch.int32, device=self.device)
+        self.shared_pool = None
+        self.slot_ready = None
+        N = n_rows_max
+        self.topk_idx = torch.zeros((N, top_k), dtype=torch.int32, device=self.device)
+        self.topk_w = torch.zeros((N, top_k), dtype=torch.float32, device=self.device)
+        self.logits = torch.zeros((N, n_experts), dtype=torch.float32, device=self.device)
+        self.y_part = torch.zeros((N, top_k, d_model), dtype=torch.float32, device=self.device)
+        self.out = torch.zeros((N, d_model), dtype=torch.uint16, device=self.device)
+
+    # --- weights -------------------------------------------------------------
+    def set_router(self, w_bits: torch.Tensor):
+        """bf16 router matrix [E][d] as uint16 bits (host or device)."""
+        self.router = w_bits.to(self.device, torch.uint16).contiguous()
+
+    def alloc_pool(self, n_slots: int):
+        self.n_slots = n_slots
+        self.pool = torch.empty(n_slots * self.slot_bytes, dtype=torch.uint8, device=self.device)
+
+    def put_slab(self, slot: int, slab):
+        """Copy one MXFP4 slab (numpy uint8 or tensor) into a pool slot."""
+        t = torch.as_tensor(slab, dtype=torch.uint8)
+        self.pool[slot * self.slot_bytes: slot * self.slot_bytes + self.slab_bytes].copy_(t, non_blocking=False)
+
+    def set_expert_slots(self, slots):
+        self.expert_slot.copy_(torch.as_tensor(slots, dtype=torch.int32))
+
+    def set_shared(self, slabs):
+        assert len(slabs) == self.n_shared
+        self.shared_pool = torch.empty(max(1, self.n_shared) * self.q8_slot_bytes, dtype=torch.uint8,
+                                       device=self.device)
+        for i, s in enumerate(slabs):
+            self.shared_pool[i * self.q8_slot_bytes: i * self.q8_slot_bytes + self.q8_bytes].copy_(
+                torch.as_tensor(s, dtype=torch.uint8))
+
+    def routed_pool(self) -> B.MoePool:
+        return B.pool(self.pool, self.slot_bytes, self.n_slots, B.MOE_FMT_MXFP4)
+
+    def shared_pool_desc(self):
+        if self.n_shared == 0:
+            return None
+        return B.pool(self.shared_pool, self.q8_slot_bytes, self.n_shared, B.MOE_FMT_Q8_0)
+
+    # --- views of the workspace ----------------------------------------------
+    def ws_view(self, offset: int, count: int, dtype) -> torch.Tensor:
+        nbytes = count * torch.empty((), dtype=dtype).element_size()
+        return self.ws[offset: offset + nbytes].view(dtype)
+
+    def shared_y(self, n_rows: int) -> torch.Tensor:
+        """Shared-expert outputs of the last block, [n_shared][n_rows][d] (the kernels lay
+        them out for the block's own row count)."""
+        return self.ws_view(self.offsets.shared_y, self.n_shared * n_rows * self.d,
+                            torch.float32).view(self.n_shared, n_rows, self.d)
+
+    # --- the layer -------------------------------------------------------------
+    def route(self, n_rows: int, x, logits_in=None, stream=None):
+        B.moe_route(self.desc, n_rows, x, self.router if logits_in is None else None, logits_in,
+                    self.logits if logits_in is None else None, self.topk_idx, self.topk_w, self.ws,
+                    self.n_rows_max, self.n_shared, stream)
+
+    def experts(self, n_rows: int, mode: int = B.MOE_MODE_DECODE, stream=None):
+        B.moe_expert_block(self.desc, n_rows, mode, self.routed_pool(), self.expert_slot, self.slot_ready,
+                           self.shared_pool_desc(), self.n_shared, self.ws, self.n_rows_max, self.y_part,
+                           stream)
+
+    def combine(self, n_rows: int, residual, stream=None):
+        shared_y = self.ws.data_ptr() + self.offsets.shared_y if self.n_shared else None
+        B.moe_combine(self.desc, n_rows, residual, self.y_part, self.topk_w, shared_y, self.n_shared,
+                      self.out, stream)
+
+    def forward(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
+                stream=None):
+        """Run one block: x, residual bf16 bits [N][d] on the device; returns out bits [N][d]."""
+        n = x.shape[0] if n_rows is None else n_rows
+        self.route(n, x, logits_in=logits_in, stream=stream)
+        self.experts(n, mode=mode, stream=stream)
+        self.combine(n, residual, stream=stream)
+        return self.out[:n]
+
+    def error_bits(self, stream=None) -> int:
+        return B.moe_get_error(self.ws, stream)
