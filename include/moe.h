@@ -234,6 +234,31 @@ MOE_API int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out,
                       int32_t epilogue, float* y, void* ws, void* stream);
 
 /*
+ * q8_0_block_matmul without a caller-provided workspace, for callers that
+ * cannot allocate device memory: a host process whose own pool allocator owns
+ * all of HBM, or a latency-critical path where cudaMalloc/cudaFree (which can
+ * synchronise the device) is not acceptable.  The pages have no counterpart of
+ * this entry point; it is a deployment convenience of this library.
+ *
+ * Same arguments and results as q8_0_block_matmul, minus ws.  Its scratch is a
+ * file-scope __device__ array of 720,896 bytes that every GPU loading this
+ * library holds until the process exits; limits: n_rows <= 16 and
+ * k_in <= 7168 (larger sizes return MOE_ERR_UNSUPPORTED before any launch).
+ * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call shares the one array: the call clears the parts that
+ * must start at zero, but calls that overlap on the GPU (different streams,
+ * or different host threads on one device) race on it and must be serialised
+ * by the caller.
+ */
+MOE_API int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n_out,
+                                      const void* x, int32_t x_dtype,
+                                      const int8_t* q, const uint16_t* d,
+                                      const int8_t* q2, const uint16_t* d2,
+                                      int32_t epilogue, float* y, void* stream);
+
+/*
  * Reads the workspace's device error word (synchronising `stream`), clears it,
  * and returns it through *bits (host).  Returns MOE_OK, or MOE_ERR_CUDA.
  */

@@ -35,6 +35,7 @@ MOE_DTYPE_F32 = 1
 EXPORTED = [
     "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
+    "q8_0_block_matmul_noalloc",
 ]
 
 
@@ -86,6 +87,7 @@ def lib() -> ctypes.CDLL:
         L.q8_0_workspace_size.argtypes = [I32, I32, I32]
         L.q8_0_workspace_size.restype = SZ
         L.q8_0_block_matmul.argtypes = [I32, I32, I32, P, I32, P, P, P, P, I32, P, P, P]
+        L.q8_0_block_matmul_noalloc.argtypes = [I32, I32, I32, P, I32, P, P, P, P, I32, P, P]
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_device_sm_count.restype = I32
         _LIB = L
@@ -167,6 +169,15 @@ def q8_0_block_matmul(n_rows: int, k_in: int, n_out: int, x, x_dtype: int, q, dq
     _check(lib().q8_0_block_matmul(n_rows, k_in, n_out, _ptr(x), x_dtype, _ptr(q), _ptr(dq), _ptr(q2),
                                    _ptr(d2), epilogue, _ptr(y), _ptr(ws), _stream(stream)),
            "q8_0_block_matmul")
+
+
+def q8_0_block_matmul_noalloc(n_rows: int, k_in: int, n_out: int, x, x_dtype: int, q, dq, q2, d2,
+                              epilogue: int, y, stream=None):
+    """q8_0_block_matmul with the library's own static device scratch (no workspace
+    argument, nothing allocated); calls that overlap on the GPU must be serialised."""
+    _check(lib().q8_0_block_matmul_noalloc(n_rows, k_in, n_out, _ptr(x), x_dtype, _ptr(q), _ptr(dq), _ptr(q2),
+                                           _ptr(d2), epilogue, _ptr(y), _stream(stream)),
+           "q8_0_block_matmul_noalloc")
 
 
 def moe_get_error(ws, stream=None) -> int:

@@ -937,3 +937,49 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     return launch_expert_kernel<MOE_FMT_Q8_0, MOE_FMT_Q8_0>(p, s);
 }
+
+// ---------------------------------------------------------------------------
+// stand-alone Q8_0 block matmul without any device allocation by the caller
+// ---------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory for the scratch that
+// q8_0_block_matmul needs: a host process that hands every byte of HBM to its
+// own pool allocator up front, or a latency-critical serving path where a
+// cudaMalloc/cudaFree (which can synchronise the device) is not acceptable.
+// This variant takes its scratch from a file-scope __device__ array instead.
+// The array lives in every GPU that loads this library until the process exits.
+
+constexpr int Q8_NOALLOC_MAX_ROWS = 16;
+constexpr int Q8_NOALLOC_MAX_K = 7168;
+constexpr size_t Q8_NOALLOC_BYTES = 720896;  // >= q8_layout(16, 7168).total, rounded to 4 KB
+constexpr int Q8_NOALLOC_MAX_DEVICES = 64;
+
+static __device__ __align__(256) unsigned char q8_noalloc_scratch[Q8_NOALLOC_BYTES];
+
+// Device address of the scratch array on each device (looked up once per
+// device, with that device current; the symbol name is only a host stand-in).
+static void* q8_noalloc_addr[Q8_NOALLOC_MAX_DEVICES];
+
+extern "C" int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n_out, const void* x,
+                                         int32_t x_dtype, const int8_t* q, const uint16_t* dq, const int8_t* q2,
+                                         const uint16_t* d2, int32_t epilogue, float* y, void* stream) {
+    if (n_rows < 1 || n_rows > Q8_NOALLOC_MAX_ROWS || k_in <= 0 || k_in > Q8_NOALLOC_MAX_K)
+        return MOE_ERR_UNSUPPORTED;
+    const Q8Ws L = q8_layout(n_rows, k_in);
+    if (L.total > Q8_NOALLOC_BYTES) return MOE_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= Q8_NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
+    if (q8_noalloc_addr[dev] == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, q8_noalloc_scratch) != cudaSuccess || addr == nullptr) return MOE_ERR_CUDA;
+        q8_noalloc_addr[dev] = addr;
+    }
+    unsigned char* ws = static_cast<unsigned char*>(q8_noalloc_addr[dev]);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: clear the control words and
+    // the gate/up completion counter, which the kernel expects to start at zero
+    if (cudaMemsetAsync(ws + L.ctrl, 0, CTRL_WORDS * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(ws + L.gu_done, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return q8_0_block_matmul(n_rows, k_in, n_out, x, x_dtype, q, dq, q2, d2, epilogue, y, ws, stream);
+}
