@@ -332,6 +332,42 @@ def time_blocks(torch, lay, X, flush, n, reps):
             "gbs_all_bytes": allb / t / 1e6, "routing": "caller logits"}
 
 
+def run_profile_case(args):
+    """Small case for `ncu --set full`: the Kimi-shaped layer on one row with router-GEMV
+    routing, but a pool holding only the 32 experts with the largest float32 logits
+    (about 0.6 GB on the device instead of 15.7 GB); four layers, L2 flushed before each."""
+    import torch
+
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+    build_mod.build()
+    sh = syn.KIMI
+    rows = list(range(args.profile_rows))
+    x = syn.x_rows(SEED, rows, sh.d_model)
+    router = syn.router_weight(SEED, sh)
+    xf = (x.astype(np.uint32) << 16).view(np.float32)
+    wf = (router.astype(np.uint32) << 16).view(np.float32)
+    lo = xf @ wf.T
+    experts = sorted(set(np.argsort(-lo, axis=1)[:, :32].ravel().tolist()))
+    lay = MoeLayer(sh.d_model, sh.d_ff, sh.n_experts, sh.top_k, n_rows_max=16, n_shared=2)
+    lay.set_router(torch.from_numpy(router.view(np.int16)).view(torch.uint16))
+    lay.alloc_pool(len(experts))
+    slots = np.zeros(sh.n_experts, dtype=np.int32)
+    for i, (e, slab) in enumerate(syn.mxfp4_slabs_parallel(SEED, experts, sh)):
+        lay.put_slab(i, slab)
+        slots[e] = i
+    lay.set_expert_slots(slots)
+    lay.set_shared([syn.q8_0_shared_slab(SEED, s, sh) for s in range(2)])
+    X = torch.from_numpy(x.view(np.int16)).cuda().view(torch.uint16)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(4):
+        flush.zero_()
+        lay.forward(X, X)
+    torch.cuda.synchronize()
+    assert lay.error_bits() == 0
+    print(json.dumps({"profile_case": "ok", "rows": len(rows), "pool_experts": len(experts)}))
+
+
 def run_reference(args):
     """The CPU oracle timed on this host's cores: each step is the oracle's expert MLP
     of one (row, selected expert) pair of the workload (17,547,264 expert bytes)."""
@@ -359,7 +395,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-blocks", action="store_true")
     ap.add_argument("--_oracle-sample", type=int, default=0, dest="oracle_sample")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run the small ncu case (a few layers, <1 GB on the device) and exit")
+    ap.add_argument("--profile-rows", type=int, default=1)
     args = ap.parse_args()
+
+    if args.profile_case:
+        run_profile_case(args)
+        return
 
     if args.oracle_sample:
         print(json.dumps({"seconds": oracle_step_seconds(oracle_pairs(args.oracle_sample))}))

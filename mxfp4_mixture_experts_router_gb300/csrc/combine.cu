@@ -10,8 +10,11 @@
 
 namespace moe {
 
-constexpr int CB_THREADS = 256;
+constexpr int CB_THREADS = 64;
 
+// One thread per 4 consecutive columns of a row; every slot's load is issued
+// before the fixed-order sum, so the loads overlap.
+template <int KMAX>
 __global__ void __launch_bounds__(CB_THREADS) combine_kernel(int d, int k, int n_shared, int N,
                                                              const uint16_t* __restrict__ residual,
                                                              const float* __restrict__ y_part,
@@ -21,24 +24,34 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(int d, int k, int n
     const int n = blockIdx.y;
     const int c = (blockIdx.x * CB_THREADS + threadIdx.x) * 4;
     if (c >= d) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* yr = y_part + (size_t)n * k * d + c;
-    for (int j = 0; j < k; j++) {
-        const float w = __ldg(topk_w + (size_t)n * k + j);
-        const float4 y = __ldg(reinterpret_cast<const float4*>(yr + (size_t)j * d));
-        acc.x = fmaf(w, y.x, acc.x);
-        acc.y = fmaf(w, y.y, acc.y);
-        acc.z = fmaf(w, y.z, acc.z);
-        acc.w = fmaf(w, y.w, acc.w);
-    }
-    for (int s = 0; s < n_shared; s++) {
-        const float4 y = __ldg(reinterpret_cast<const float4*>(shared_y + ((size_t)s * N + n) * d + c));
-        acc.x += y.x;
-        acc.y += y.y;
-        acc.z += y.z;
-        acc.w += y.w;
+    float4 y[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; j++) {
+        if (j < k) {
+            w[j] = __ldg(topk_w + (size_t)n * k + j);
+            y[j] = __ldg(reinterpret_cast<const float4*>(yr + (size_t)j * d));
+        }
     }
     const uint2 rb = __ldg(reinterpret_cast<const uint2*>(residual + (size_t)n * d + c));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < KMAX; j++) {
+        if (j < k) {
+            acc.x = fmaf(w[j], y[j].x, acc.x);
+            acc.y = fmaf(w[j], y[j].y, acc.y);
+            acc.z = fmaf(w[j], y[j].z, acc.z);
+            acc.w = fmaf(w[j], y[j].w, acc.w);
+        }
+    }
+    for (int s = 0; s < n_shared; s++) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(shared_y + ((size_t)s * N + n) * d + c));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+    }
     const float r0 = __uint_as_float(rb.x << 16), r1 = __uint_as_float(rb.x & 0xFFFF0000u);
     const float r2 = __uint_as_float(rb.y << 16), r3 = __uint_as_float(rb.y & 0xFFFF0000u);
     const __nv_bfloat16 o0 = __float2bfloat16_rn(r0 + acc.x), o1 = __float2bfloat16_rn(r1 + acc.y);
@@ -64,8 +77,11 @@ extern "C" int moe_combine(const moe_desc* desc, int32_t n_rows, const uint16_t*
         (shared_y && ((uintptr_t)shared_y & 15)))
         return MOE_ERR_INVALID_ARG;
     dim3 grid((d / 4 + CB_THREADS - 1) / CB_THREADS, n_rows);
-    combine_kernel<<<grid, CB_THREADS, 0, static_cast<cudaStream_t>(stream)>>>(d, k, n_shared, n_rows, residual,
-                                                                                y_part, topk_w, shared_y, out);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (k <= 16)
+        combine_kernel<16><<<grid, CB_THREADS, 0, s>>>(d, k, n_shared, n_rows, residual, y_part, topk_w, shared_y, out);
+    else
+        combine_kernel<32><<<grid, CB_THREADS, 0, s>>>(d, k, n_shared, n_rows, residual, y_part, topk_w, shared_y, out);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -35,10 +35,12 @@ constexpr int EX_CW = 8;                      // consumer warps
 constexpr int EX_CT = EX_CW * 32;             // consumer threads
 constexpr int EX_THREADS = EX_CT + 32;        // + producer warp
 constexpr int EX_NST = 8;                     // ring stages
+constexpr int EX_CTAS_PER_SM = 1;
 constexpr int EX_CODE_BYTES = 16384;
 constexpr int EX_STAGE = 17408;               // codes + scales
 constexpr int EX_NT = 2;                      // n-tiles of 8 rows: up to 16 rows per expert
-constexpr int EX_RED_FLOATS = EX_CW * 4 * EX_NT * 4 * 32;
+constexpr int EX_RED_FLOATS = EX_CW * 4 * EX_NT * 4 * 32;  // one down-item reduction
+constexpr int EX_RED_GU = EX_CW * 2 * EX_NT * 4 * 32;      // a gate/up item uses half of it
 constexpr size_t EX_SMEM = (size_t)EX_NST * EX_STAGE + EX_RED_FLOATS * 4 + 1024 + 1024;
 
 enum { IT_GU = 0, IT_DN = 1 };
@@ -46,6 +48,7 @@ enum { J_LAYER = 0, J_Q8_SWIGLU = 1, J_Q8_PLAIN = 2 };
 
 struct Geom {
     int row_bytes, bi, cb, nbox, sb, flat, chunks, gps, rows_item;
+    int fast;  // full-width swizzled stages: the unrolled per-warp tile paths apply
     uint32_t tx;
 };
 
@@ -266,6 +269,179 @@ __device__ __forceinline__ void dn_stage(uint32_t st, const Geom& g, int chunk, 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Fast paths for full-width stages (128-byte swizzled boxes, 512 code bytes per
+// row per gate/up stage, 256 per down stage).  Warp w owns the T consecutive
+// scale groups q = w*T + t of every stage, so each thread's shared-memory
+// offsets are constants of the kernel and every loop is unrolled.
+// ---------------------------------------------------------------------------
+
+template <int FMT>
+struct Tiles {
+    static constexpr int T_GU = FMT == MOE_FMT_MXFP4 ? 4 : 2;  // groups per warp per gate/up stage
+    static constexpr int T_DN = FMT == MOE_FMT_MXFP4 ? 2 : 1;  // groups per warp per down stage
+};
+
+// offset of row (lane/4) of the thread's A words for each of its T groups,
+// inside a matrix region of R rows made of 128-byte swizzled boxes
+template <int FMT, int T, int R>
+__device__ __forceinline__ void fast_offsets(int cw, int lane, uint32_t (&aoff)[T]) {
+    const int g = lane >> 2, i = lane & 3;
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        const int q = cw * T + t;
+        int box, chunk, inner;
+        if (FMT == MOE_FMT_MXFP4) {
+            box = q >> 3;
+            chunk = q & 7;
+            inner = 4 * i;
+        } else {
+            box = q >> 2;
+            chunk = 2 * (q & 3) + (i >> 1);
+            inner = 8 * (i & 1);
+        }
+        aoff[t] = (uint32_t)(box * 128 * R + g * 128 + ((chunk ^ g) << 4) + inner);
+    }
+}
+
+// A fragments of rows g (at addr) and g+8 (addr + 1024): same swizzle phase
+template <int FMT>
+__device__ __forceinline__ void load_a_fast(uint32_t addr, uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+    uint32_t x0, x1, x2, x3, y0, y1, y2, y3;
+    if (FMT == MOE_FMT_MXFP4) {
+        const uint32_t w0 = lds32(addr), w1 = lds32(addr + 1024);
+        e2m1x8_to_f16x2(w0, x0, x1, x2, x3);
+        e2m1x8_to_f16x2(w1, y0, y1, y2, y3);
+    } else {
+        const uint2 w0 = lds64(addr), w1 = lds64(addr + 1024);
+        s8x4_to_f16x2(w0.x, x0, x1);
+        s8x4_to_f16x2(w0.y, x2, x3);
+        s8x4_to_f16x2(w1.x, y0, y1);
+        s8x4_to_f16x2(w1.y, y2, y3);
+    }
+    a0[0] = x0; a0[1] = y0; a0[2] = x1; a0[3] = y1;
+    a1[0] = x2; a1[1] = y2; a1[2] = x3; a1[3] = y3;
+}
+
+// scale t of a word holding the thread's consecutive group scales.  E8M0
+// exponents 1..254 are exact powers of two; 0 reads as 0 and 255 as +inf.
+template <int FMT>
+__device__ __forceinline__ float scale_t(uint32_t w, int t) {
+    if (FMT == MOE_FMT_MXFP4) return __uint_as_float(((w >> (8 * t)) & 0xFFu) << 23);
+    return __half2float(__ushort_as_half((unsigned short)(w >> (16 * t))));
+}
+
+template <int FMT, int T, int NT>
+__device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunks, int cw, int lane,
+                                              const __half* const (&xrow)[EX_NT],
+                                              const bool (&bval)[EX_NT], float (&ag)[EX_NT][4],
+                                              float (&au)[EX_NT][4]) {
+    constexpr int GPS = 8 * T;
+    constexpr int SB = FMT == MOE_FMT_MXFP4 ? GPS : 2 * GPS;
+    const int gq = lane >> 2, i = lane & 3;
+    uint32_t aoff[T];
+    fast_offsets<FMT, T, 16>(cw, lane, aoff);
+    const uint32_t upC = st + 512 * 16;
+    const uint32_t gateS = st + EX_CODE_BYTES + gq * SB + 4 * cw, upS = gateS + 512;
+    if (chunk + 1 < nchunks) {
+        // the item's next stage reads the next K slice of the same rows: T*64 bytes
+        // per row and warp, fetched into L1 one 128-byte line per lane i
+        constexpr int LINES = (T * 64 + 127) / 128;
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            if (bval[nt] && i < LINES)
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(xrow[nt] + ((chunk + 1) * GPS + cw * T) * 32 + 64 * i));
+    }
+    const uint32_t sg0 = lds32(gateS), sg1 = lds32(gateS + 8 * SB);
+    const uint32_t su0 = lds32(upS), su1 = lds32(upS + 8 * SB);
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        uint4 bx[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            bx[nt] = make_uint4(0, 0, 0, 0);
+            if (bval[nt])
+                bx[nt] = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i));
+        }
+        uint32_t g0[4], g1[4], u0[4], u1[4];
+        load_a_fast<FMT>(st + aoff[t], g0, g1);
+        load_a_fast<FMT>(upC + aoff[t], u0, u1);
+        const float fg0 = scale_t<FMT>(sg0, t), fg1 = scale_t<FMT>(sg1, t);
+        const float fu0 = scale_t<FMT>(su0, t), fu1 = scale_t<FMT>(su1, t);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            {
+                float pg[4] = {0.f, 0.f, 0.f, 0.f}, pu[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(pg, g0[0], g0[1], g0[2], g0[3], bx[nt].x, bx[nt].y);
+                mma_f16(pg, g1[0], g1[1], g1[2], g1[3], bx[nt].z, bx[nt].w);
+                mma_f16(pu, u0[0], u0[1], u0[2], u0[3], bx[nt].x, bx[nt].y);
+                mma_f16(pu, u1[0], u1[1], u1[2], u1[3], bx[nt].z, bx[nt].w);
+                fma4(ag[nt], fg0, fg1, pg);
+                fma4(au[nt], fu0, fu1, pu);
+            }
+        }
+    }
+}
+
+template <int FMT, int T, int NT>
+__device__ __forceinline__ void dn_stage_fast(uint32_t st, int chunk, int cw, int lane,
+                                              const float* const (&hrow)[EX_NT],
+                                              const float (&hs)[EX_NT], const bool (&bval)[EX_NT],
+                                              float (&acc)[4][EX_NT][4]) {
+    constexpr int GPS = 8 * T;
+    constexpr int SB = FMT == MOE_FMT_MXFP4 ? GPS : 2 * GPS;
+    const int gq = lane >> 2, i = lane & 3;
+    uint32_t aoff[T];
+    fast_offsets<FMT, T, 64>(cw, lane, aoff);
+    const uint32_t S = st + EX_CODE_BYTES + gq * SB + 2 * cw;
+    uint32_t sw0[4], sw1[4];
+#pragma unroll
+    for (int mt = 0; mt < 4; mt++) {
+        sw0[mt] = lds16(S + mt * 16 * SB);
+        sw1[mt] = lds16(S + (mt * 16 + 8) * SB);
+    }
+#pragma unroll
+    for (int t = 0; t < T; t++) {
+        uint32_t hi[NT][4], lo[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
+            if (bval[nt]) {
+                const float* src = hrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i;
+                va = __ldcg(reinterpret_cast<const float4*>(src));
+                vb = __ldcg(reinterpret_cast<const float4*>(src + 4));
+            }
+            const float v[8] = {va.x * hs[nt], va.y * hs[nt], va.z * hs[nt],
+                                va.w * hs[nt], vb.x * hs[nt], vb.y * hs[nt],
+                                vb.z * hs[nt], vb.w * hs[nt]};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const __half2 hh = __floats2half2_rn(v[2 * e], v[2 * e + 1]);
+                const float2 back = __half22float2(hh);
+                hi[nt][e] = *reinterpret_cast<const uint32_t*>(&hh);
+                lo[nt][e] = pack_h2(v[2 * e] - back.x, v[2 * e + 1] - back.y);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 4; mt++) {
+            uint32_t a0[4], a1[4];
+            load_a_fast<FMT>(st + aoff[t] + mt * 2048, a0, a1);
+            const float s0 = scale_t<FMT>(sw0[mt], t), s1 = scale_t<FMT>(sw1[mt], t);
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                {
+                    float pp[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_f16(pp, a0[0], a0[1], a0[2], a0[3], hi[nt][0], hi[nt][1]);
+                    mma_f16(pp, a1[0], a1[1], a1[2], a1[3], hi[nt][2], hi[nt][3]);
+                    mma_f16(pp, a0[0], a0[1], a0[2], a0[3], lo[nt][0], lo[nt][1]);
+                    mma_f16(pp, a1[0], a1[1], a1[2], a1[3], lo[nt][2], lo[nt][3]);
+                    fma4(acc[mt][nt], s0, s1, pp);
+                }
+            }
+        }
+    }
+}
+
 // the block rows behind pair column `col` of expert v
 struct ItemCtx {
     int v, r, NT, pb, u_off;
@@ -374,8 +550,8 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
         if (pending & (1u << s)) mbar_wait(&full[s], (pending_par >> s) & 1u);
 }
 
-template <int FR, int FS>
-__device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* red, uint64_t* full,
+template <int FR, int FS, bool FAST>
+__device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* red_base, uint64_t* full,
                          uint64_t* empty, const Meta* meta) {
     const int tid = threadIdx.x, cw = tid >> 5, lane = tid & 31;
     const int S = p.n_shared, N = p.n_rows;
@@ -385,9 +561,9 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
     const float* hrow[EX_NT];
     float hs[EX_NT];
     bool bval[EX_NT];
-    float ag[EX_NT][4], au[EX_NT][4];
     float acc[4][EX_NT][4];
     int type = IT_GU, blk = 0;
+    uint32_t items_done = 0;
 
     while (true) {
         if (!mbar_wait(&full[stage], phase)) {
@@ -433,7 +609,6 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
                 }
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
-                    ag[nt][t] = au[nt][t] = 0.f;
 #pragma unroll
                     for (int mt = 0; mt < 4; mt++) acc[mt][nt][t] = 0.f;
                 }
@@ -460,16 +635,44 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
             }
         }
         const uint32_t st = smem_u32(ring + (size_t)stage * EX_STAGE);
-        if (type == IT_GU) {
-            if (c.shared)
-                gu_stage<FS>(st, p.geom[2], m.chunk, cw, lane, c.NT, xrow, bval, ag, au);
-            else
-                gu_stage<FR>(st, p.geom[0], m.chunk, cw, lane, c.NT, xrow, bval, ag, au);
+        if constexpr (FAST) {
+            if (type == IT_GU) {
+                if (c.shared) {
+                    if (c.NT == 1)
+                        gu_stage_fast<FS, Tiles<FS>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                    else
+                        gu_stage_fast<FS, Tiles<FS>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                } else {
+                    if (c.NT == 1)
+                        gu_stage_fast<FR, Tiles<FR>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                    else
+                        gu_stage_fast<FR, Tiles<FR>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                }
+            } else {
+                if (c.shared) {
+                    if (c.NT == 1)
+                        dn_stage_fast<FS, Tiles<FS>::T_DN, 1>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                    else
+                        dn_stage_fast<FS, Tiles<FS>::T_DN, 2>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                } else {
+                    if (c.NT == 1)
+                        dn_stage_fast<FR, Tiles<FR>::T_DN, 1>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                    else
+                        dn_stage_fast<FR, Tiles<FR>::T_DN, 2>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                }
+            }
         } else {
-            if (c.shared)
-                dn_stage<FS>(st, p.geom[3], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
-            else
-                dn_stage<FR>(st, p.geom[1], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
+            if (type == IT_GU) {
+                if (c.shared)
+                    gu_stage<FS>(st, p.geom[2], m.chunk, cw, lane, c.NT, xrow, bval, acc[0], acc[1]);
+                else
+                    gu_stage<FR>(st, p.geom[0], m.chunk, cw, lane, c.NT, xrow, bval, acc[0], acc[1]);
+            } else {
+                if (c.shared)
+                    dn_stage<FS>(st, p.geom[3], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
+                else
+                    dn_stage<FR>(st, p.geom[1], m.chunk, cw, lane, c.NT, hrow, hs, bval, acc);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
@@ -480,16 +683,21 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
         if (m.chunk != m.nchunks - 1) continue;
 
         // ---- item epilogue: fixed-order reduction over the consumer warps ----
-        consumer_sync<EX_CT>();
+        // (two buffers alternate between items, so one barrier per item suffices
+        // before the reads: a warp writing item i+1 cannot overwrite item i's data)
+        float* red = red_base;
         if (type == IT_GU) {
+            red = red_base + (items_done & 1u) * EX_RED_GU;
+            items_done++;
 #pragma unroll
             for (int nt = 0; nt < EX_NT; nt++)
 #pragma unroll
                 for (int t = 0; t < 4; t++) {
-                    red[((cw * 2 + 0) * EX_NT + nt) * 128 + t * 32 + lane] = ag[nt][t];
-                    red[((cw * 2 + 1) * EX_NT + nt) * 128 + t * 32 + lane] = au[nt][t];
+                    red[((cw * 2 + 0) * EX_NT + nt) * 128 + t * 32 + lane] = acc[0][nt][t];
+                    red[((cw * 2 + 1) * EX_NT + nt) * 128 + t * 32 + lane] = acc[1][nt][t];
                 }
             consumer_sync<EX_CT>();
+            bool wrote = false;
             for (int idx = tid; idx < c.NT * 128; idx += EX_CT) {
                 const int nt = idx >> 7, t = (idx >> 5) & 3, ln = idx & 31;
                 float gs = 0.f, us = 0.f;
@@ -513,16 +721,20 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
                         p.dbg_u[o] = us;
                     }
                     amax = __float_as_uint(hv) & 0x7FFFFFFFu;
+                    wrote = true;
                 }
                 amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
                 amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
                 amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
                 if (ln < 4 && col < c.r) atomicMax(p.hmax + c.pb + col, amax);
             }
-            __threadfence();
+            if (wrote) __threadfence();
             consumer_sync<EX_CT>();
             if (tid == 0) red_release_add(p.gu_done + c.v, 1u);
         } else {
+            // the down item needs the whole buffer: wait for every reader of the last item
+            consumer_sync<EX_CT>();
+            items_done = 0;
 #pragma unroll
             for (int mt = 0; mt < 4; mt++)
 #pragma unroll
@@ -552,7 +764,7 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
     }
 }
 
-template <int FR, int FS>
+template <int FR, int FS, bool FAST>
 __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_constant__ ExParams p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -580,7 +792,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         if (tid == EX_CT) producer(p, V, ring, full, empty, meta);
         return;
     }
-    consumer<FR, FS>(p, V, ring, red, full, empty, meta);
+    consumer<FR, FS, FAST>(p, V, ring, red, full, empty, meta);
 
     // the last CTA to finish leaves the workspace clean for the next call
     consumer_sync<EX_CT>();
@@ -639,6 +851,7 @@ static bool make_geom(Geom& g, int fmt, bool gu, int K, int rows_total) {
     if (!g.flat && rsb % 16) return false;
     if (rows_total % g.rows_item) return false;
     g.tx = (uint32_t)((gu ? 2 : 1) * (g.nbox * g.bi * g.rows_item + g.rows_item * g.sb));
+    g.fast = (g.bi == 128 && g.cb == cap) ? 1 : 0;
     return true;
 }
 
@@ -705,19 +918,27 @@ static int sm_count() {
     return n;
 }
 
-template <int FR, int FS>
-static int launch_expert_kernel(const ExParams& p, cudaStream_t stream) {
+template <int FR, int FS, bool FAST>
+static int launch_variant(const ExParams& p, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(expert_kernel<FR, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)EX_SMEM) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(expert_kernel<FR, FS, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)EX_SMEM) != cudaSuccess)
             return MOE_ERR_CUDA;
         attr = true;
     }
-    const int grid = sm_count();
+    const int grid = sm_count() * EX_CTAS_PER_SM;
     if (grid <= 0) return MOE_ERR_CUDA;
-    expert_kernel<FR, FS><<<grid, EX_THREADS, EX_SMEM, stream>>>(p);
+    expert_kernel<FR, FS, FAST><<<grid, EX_THREADS, EX_SMEM, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// The unrolled fast paths serve every matrix of the job when all their stages
+// are full width (the Kimi shapes); other shapes take the generic paths.
+template <int FR, int FS>
+static int launch_expert_kernel(const ExParams& p, cudaStream_t stream) {
+    const bool fast = p.geom[0].fast && p.geom[1].fast && p.geom[2].fast && p.geom[3].fast;
+    return fast ? launch_variant<FR, FS, true>(p, stream) : launch_variant<FR, FS, false>(p, stream);
 }
 
 }  // namespace moe
@@ -778,7 +999,7 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     p.n_shared = n_shared;
     p.n_gu = f / 16;
     p.n_dn = d / 64;
-    p.lag = 2;
+    p.lag = 4;
     p.debug_gu = (mode & MOE_MODE_DEBUG_GU) ? 1 : 0;
     p.accum = 0;
     p.expert_slot = expert_slot;

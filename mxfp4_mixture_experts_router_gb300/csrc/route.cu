@@ -49,20 +49,6 @@ struct RouteParams {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// (a, ia) ranks above (b, ib): larger value first, equal values by lower index,
-// NaN after every number; index >= E marks "no candidate".
-__device__ __forceinline__ bool ranks_above(float a, int ia, float b, int ib, int E) {
-    if (ib >= E) return ia < E;
-    if (ia >= E) return false;
-    const bool na = isnan(a), nb = isnan(b);
-    if (na != nb) return nb;
-    if (!na) {
-        if (a > b) return true;
-        if (a < b) return false;
-    }
-    return ia < ib;
-}
-
 // Activation preparation for the expert kernel: x16 = f16(x * 2^-p), p chosen
 // from the row's largest magnitude so the row sits inside the f16 range.
 __device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float* red) {
@@ -166,51 +152,64 @@ __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N]
     }
 }
 
-// top-k of one row by one warp; writes idx/w and returns nothing.
+// Rank key of (logit, expert): a larger key ranks higher.  The high word is an
+// order-preserving image of the float (NaN below every number, -0 equal to +0),
+// the low word the complement of the index (ties go to the lower index).
+__device__ __forceinline__ uint64_t rank_key(float v, int e) {
+    uint32_t b = __float_as_uint(v);
+    b = (b == 0x80000000u) ? 0u : b;
+    uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    ord = isnan(v) ? 0u : ord;
+    return ((uint64_t)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, o);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), o);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+// top-k of one row by one warp: lane l holds experts l, l+32, ...; each round the
+// warp takes the largest key, and only the lane that held it rescans its own.
 __device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2) {
     const int lane = threadIdx.x & 31;
     const int T = (p.E + 31) / 32;
-    float v[32];
+    uint64_t key[32];
     bool any_nan = false;
 #pragma unroll
     for (int t = 0; t < 32; t++) {
         const int e = lane + 32 * t;
-        v[t] = 0.f;
+        key[t] = 0ull;  // "no candidate": every real key, NaN included, has a non-zero low word
         if (t < T && e < p.E) {
-            v[t] = from_l2 ? __ldcg(lrow + e) : lrow[e];
-            any_nan |= isnan(v[t]);
+            const float v = from_l2 ? __ldcg(lrow + e) : lrow[e];
+            any_nan |= isnan(v);
+            key[t] = rank_key(v, e);
         }
     }
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(p.ctrl, MOE_EBIT_NAN);
-    uint32_t taken = 0;
-    float my_val = 0.f;
-    int my_idx = p.E;
-    for (int j = 0; j < p.k; j++) {
-        float bv = 0.f;
-        int bi = p.E;
+    uint64_t local = 0ull;
 #pragma unroll
-        for (int t = 0; t < 32; t++) {
-            const int e = lane + 32 * t;
-            if (t < T && e < p.E && !((taken >> t) & 1u) && ranks_above(v[t], e, bv, bi, p.E)) {
-                bv = v[t];
-                bi = e;
-            }
-        }
+    for (int t = 0; t < 32; t++) local = key[t] > local ? key[t] : local;
+    uint64_t mine = 0ull;
+    for (int j = 0; j < p.k; j++) {
+        uint64_t best = local;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ranks_above(ov, oi, bv, bi, p.E)) {
-                bv = ov;
-                bi = oi;
+            const uint64_t other = shfl_xor_u64(best, o);
+            best = other > best ? other : best;
+        }
+        if (lane == j) mine = best;
+        if (best == local) {  // this lane held the winner: drop it and rescan
+            local = 0ull;
+#pragma unroll
+            for (int t = 0; t < 32; t++) {
+                if (key[t] == best) key[t] = 0ull;
+                local = key[t] > local ? key[t] : local;
             }
         }
-        if (bi < p.E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) {
-            my_val = bv;
-            my_idx = bi;
-        }
     }
+    const int my_idx = (int)(0xFFFFFFFFu - (uint32_t)mine);
+    const float my_val = (lane < p.k) ? (from_l2 ? __ldcg(lrow + my_idx) : lrow[my_idx]) : 0.f;
     // weights: exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in slot order
     const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
     const float ex = (lane < p.k) ? expf(my_val - l0) : 0.f;
