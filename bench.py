@@ -9,7 +9,7 @@ seeded N(0,1) rows, timed one at a time.  A step is one whole layer
 
 Metric: HBM GB/s on the unique MXFP4 expert bytes the layer reads (16 experts x
 17,547,264 B per row), i.e. unique expert bytes / layer time.  Inputs are
-resident in HBM; L2 is flushed (256 MB write) before every timed step, outside
+resident in HBM; L2 is flushed (256 MB write + 256 MB read) before every timed step, outside
 the timed events.  Extra keys report 8- and 16-row verification blocks and the
 roofline of the expert kernel.
 
@@ -46,6 +46,21 @@ ROUTER_BYTES = 896 * 7168 * 2
 METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Cold-L2 reset between timed steps: write a 256 MB buffer (larger than the
+    129 MB L2), then read a second 256 MB buffer so the L2 ends up holding clean
+    lines and the timed step does not pay for the flush's own write-backs."""
+
+    def __init__(self, torch, dev):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+
+    def zero_(self):
+        self.w.zero_()
+        self.sink.copy_(self.r.sum())
 
 
 def load_peaks():
@@ -200,48 +215,60 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     xs = syn.x_rows(SEED, range(N_ROWS_SEEDED), syn.KIMI.d_model)
     X = torch.from_numpy(xs.view(np.int16)).to(dev).view(torch.uint16)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flusher = L2Flush(torch, dev)
+    flush = flusher
     K, W = args.steps, args.warmup
 
-    def layer_step(i, kev=None):
-        x = X[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1]
-        lay.route(1, x)
-        if kev:
-            kev[0].record()
-        lay.experts(1)
-        if kev:
-            kev[1].record()
-        lay.combine(1, x)
-
+    # one captured graph per step: route -> experts -> combine, timing events inside
+    Xs = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
+    Xs.copy_(X[:1])
+    graph, gev = lay.capture(Xs, Xs, events=True)
     for i in range(W):
         flush.zero_()
-        layer_step(i)
+        Xs.copy_(X[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1])
+        graph.replay()
     torch.cuda.synchronize()
     assert lay.error_bits() == 0
+    gev = timeable(gev)
 
     props = torch.cuda.get_device_properties(dev)
     bus = getattr(props, "pci_bus_id", None)
     sampler = ClockSampler(bus if isinstance(bus, str) else None)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    layer_ms, kern_ms = [], []
+    outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     sampler.start()
     t_wall = time.perf_counter()
     for i in range(K):
+        r = (W + i) % N_ROWS_SEEDED
         flush.zero_()
-        ev[i][0].record()
-        layer_step(W + i, kev[i])
-        ev[i][1].record()
-    torch.cuda.synchronize()
+        Xs.copy_(X[r: r + 1])
+        outer[i][0].record()
+        graph.replay()
+        outer[i][1].record()
+        torch.cuda.synchronize()
+        if gev is not None:
+            layer_ms.append(gev[0].elapsed_time(gev[3]))
+            kern_ms.append(gev[1].elapsed_time(gev[2]))
+        else:
+            layer_ms.append(outer[i][0].elapsed_time(outer[i][1]))
     wall = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     assert lay.error_bits() == 0
-    layer_ms = [a.elapsed_time(b) for a, b in ev]
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    if not kern_ms:  # no events inside the graph: time the expert kernel on its own
+        for i in range(K):
+            flush.zero_()
+            lay.route(1, Xs)
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record()
+            lay.experts(1)
+            b_.record()
+            torch.cuda.synchronize()
+            kern_ms.append(a_.elapsed_time(b_))
     total_ms = sum(layer_ms)
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
@@ -256,21 +283,21 @@ def run_ours(args, rank, world):
     peak, peak_kind = load_peaks()
     achieved = kern_bytes / kern_avg_s / 1e9
 
-    # end to end through the public API: pinned host input -> layer -> pinned host output
+    # end to end through the public API: pinned host row -> graph replay -> pinned host output
     xh = torch.from_numpy(xs.view(np.int16)).view(torch.uint16).pin_memory()
     oh = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16).pin_memory()
-    xd = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
     e2e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for i in range(K + W):
+        r = i % N_ROWS_SEEDED
         flush.zero_()
         if i >= W:
             e2e[i - W][0].record()
-        xd.copy_(xh[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1], non_blocking=True)
-        out = lay.forward(xd, xd, n_rows=1)
-        oh.copy_(out, non_blocking=True)
+        Xs.copy_(xh[r: r + 1], non_blocking=True)
+        graph.replay()
+        oh.copy_(lay.out[:1], non_blocking=True)
         if i >= W:
             e2e[i - W][1].record()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
@@ -293,7 +320,8 @@ def run_ours(args, rank, world):
         "dtype": "mxfp4 weights x f16 activations, fp32 accumulate, bf16 out", "data": "synthetic",
         "config": {"workload": "Kimi K3.1 MoE layer decode, 1 row/step: d=7168 f=1536 E=896 top-16 + 2 Q8_0 "
                                "shared, all experts resident, 100 seeded rows",
-                   "rows_per_step": 1, "l2": "flushed before every step (256 MB write), outside the events",
+                   "rows_per_step": 1,
+                   "l2": "flushed before every step (256 MB write, then 256 MB read), outside the events",
                    "parallelism": f"replicas x{world}", "blocks_sigma0.5": blocks},
         "layer_us_p10_p50_p90": [float(np.percentile(layer_ms, q)) * 1e3 for q in (10, 50, 90)],
         "all_bytes_gbs": world * K * all_bytes / (total_ms * 1e-3) / 1e9,
@@ -304,26 +332,52 @@ def run_ours(args, rank, world):
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
                 "d2h_bytes_per_step": syn.KIMI.d_model * 2},
         "gpu_launches": K * 3,
+        "timing": "one CUDA graph per step (route, experts, combine), events inside the graph"
+                  if gev is not None else "one CUDA graph per step, events around the replay",
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
     return line
 
 
+def timeable(evs):
+    """The graph's timing events if the runtime lets them be timed, else None."""
+    if evs is None:
+        return None
+    try:
+        evs[0].elapsed_time(evs[3])
+        return evs
+    except Exception:
+        return None
+
+
 def time_blocks(torch, lay, X, flush, n, reps):
-    """Verification blocks of n rows: shared N(0,1) base logits + N(0, 0.5) per-row noise."""
+    """Verification blocks of n rows: shared N(0,1) base logits + N(0, 0.5) per-row noise,
+    one captured graph replayed per block."""
+    dev = X.device
+    Xs = torch.empty((n, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
+    Ls = torch.empty((n, syn.KIMI.n_experts), dtype=torch.float32, device=dev)
+    lgs = [torch.from_numpy(syn.block_logits(SEED, n, syn.KIMI.n_experts, 0.5, block=b)).to(dev)
+           for b in range(reps + 3)]
+    Xs.copy_(X[:n])
+    Ls.copy_(lgs[0])
+    graph, gev = lay.capture(Xs, Xs, logits_in=Ls, events=True)
+    graph.replay()
+    torch.cuda.synchronize()
+    gev = timeable(gev)
     ts, us = [], []
     for b in range(reps + 3):
-        lg = torch.from_numpy(syn.block_logits(SEED, n, syn.KIMI.n_experts, 0.5, block=b)).to(X.device)
-        x = X[(b * n) % (N_ROWS_SEEDED - n): (b * n) % (N_ROWS_SEEDED - n) + n]
+        x0 = (b * n) % (N_ROWS_SEEDED - n)
         flush.zero_()
+        Xs.copy_(X[x0: x0 + n])
+        Ls.copy_(lgs[b])
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        lay.forward(x, x, logits_in=lg)
+        graph.replay()
         e1.record()
         torch.cuda.synchronize()
         if b >= 3:
-            ts.append(e0.elapsed_time(e1))
+            ts.append(gev[0].elapsed_time(gev[3]) if gev is not None else e0.elapsed_time(e1))
             us.append(int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item()))
     t = statistics.median(ts)
     u = statistics.mean(us)
@@ -359,7 +413,7 @@ def run_profile_case(args):
     lay.set_expert_slots(slots)
     lay.set_shared([syn.q8_0_shared_slab(SEED, s, sh) for s in range(2)])
     X = torch.from_numpy(x.view(np.int16)).cuda().view(torch.uint16)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush(torch, torch.device("cuda"))
     for _ in range(4):
         flush.zero_()
         lay.forward(X, X)

@@ -158,6 +158,7 @@ MOE_API int moe_workspace_offsets(const moe_desc* desc, int32_t n_rows_max, int3
  * and groups the block's (row, slot) pairs by expert for moe_expert_block.
  *
  *  n_rows      1..n_rows_max of the workspace; the GEMV path needs n_rows <= 32
+ *              and d_model <= 8192
  *  x           bf16 [n_rows][d] activations, row-major; may be NULL only when
  *              logits_in is given and no moe_expert_block call follows
  *  w_router    bf16 [E][d] router matrix, row-major (ignored with logits_in)

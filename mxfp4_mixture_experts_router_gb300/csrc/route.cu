@@ -22,6 +22,7 @@ constexpr int RT_THREADS = 256;
 constexpr int RT_KS = 512;      // K elements per slice
 constexpr int RT_EG = 64;       // experts per group (8 per warp)
 constexpr int RT_MAX_ROWS = 32;
+constexpr int RT_MAX_KS = 16;   // K slices: d <= 8192
 constexpr int RT_TICKET_EG = 32;  // ctrl words [32, 64) hold the per-group tickets
 
 struct RouteParams {
@@ -50,11 +51,31 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 // Activation preparation for the expert kernel: x16 = f16(x * 2^-p), p chosen
-// from the row's largest magnitude so the row sits inside the f16 range.
+// from the row's largest magnitude so the row sits inside the f16 range.  Rows of
+// up to 8192 elements stay in registers between the max and the conversion (all
+// 16-byte loads issued before any is used); longer rows are read twice.
 __device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float* red) {
+    constexpr int PER = 4;  // 16-byte chunks per thread and pass
     const int tid = threadIdx.x;
+    const int nv = d / 8;
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint4* ov = reinterpret_cast<uint4*>(x16);
+    const bool resident = nv <= PER * (int)blockDim.x;
+    uint4 v[PER];
     uint32_t mx = 0;
-    for (int c = tid; c < d; c += blockDim.x) mx = max(mx, (uint32_t)(x[c] & 0x7FFFu) << 16);
+    for (int base = 0; base < nv; base += PER * blockDim.x) {
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            const int c = base + j * blockDim.x + tid;
+            v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int t = 0; t < 4; t++) mx = max(mx, max((w[t] & 0x7FFFu) << 16, w[t] & 0x7FFF0000u));
+        }
+    }
     for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((tid & 31) == 0) red[tid >> 5] = __uint_as_float(mx);
     __syncthreads();
@@ -66,101 +87,158 @@ __device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float
     __syncthreads();
     const int p = (int)__float_as_uint(red[32]);
     const float s = exp2i(-p);
-    for (int c = tid; c < d; c += blockDim.x) x16[c] = __float2half_rn(bf16_lo(x[c]) * s);
+    for (int base = 0; base < nv; base += PER * blockDim.x) {
+        if (!resident) {
+#pragma unroll
+            for (int j = 0; j < PER; j++) {
+                const int c = base + j * blockDim.x + tid;
+                v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < PER; j++) {
+            const int c = base + j * blockDim.x + tid;
+            if (c >= nv) continue;
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; t++) {
+                const __half2 h = __floats2half2_rn(bf16_lo(w[t]) * s, bf16_hi(w[t]) * s);
+                o[t] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            ov[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
     if (tid == 0) *xexp = p;
     __syncthreads();
 }
 
-__device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N][RT_KS]*/) {
+__device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N][32][17]*/) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int KS = min(RT_KS, p.d);
     const int k0 = ks * KS;
-    // stage the x slice of every row (fp32)
-    for (int i = tid; i < p.N * KS; i += RT_THREADS) {
-        const int n = i / KS, c = i - n * KS;
-        xs[n * RT_KS + c] = bf16_lo(p.x[(size_t)n * p.d + k0 + c]);
-    }
-    // every lane loads its 16 K of the warp's 8 experts up front
     const int per_lane = KS / 32;  // 16 (or fewer for small d)
-    uint4 wv[8][2];
-    int e0 = eg * RT_EG + warp * 8;
+    // the warp's 8 experts are done in two batches of 4; each lane loads its 16 K of
+    // a batch up front (the first batch's loads overlap the staging of x)
+    const int e0 = eg * RT_EG + warp * 8;
+    uint4 wv[4][2];
+    auto load_batch = [&](int jb) {
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-        const int e = e0 + j;
+        for (int j = 0; j < 4; j++) {
+            const int e = e0 + 4 * jb + j;
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            wv[j][h] = make_uint4(0, 0, 0, 0);
-            if (e < p.E && h * 8 < per_lane) {
-                const uint16_t* src = p.w + (size_t)e * p.d + k0 + lane * per_lane + h * 8;
-                wv[j][h] = __ldg(reinterpret_cast<const uint4*>(src));
+            for (int h = 0; h < 2; h++) {
+                wv[j][h] = make_uint4(0, 0, 0, 0);
+                if (e < p.E && h * 8 < per_lane) {
+                    const uint16_t* src = p.w + (size_t)e * p.d + k0 + lane * per_lane + h * 8;
+                    wv[j][h] = __ldg(reinterpret_cast<const uint4*>(src));
+                }
+            }
+        }
+    };
+    load_batch(0);
+    // stage the x slice of every row (fp32) while the weight loads are in flight:
+    // row n, lane l's 16 values at xs[(n*32 + l)*17 + c] (padded: conflict-free reads)
+    {
+        const int nv = p.N * KS / 8;  // 16-byte chunks of the x slice
+        for (int base = 0; base < nv; base += 4 * RT_THREADS) {
+            uint4 xv[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int c = base + j * RT_THREADS + tid;
+                xv[j] = make_uint4(0, 0, 0, 0);
+                if (c < nv) {
+                    const int n = c / (KS / 8), off = (c - n * (KS / 8)) * 8;
+                    xv[j] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)n * p.d + k0 + off));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; j++) {
+                const int c = base + j * RT_THREADS + tid;
+                if (c >= nv) continue;
+                const int n = c / (KS / 8), off = (c - n * (KS / 8)) * 8;
+                const uint32_t w[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
+#pragma unroll
+                for (int t = 0; t < 8; t++) {
+                    const int kk = off + t;  // element of the slice
+                    const int l = kk / per_lane, cc = kk - l * per_lane;
+                    xs[(n * 32 + l) * 17 + cc] = (t & 1) ? bf16_hi(w[t >> 1]) : bf16_lo(w[t >> 1]);
+                }
             }
         }
     }
     __syncthreads();
-    for (int n = 0; n < p.N; n++) {
-        float xr[16];
+    for (int jb = 0; jb < 2; jb++) {
+        if (jb == 1) load_batch(1);
+        for (int n = 0; n < p.N; n++) {
+            float xr[16];
 #pragma unroll
-        for (int c = 0; c < 16; c++) xr[c] = (c < per_lane) ? xs[n * RT_KS + lane * per_lane + c] : 0.f;
-        float s[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-            float a = 0.f;
-#pragma unroll
-            for (int h = 0; h < 2; h++) {
-                const uint32_t q[4] = {wv[j][h].x, wv[j][h].y, wv[j][h].z, wv[j][h].w};
-#pragma unroll
-                for (int t = 0; t < 4; t++) {
-                    a = fmaf(xr[h * 8 + 2 * t], bf16_lo(q[t]), a);
-                    a = fmaf(xr[h * 8 + 2 * t + 1], bf16_hi(q[t]), a);
-                }
-            }
-            s[j] = a;
-        }
-        // transposed butterfly: after 5 levels lane l holds the full sum of
-        // expert ((l>>4)&1)*4 + ((l>>3)&1)*2 + ((l>>2)&1)
-        {
-            const bool up = lane & 16;
+            for (int c = 0; c < 16; c++) xr[c] = (c < per_lane) ? xs[(n * 32 + lane) * 17 + c] : 0.f;
+            float s4[4];
 #pragma unroll
             for (int j = 0; j < 4; j++) {
-                const float send = up ? s[j] : s[j + 4];
-                const float keep = up ? s[j + 4] : s[j];
-                s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-        }
-        {
-            const bool up = lane & 8;
+                float a = 0.f;
 #pragma unroll
-            for (int j = 0; j < 2; j++) {
-                const float send = up ? s[j] : s[j + 2];
-                const float keep = up ? s[j + 2] : s[j];
-                s[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+                for (int h = 0; h < 2; h++) {
+                    const uint32_t q[4] = {wv[j][h].x, wv[j][h].y, wv[j][h].z, wv[j][h].w};
+#pragma unroll
+                    for (int t = 0; t < 4; t++) {
+                        a = fmaf(xr[h * 8 + 2 * t], bf16_lo(q[t]), a);
+                        a = fmaf(xr[h * 8 + 2 * t + 1], bf16_hi(q[t]), a);
+                    }
+                }
+                s4[j] = a;
             }
-        }
-        {
-            const bool up = lane & 4;
-            const float send = up ? s[0] : s[1];
-            const float keep = up ? s[1] : s[0];
-            s[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-        }
-        s[0] += __shfl_xor_sync(0xffffffffu, s[0], 2);
-        s[0] += __shfl_xor_sync(0xffffffffu, s[0], 1);
-        if ((lane & 3) == 0) {
-            const int j = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-            const int e = e0 + j;
-            if (e < p.E) p.part[((size_t)ks * p.N + n) * p.E + e] = s[0];
+            // transposed butterfly: after 5 levels lane l holds the full sum of
+            // expert ((l>>4)&1)*2 + ((l>>3)&1) of the batch
+            {
+                const bool up = lane & 16;
+#pragma unroll
+                for (int j = 0; j < 2; j++) {
+                    const float send = up ? s4[j] : s4[j + 2];
+                    const float keep = up ? s4[j + 2] : s4[j];
+                    s4[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+                }
+            }
+            {
+                const bool up = lane & 8;
+                const float send = up ? s4[0] : s4[1];
+                const float keep = up ? s4[1] : s4[0];
+                s4[0] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+            }
+            s4[0] += __shfl_xor_sync(0xffffffffu, s4[0], 4);
+            s4[0] += __shfl_xor_sync(0xffffffffu, s4[0], 2);
+            s4[0] += __shfl_xor_sync(0xffffffffu, s4[0], 1);
+            if ((lane & 7) == 0) {
+                const int j = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+                const int e = e0 + 4 * jb + j;
+                if (e < p.E) p.part[((size_t)ks * p.N + n) * p.E + e] = s4[0];
+            }
         }
     }
 }
 
-// Rank key of (logit, expert): a larger key ranks higher.  The high word is an
-// order-preserving image of the float (NaN below every number, -0 equal to +0),
-// the low word the complement of the index (ties go to the lower index).
-__device__ __forceinline__ uint64_t rank_key(float v, int e) {
+// Order-preserving image of a logit: a larger key means a larger value; NaN maps
+// below every number and -0 to +0.
+__device__ __forceinline__ uint32_t order_key(float v) {
     uint32_t b = __float_as_uint(v);
     b = (b == 0x80000000u) ? 0u : b;
     uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    ord = isnan(v) ? 0u : ord;
-    return ((uint64_t)ord << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e);
+    return isnan(v) ? 0u : ord;
+}
+
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// largest of 32 keys by a pairwise tree (depth 5)
+__device__ __forceinline__ uint64_t tree_max32(const uint64_t (&k)[32]) {
+    uint64_t m16[16], m8[8], m4[4];
+#pragma unroll
+    for (int i = 0; i < 16; i++) m16[i] = umax64(k[2 * i], k[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 8; i++) m8[i] = umax64(m16[2 * i], m16[2 * i + 1]);
+#pragma unroll
+    for (int i = 0; i < 4; i++) m4[i] = umax64(m8[2 * i], m8[2 * i + 1]);
+    return umax64(umax64(m4[0], m4[1]), umax64(m4[2], m4[3]));
 }
 
 __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
@@ -169,43 +247,39 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
     return ((uint64_t)hi << 32) | lo;
 }
 
-// top-k of one row by one warp: lane l holds experts l, l+32, ...; each round the
-// warp takes the largest key, and only the lane that held it rescans its own.
+// top-k of one row by one warp.  A candidate's key is (order_key(logit) << 32) |
+// (0xFFFFFFFF - expert): the larger key ranks higher (larger logit, then lower
+// index, NaN last); 0 means "no candidate".  Lane l holds experts l, l+32, ...;
+// each round the warp takes the largest key and the lane that held it rescans.
 __device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2) {
     const int lane = threadIdx.x & 31;
-    const int T = (p.E + 31) / 32;
+    float v[32];
+#pragma unroll
+    for (int t = 0; t < 32; t++) {  // every load in flight before any is used
+        const int e = min(lane + 32 * t, p.E - 1);
+        v[t] = from_l2 ? __ldcg(lrow + e) : lrow[e];
+    }
     uint64_t key[32];
     bool any_nan = false;
 #pragma unroll
     for (int t = 0; t < 32; t++) {
         const int e = lane + 32 * t;
-        key[t] = 0ull;  // "no candidate": every real key, NaN included, has a non-zero low word
-        if (t < T && e < p.E) {
-            const float v = from_l2 ? __ldcg(lrow + e) : lrow[e];
-            any_nan |= isnan(v);
-            key[t] = rank_key(v, e);
-        }
+        const bool ok = e < p.E;
+        any_nan |= ok && isnan(v[t]);
+        key[t] = ok ? (((uint64_t)order_key(v[t]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e)) : 0ull;
     }
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(p.ctrl, MOE_EBIT_NAN);
-    uint64_t local = 0ull;
-#pragma unroll
-    for (int t = 0; t < 32; t++) local = key[t] > local ? key[t] : local;
+    uint64_t local = tree_max32(key);
     uint64_t mine = 0ull;
     for (int j = 0; j < p.k; j++) {
         uint64_t best = local;
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const uint64_t other = shfl_xor_u64(best, o);
-            best = other > best ? other : best;
-        }
+        for (int o = 16; o; o >>= 1) best = umax64(best, shfl_xor_u64(best, o));
         if (lane == j) mine = best;
-        if (best == local) {  // this lane held the winner: drop it and rescan
-            local = 0ull;
+        if (best == local) {
 #pragma unroll
-            for (int t = 0; t < 32; t++) {
-                if (key[t] == best) key[t] = 0ull;
-                local = key[t] > local ? key[t] : local;
-            }
+            for (int t = 0; t < 32; t++) key[t] = (key[t] == best) ? 0ull : key[t];
+            local = tree_max32(key);
         }
     }
     const int my_idx = (int)(0xFFFFFFFFu - (uint32_t)mine);
@@ -292,7 +366,7 @@ __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, 
     }
 }
 
-__global__ void __launch_bounds__(RT_THREADS) route_kernel(const RouteParams p) {
+__global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(smem_raw);
     __shared__ float red[40];
@@ -315,11 +389,28 @@ __global__ void __launch_bounds__(RT_THREADS) route_kernel(const RouteParams p) 
             // sum the K slices in slice order for this group's experts
             const int e_lo = eg * RT_EG, e_hi = min(p.E, e_lo + RT_EG);
             const int span = e_hi - e_lo;
-            for (int i = tid; i < p.N * span; i += RT_THREADS) {
-                const int n = i / span, e = e_lo + (i - n * span);
-                float a = 0.f;
-                for (int ks2 = 0; ks2 < p.n_ks; ks2++) a += __ldcg(p.part + ((size_t)ks2 * p.N + n) * p.E + e);
-                p.logits[(size_t)n * p.E + e] = a;
+            for (int base = 0; base < p.N * span; base += 4 * RT_THREADS) {
+                float v[4][RT_MAX_KS];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int i = base + q * RT_THREADS + tid;
+                    const int n = i / span, e = e_lo + (i - n * span);
+#pragma unroll
+                    for (int ks2 = 0; ks2 < RT_MAX_KS; ks2++)
+                        v[q][ks2] = (ks2 < p.n_ks && i < p.N * span)
+                                        ? __ldcg(p.part + ((size_t)ks2 * p.N + n) * p.E + e) : 0.f;
+                }
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int i = base + q * RT_THREADS + tid;
+                    if (i >= p.N * span) continue;
+                    const int n = i / span, e = e_lo + (i - n * span);
+                    float a = 0.f;  // slices summed in slice order
+#pragma unroll
+                    for (int ks2 = 0; ks2 < RT_MAX_KS; ks2++)
+                        if (ks2 < p.n_ks) a += v[q][ks2];
+                    p.logits[(size_t)n * p.E + e] = a;
+                }
             }
             if (tid == 0) p.ctrl[RT_TICKET_EG + eg] = 0;
             group_finisher = true;
@@ -394,12 +485,12 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     const int KS = d < RT_KS ? d : RT_KS;
     p.n_ks = d / KS;
     p.n_eg = (E + RT_EG - 1) / RT_EG;
-    if (p.n_eg > 32) return MOE_ERR_UNSUPPORTED;
+    if (p.n_eg > 32 || p.n_ks > RT_MAX_KS) return MOE_ERR_UNSUPPORTED;
     // the partial logits must fit in the h buffer: n_ks * N * E floats
     if ((size_t)p.n_ks * n_rows * E * 4 > L.dbg_g - L.h) return MOE_ERR_UNSUPPORTED;
     p.n_gemv_ctas = logits_in ? 0 : p.n_ks * p.n_eg;
     int grid = p.n_gemv_ctas > n_rows ? p.n_gemv_ctas : n_rows;
-    const size_t smem = (size_t)RT_MAX_ROWS * RT_KS * 4;  // x slice (also covers the grouping tables)
+    const size_t smem = (size_t)RT_MAX_ROWS * 32 * 17 * 4;  // padded x slice (also covers the grouping tables)
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=

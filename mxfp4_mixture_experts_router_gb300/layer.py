@@ -111,5 +111,56 @@ class MoeLayer:
         self.combine(n, residual, stream=stream)
         return self.out[:n]
 
+    def capture(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
+                events: bool = False):
+        """Capture one block (route -> experts -> combine) into a CUDA graph.
+
+        The graph reads the block from the given device buffers (x, residual and, if
+        given, logits_in): refill them and call ``graph.replay()`` per block; the
+        output lands in ``self.out``.  Kernel parameters, including the TMA tensor
+        maps, are fixed at capture time.  With events=True, four timing events are
+        recorded inside the graph (before route, before experts, before combine, after
+        combine) and returned; the events are None if the runtime refuses them."""
+        import torch as _torch
+        n = x.shape[0] if n_rows is None else n_rows
+        side = _torch.cuda.Stream()
+        side.wait_stream(_torch.cuda.current_stream())
+        with _torch.cuda.stream(side):  # first launches (kernel attributes) outside the capture
+            self.forward(x, residual, n_rows=n, logits_in=logits_in, mode=mode)
+        _torch.cuda.current_stream().wait_stream(side)
+        _torch.cuda.synchronize()
+
+        def body(evs):
+            if evs:
+                evs[0].record()
+            self.route(n, x, logits_in=logits_in)
+            if evs:
+                evs[1].record()
+            self.experts(n, mode=mode)
+            if evs:
+                evs[2].record()
+            self.combine(n, residual)
+            if evs:
+                evs[3].record()
+
+        evs = None
+        if events:
+            try:  # external events are the ones a graph's event-record nodes can time
+                evs = [_torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+            except TypeError:
+                evs = None
+        g = _torch.cuda.CUDAGraph()
+        try:
+            with _torch.cuda.graph(g):
+                body(evs)
+        except RuntimeError:
+            if not events:
+                raise
+            evs = None
+            g = _torch.cuda.CUDAGraph()
+            with _torch.cuda.graph(g):
+                body(None)
+        return g, evs
+
     def error_bits(self, stream=None) -> int:
         return B.moe_get_error(self.ws, stream)
