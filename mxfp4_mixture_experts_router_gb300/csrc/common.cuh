@@ -24,12 +24,15 @@ enum Ctrl : int {
     CTRL_TICKET = 3,     // CTAs of the route kernel that finished
     CTRL_UNIQUE = 4,     // U: experts selected by the block
     CTRL_ROWS = 5,       // rows of the routed block
+    CTRL_WORK_TC = 6,    // next work item of the block-scaled tensor-core expert kernel
+    CTRL_EXIT_TC = 7,    // its finished CTAs
     CTRL_WORDS = 64
 };
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, total;
+    int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
 
@@ -55,6 +58,15 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.dbg_u = take((size_t)L.pairs * f * 4);
     L.shared_y = take((size_t)n_shared * N * d * 4);
     L.logits = take((size_t)N * E * 4);
+    // MX activations for the block-scaled expert kernel: 3 E4M3 rows per row of x
+    // and per routed pair of h, plus 64 rows of padding that a 64-row tile may read
+    L.mx_rows_x = 3 * N + 64;
+    L.mx_rows_h = 3 * N * k + 64;
+    L.x_mx = take((size_t)L.mx_rows_x * d);
+    L.x_sc = take((size_t)L.mx_rows_x * (d / 32));
+    L.h_mx = take((size_t)L.mx_rows_h * f);
+    L.h_sc = take((size_t)L.mx_rows_h * (f / 32));
+    L.gu_done_tc = take((size_t)E * 4);
     L.total = o;
     return L;
 }
@@ -206,6 +218,37 @@ __device__ __forceinline__ int f16_scale_exponent(uint32_t maxbits) {
     return p;
 }
 
+// One E4M3 code of v (round to nearest even, saturating) and its exact value.
+__device__ __forceinline__ uint32_t e4m3_code(float v, float& back) {
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(pair) : "f"(v));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    back = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    return pair & 0xFFu;
+}
+
+// Splits the 32 values of a block (one per lane) into three E4M3 terms with their
+// own power-of-two block scales, v ~ sum_t q_t * 2^(s_t - 127): each term codes the
+// residual of the previous ones, so about 12 significant bits survive.  Writes the
+// lane's three codes and, in every lane, the three E8M0 scale bytes.
+__device__ __forceinline__ void mx3_split(float v, uint32_t (&q)[3], uint32_t (&sbyte)[3]) {
+    float r = v;
+#pragma unroll
+    for (int t = 0; t < 3; t++) {
+        uint32_t m = __float_as_uint(r) & 0x7FFFFFFFu;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        int e = (int)(m >> 23) - 127 - 7;  // |r| / 2^e < 256 <= 448
+        e = m == 0u ? 0 : e;
+        e = e < -126 ? -126 : (e > 127 ? 127 : e);
+        float back;
+        q[t] = e4m3_code(r * exp2i(-e), back);
+        r -= back * exp2i(e);
+        sbyte[t] = (uint32_t)(e + 127);
+    }
+}
+
 // D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulate.
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -239,5 +282,11 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
+
+// the block-scaled tensor-core path for routed MXFP4 experts (experts_tc.cu)
+bool tc_expert_supported(int d, int f, int n_rows);
+int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool* routed, const int32_t* expert_slot,
+                     const uint32_t* slot_ready, int n_shared, void* ws, int n_rows_max, float* y_part,
+                     cudaStream_t stream);
 
 }  // namespace moe

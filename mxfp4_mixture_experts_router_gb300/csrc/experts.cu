@@ -60,6 +60,7 @@ struct ExParams {
     int top_k, n_rows, n_shared;
     int n_gu, n_dn, lag;
     int debug_gu, accum;
+    int routed_off;  // layer job without the routed experts (they run on the block-scaled path)
     const int* expert_slot;
     const uint32_t* slot_ready;
     int n_slots;
@@ -785,7 +786,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
     }
     __syncthreads();
     const int S = p.n_shared;
-    const int U = (p.job == J_LAYER) ? (int)p.ctrl[CTRL_UNIQUE] : 0;
+    const int U = (p.job == J_LAYER && !p.routed_off) ? (int)p.ctrl[CTRL_UNIQUE] : 0;
     const int V = S + U;
 
     if (tid >= EX_CT) {
@@ -1019,8 +1020,19 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     p.out_shared = reinterpret_cast<float*>(base + L.shared_y);
     p.y_part = y_part;
     p.pairs_cap = L.pairs;
-    return n_shared > 0 ? launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream))
-                        : launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (tc_expert_supported(d, f, n_rows)) {
+        // shared Q8_0 experts on the tensor-core MMA.sync engine, routed MXFP4
+        // experts on the block-scaled tcgen05 kernel
+        if (n_shared > 0) {
+            p.routed_off = 1;
+            const int st = launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
+            if (st != MOE_OK) return st;
+        }
+        return tc_expert_launch(desc, n_rows, mode, routed, expert_slot, slot_ready, n_shared, ws, n_rows_max, y_part,
+                                s);
+    }
+    return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -43,6 +43,9 @@ struct RouteParams {
     int* xexp;
     uint32_t* gu_done;
     uint32_t* hmax;
+    uint8_t* x_mx;        // [3N][d] E4M3 terms of x for the block-scaled expert kernel
+    uint8_t* x_sc;        // [3N][d/32] their E8M0 scales
+    uint32_t* gu_done_tc;
     int v_cap;
     int64_t pairs_cap;
 };
@@ -111,6 +114,22 @@ __device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float
     }
     if (tid == 0) *xexp = p;
     __syncthreads();
+}
+
+// Row x as three E4M3 terms with per-32 E8M0 block scales (rows 3n, 3n+1, 3n+2 of
+// the MX activation buffer): one warp per 32-element block.
+__device__ void prep_row_mx(const uint16_t* x, int d, int n, uint8_t* x_mx, uint8_t* x_sc) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int blk = warp; blk < d / 32; blk += nw) {
+        const float v = bf16_lo(__ldg(x + blk * 32 + lane));
+        uint32_t q[3], sb[3];
+        mx3_split(v, q, sb);
+#pragma unroll
+        for (int t = 0; t < 3; t++) {
+            x_mx[(size_t)(3 * n + t) * d + blk * 32 + lane] = (uint8_t)q[t];
+            if (lane == 0) x_sc[(size_t)(3 * n + t) * (d / 32) + blk] = (uint8_t)sb[t];
+        }
+    }
 }
 
 __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N][32][17]*/) {
@@ -359,10 +378,13 @@ __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, 
     }
     // clean state for the expert kernel
     for (int i = tid; i < p.v_cap; i += RT_THREADS) p.gu_done[i] = 0;
+    for (int i = tid; i < p.E; i += RT_THREADS) p.gu_done_tc[i] = 0;
     for (int64_t i = tid; i < p.pairs_cap; i += RT_THREADS) p.hmax[i] = 0;
     if (tid == 0) {
         p.ctrl[CTRL_WORK] = 0;
         p.ctrl[CTRL_EXIT] = 0;
+        p.ctrl[CTRL_WORK_TC] = 0;
+        p.ctrl[CTRL_EXIT_TC] = 0;
     }
 }
 
@@ -374,7 +396,10 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
 
-    if (p.x != nullptr && b < p.N) prep_row(p.x + (size_t)b * p.d, p.d, p.x16 + (size_t)b * p.d, p.xexp + b, red);
+    if (p.x != nullptr && b < p.N) {
+        prep_row(p.x + (size_t)b * p.d, p.d, p.x16 + (size_t)b * p.d, p.xexp + b, red);
+        prep_row_mx(p.x + (size_t)b * p.d, p.d, b, p.x_mx, p.x_sc);
+    }
 
     bool group_finisher = false;
     if (b < p.n_gemv_ctas) {
@@ -480,6 +505,9 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     p.xexp = reinterpret_cast<int*>(base + L.xexp);
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done);
     p.hmax = reinterpret_cast<uint32_t*>(base + L.hmax);
+    p.x_mx = reinterpret_cast<uint8_t*>(base + L.x_mx);
+    p.x_sc = reinterpret_cast<uint8_t*>(base + L.x_sc);
+    p.gu_done_tc = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
     p.v_cap = n_shared + (n_rows_max * k < E ? n_rows_max * k : E);
     p.pairs_cap = L.pairs;
     const int KS = d < RT_KS ? d : RT_KS;
