@@ -43,6 +43,10 @@ N_ROWS_SEEDED = 100
 SLAB = 17547264
 Q8_SLAB = 35094528
 ROUTER_BYTES = 896 * 7168 * 2
+# DRAM bytes (read + write) of one routed-expert kernel launch on this workload, from
+# an ncu capture of the profile case scaled to 16 experts; None until one is taken
+# of the kernel as it stands
+TC_TRAFFIC = None
 METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
@@ -234,7 +238,7 @@ def run_ours(args, rank, world):
     props = torch.cuda.get_device_properties(dev)
     bus = getattr(props, "pci_bus_id", None)
     sampler = ClockSampler(bus if isinstance(bus, str) else None)
-    layer_ms, kern_ms = [], []
+    layer_ms, kern_ms, seg_ms = [], [], []
     outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
@@ -250,8 +254,9 @@ def run_ours(args, rank, world):
         outer[i][1].record()
         torch.cuda.synchronize()
         if gev is not None:
-            layer_ms.append(gev[0].elapsed_time(gev[3]))
-            kern_ms.append(gev[1].elapsed_time(gev[2]))
+            layer_ms.append(gev[0].elapsed_time(gev[4]))
+            kern_ms.append(gev[2].elapsed_time(gev[3]))
+            seg_ms.append([gev[i].elapsed_time(gev[i + 1]) for i in range(4)])
         else:
             layer_ms.append(outer[i][0].elapsed_time(outer[i][1]))
     wall = time.perf_counter() - t_wall
@@ -259,13 +264,14 @@ def run_ours(args, rank, world):
         torch.distributed.barrier()
     clocks = sampler.stop()
     assert lay.error_bits() == 0
-    if not kern_ms:  # no events inside the graph: time the expert kernel on its own
+    if not kern_ms:  # no events inside the graph: time the routed-expert kernel on its own
         for i in range(K):
             flush.zero_()
             lay.route(1, Xs)
+            lay.experts(1, mode=B.MOE_MODE_SHARED_ONLY)
             a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a_.record()
-            lay.experts(1)
+            lay.experts(1, mode=B.MOE_MODE_ROUTED_ONLY)
             b_.record()
             torch.cuda.synchronize()
             kern_ms.append(a_.elapsed_time(b_))
@@ -278,7 +284,10 @@ def run_ours(args, rank, world):
     unique_bytes = U * SLAB
     value = world * K * unique_bytes / (total_ms * 1e-3) / 1e9
     all_bytes = unique_bytes + 2 * Q8_SLAB + ROUTER_BYTES + 3 * syn.KIMI.d_model * 2
-    kern_bytes = unique_bytes + 2 * Q8_SLAB + syn.KIMI.d_model * 2 + (16 + 2) * syn.KIMI.d_model * 4
+    # routed-expert kernel, algorithmic bytes of one launch: the unique experts' slabs,
+    # the row's three E4M3 activation terms with their scales, the fp32 y_part rows
+    d_ = syn.KIMI.d_model
+    kern_bytes = unique_bytes + 3 * (d_ + d_ // 32) + U * d_ * 4
     kern_avg_s = statistics.mean(kern_ms) * 1e-3
     peak, peak_kind = load_peaks()
     achieved = kern_bytes / kern_avg_s / 1e9
@@ -326,9 +335,12 @@ def run_ours(args, rank, world):
         "layer_us_p10_p50_p90": [float(np.percentile(layer_ms, q)) * 1e3 for q in (10, 50, 90)],
         "all_bytes_gbs": world * K * all_bytes / (total_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "moe::expert_kernel", "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4), "traffic": TC_TRAFFIC,
+                     "kernel": "moe::tc::tc_expert_kernel", "peak_kind": peak_kind,
                      "bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_s * 1e6},
+        "segments_us_median": ({name: statistics.median(s_[i] for s_ in seg_ms) * 1e3
+                                for i, name in enumerate(("route", "shared_experts", "routed_experts", "combine"))}
+                               if seg_ms else None),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
                 "d2h_bytes_per_step": syn.KIMI.d_model * 2},
         "gpu_launches": K * 3,
@@ -345,7 +357,7 @@ def timeable(evs):
     if evs is None:
         return None
     try:
-        evs[0].elapsed_time(evs[3])
+        evs[0].elapsed_time(evs[4])
         return evs
     except Exception:
         return None
@@ -377,7 +389,7 @@ def time_blocks(torch, lay, X, flush, n, reps):
         e1.record()
         torch.cuda.synchronize()
         if b >= 3:
-            ts.append(gev[0].elapsed_time(gev[3]) if gev is not None else e0.elapsed_time(e1))
+            ts.append(gev[0].elapsed_time(gev[4]) if gev is not None else e0.elapsed_time(e1))
             us.append(int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item()))
     t = statistics.median(ts)
     u = statistics.mean(us)

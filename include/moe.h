@@ -65,6 +65,11 @@ extern "C" {
                                    do not depend on the other rows of the block) */
 #define MOE_MODE_PREFILL 1      /* any N: block-scaled tensor-core path */
 #define MOE_MODE_DEBUG_GU 0x100 /* also write g and u (before SwiGLU) to the workspace */
+#define MOE_MODE_SHARED_ONLY 0x200 /* only the block's shared experts (writes shared_y) */
+#define MOE_MODE_ROUTED_ONLY 0x400 /* only the routed experts (writes y_part); with a
+                                      SHARED_ONLY call on the same workspace this does
+                                      the work of one plain call, e.g. split over two
+                                      streams that join before moe_combine */
 
 /* weight formats of a pool */
 #define MOE_FMT_MXFP4 0
@@ -184,7 +189,8 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
  * moe_route on the same workspace and stream.
  *
  *  mode         MOE_MODE_DECODE (n_rows <= 16) or MOE_MODE_PREFILL, optionally
- *               | MOE_MODE_DEBUG_GU
+ *               | MOE_MODE_DEBUG_GU, and at most one of MOE_MODE_SHARED_ONLY /
+ *               MOE_MODE_ROUTED_ONLY (both: MOE_ERR_INVALID_ARG)
  *  routed       pool holding the routed experts (host struct, MXFP4)
  *  expert_slot  int32 [E] slot of each expert in `routed` (device)
  *  slot_ready   uint32 [routed->n_slots] flags, or NULL when every slot is

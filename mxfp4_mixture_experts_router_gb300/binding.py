@@ -24,6 +24,8 @@ MOE_EBIT_BAD_SLOT = 0x4
 MOE_MODE_DECODE = 0
 MOE_MODE_PREFILL = 1
 MOE_MODE_DEBUG_GU = 0x100
+MOE_MODE_SHARED_ONLY = 0x200
+MOE_MODE_ROUTED_ONLY = 0x400
 MOE_FMT_MXFP4 = 0
 MOE_FMT_Q8_0 = 1
 MOE_EPI_NONE = 0

@@ -26,12 +26,16 @@ enum Ctrl : int {
     CTRL_ROWS = 5,       // rows of the routed block
     CTRL_WORK_TC = 6,    // next work item of the block-scaled tensor-core expert kernel
     CTRL_EXIT_TC = 7,    // its finished CTAs
-    CTRL_WORDS = 64
+    CTRL_XMAX = 64,      // [64, 96): per-row max |x| bits published by the router GEMV CTAs
+    CTRL_WORDS = 128
 };
+
+// K splits of a gate/up tile in the block-scaled tensor-core expert kernel
+constexpr int TC_GU_SPLIT = 2;
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -67,6 +71,10 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.h_mx = take((size_t)L.mx_rows_h * f);
     L.h_sc = take((size_t)L.mx_rows_h * (f / 32));
     L.gu_done_tc = take((size_t)E * 4);
+    // split-K gate/up partial sums of the block-scaled kernel: [f/64 tiles][TC_GU_SPLIT]
+    // [routed pairs][64 gate + 64 up] floats, and one arrival counter per (expert, tile)
+    L.gu_part = take((size_t)(f / 64) * TC_GU_SPLIT * (N * k) * 128 * 4);
+    L.gu_cnt = take((size_t)E * (f / 64) * 4);
     L.total = o;
     return L;
 }
@@ -236,9 +244,7 @@ __device__ __forceinline__ void mx3_split(float v, uint32_t (&q)[3], uint32_t (&
     float r = v;
 #pragma unroll
     for (int t = 0; t < 3; t++) {
-        uint32_t m = __float_as_uint(r) & 0x7FFFFFFFu;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(r) & 0x7FFFFFFFu);
         int e = (int)(m >> 23) - 127 - 7;  // |r| / 2^e < 256 <= 448
         e = m == 0u ? 0 : e;
         e = e < -126 ? -126 : (e > 127 ? 127 : e);

@@ -971,6 +971,8 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
         return MOE_ERR_UNSUPPORTED;
     const int base_mode = mode & 0xFF;
     if (base_mode != MOE_MODE_DECODE) return MOE_ERR_UNSUPPORTED;
+    const bool only_shared = (mode & MOE_MODE_SHARED_ONLY) != 0, only_routed = (mode & MOE_MODE_ROUTED_ONLY) != 0;
+    if (only_shared && only_routed) return MOE_ERR_INVALID_ARG;
     if (n_rows < 1 || n_rows > 16 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
     if (n_shared < 0 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
     if (!pool_ok(desc, routed, MOE_FMT_MXFP4)) return MOE_ERR_INVALID_ARG;
@@ -1021,17 +1023,20 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     p.y_part = y_part;
     p.pairs_cap = L.pairs;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (only_shared && n_shared == 0) return MOE_OK;
     if (tc_expert_supported(d, f, n_rows)) {
         // shared Q8_0 experts on the tensor-core MMA.sync engine, routed MXFP4
         // experts on the block-scaled tcgen05 kernel
-        if (n_shared > 0) {
+        if (n_shared > 0 && !only_routed) {
             p.routed_off = 1;
             const int st = launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
-            if (st != MOE_OK) return st;
+            if (st != MOE_OK || only_shared) return st;
         }
         return tc_expert_launch(desc, n_rows, mode, routed, expert_slot, slot_ready, n_shared, ws, n_rows_max, y_part,
                                 s);
     }
+    if (only_shared) p.routed_off = 1;
+    if (only_routed) p.n_shared = 0;
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }
 

@@ -14,46 +14,76 @@
 // token is three B columns whose results are summed in a fixed order.
 //
 // One CTA per SM, persistent, warp-specialised:
-//   warp 0      producer: claims work items in order, TMA loads (4-stage ring)
+//   warp 0      producer: claims work items in order and TMA-loads them into a
+//               ring of shared-memory stages
 //   warp 1      one thread issues the MMAs and the commits
 //   warps 2..5  move each stage's block scales from shared to tensor memory
-//   warps 6..9  epilogue: read the TMEM accumulators (double-buffered), finish
-//               SwiGLU and re-split h into E4M3 terms, or write the outputs.
+//   warps 6..9  epilogue: read the TMEM accumulators (double-buffered), reduce
+//               the K splits of a gate/up tile, finish SwiGLU and re-split h into
+//               E4M3 terms, or write the outputs.
 // Work items: gate/up items (64 rows of gate + the same 64 rows of up = one
-// M=128 tile, full K) and down items (128 rows, full K), ordered gate/up of
-// expert v then down of expert v-4; a down item's activations are read only
-// after every gate/up item of its expert has finished (bounded wait).
+// M=128 tile, over one of TC_GU_SPLIT K ranges) and down items (128 rows, full
+// K), ordered gate/up of expert v then down of expert v-lag.  A down item's
+// activations are read only after every gate/up tile of its expert is finished
+// (bounded wait).
+//
+// The single producer thread sets the pace, so its loop does little: a TMA box
+// costs a roughly fixed time whatever its size, and a stage is one box of code
+// rows (128 rows x 256 K: gate and up rows and both 128-K halves arrive through
+// a 5-D tensor map) and one box of activation rows; the scales of a whole item
+// arrive in one box per operand into a per-item buffer; every expert's slot and
+// pair range sit in shared memory (read by all threads at the start), and the
+// next item's claim is issued while the current item streams.
 #include "common.cuh"
 
 namespace moe {
 namespace tc {
 
-constexpr int NST = 4;                      // ring stages
 constexpr int KC = 256;                     // K elements per stage
-constexpr int NB_MAX = 48;                  // B rows: 3 terms x 16 tokens / pairs
 constexpr int A_BYTES = 128 * KC;           // 128 rows x 256 codes, one byte each after unpacking
-constexpr int OFF_AS = A_BYTES;             // A scales: 128 rows x 16 bytes (8 used per stage)
-constexpr int OFF_B = OFF_AS + 128 * 16;    // 34816: B, two K boxes of NB_MAX rows x 128 bytes
-constexpr int B_BOX = NB_MAX * 128;         // 6144
-constexpr int OFF_BS = OFF_B + 2 * B_BOX;   // 47104: B scales, NB_MAX rows x 16 bytes
-constexpr int STAGE = 48128;                // rounded up to 1024
-constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens
+constexpr int SC_MAX = 112;                 // scale bytes per row of one item (its K range / 32)
+constexpr int SA_BYTES = 128 * SC_MAX;      // A scales of an item
+constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens (xor-swizzled)
+constexpr int MAX_U = 512;                  // experts of one block (N*k <= 16*32)
+constexpr int META_BYTES = MAX_U * 4;       // packed (slot, first pair, pairs) per expert
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr size_t SMEM = (size_t)NST * STAGE + XCH_FLOATS * 4 + 1024 + 1024;
 constexpr uint32_t TM_COLS = 256;
 constexpr uint32_t TM_ACC = 0;    // accumulators: columns [0, 64) and [64, 128)
-constexpr uint32_t TM_SFA = 128;  // A scales: + stage*8 + set*4 (four 32-row columns)
-constexpr uint32_t TM_SFB = 160;  // B scales: same layout
+constexpr uint32_t TM_SFA = 128;  // A scales: + stage*8 + set*4 (four 32-row columns); B scales follow
+constexpr int S = TC_GU_SPLIT;
+constexpr int MAX_NST = 5;
+constexpr int SLOT_BITS = 18;     // packed expert entry: slot | first pair << 18 | pairs << 27
+
+// Two configurations: blocks of up to 5 rows (16 activation rows, 5-stage ring)
+// and of up to 16 rows (48 activation rows, 4-stage ring).
+template <int NBM>
+struct Cfg {
+    static constexpr int NST = NBM == 16 ? 5 : 4;      // ring stages
+    static constexpr int B_BYTES = 2 * NBM * 128;      // B of a stage: two K halves of up to NBM rows x 128 B
+    static constexpr int STAGE = A_BYTES + B_BYTES;    // a multiple of 1024
+    static constexpr int SB_BYTES = NBM * SC_MAX;      // B scales of an item
+    static constexpr int SCB = SA_BYTES + SB_BYTES;    // one per-item scale buffer (two, by item parity)
+    static constexpr uint32_t TM_SFB = TM_SFA + NST * 8;
+    static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
+    static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
+    static_assert(SMEM <= 232448, "shared memory per CTA");
+    static_assert(TM_SFB + NST * 8 <= TM_COLS, "tensor memory columns");
+    static_assert(NST <= MAX_NST, "ring");
+};
 
 enum { IT_GU = 0, IT_DN = 1 };
 
 struct Params {
-    CUtensorMap a_map[3];  // codes of gate, up, down (4-bit elements, unpacked to bytes)
-    CUtensorMap s_map[3];  // E8M0 scales of gate, up, down
-    CUtensorMap x_map, xs_map;  // E4M3 terms of the block's rows (row 3n+t) and their scales
-    CUtensorMap h_map, hs_map;  // E4M3 terms of the pairs' SwiGLU activations (row 3P+t)
-    int d, f, k, n_rows, n_shared, nbx;
+    CUtensorMap a_gu;       // gate and up codes {128 K, f rows, 2 matrices, d/128, slot}, 4-bit unpacked to bytes
+    CUtensorMap a_dn;       // down codes {128 K, d rows, f/128, slot}
+    CUtensorMap s_gu;       // gate and up E8M0 scales {d/32, f rows, 2, slot}
+    CUtensorMap s_dn;       // down scales {f/32, d rows, slot}
+    CUtensorMap x_map;      // E4M3 terms of the block's rows (row 3n+t): {128 K, rows, d/128}
+    CUtensorMap xs_map;     // their scales {d/32, rows}
+    CUtensorMap h_map[3];   // E4M3 terms of the pairs' SwiGLU activations (row 3P+t), boxes of 16/32/48 rows
+    CUtensorMap hs_map[3];  // their scales
+    int d, f, k, n_rows, n_shared, nbx, nk;
     int n_gu, n_dn, lag, debug;
     const int* expert_slot;
     const uint32_t* slot_ready;
@@ -63,6 +93,8 @@ struct Params {
     const int* off;
     const int* pair;
     uint32_t* gu_done;
+    uint32_t* gu_cnt;
+    float* gu_part;
     uint8_t* h_mx;
     uint8_t* h_sc;
     float* y_part;
@@ -71,11 +103,11 @@ struct Params {
 };
 
 struct Meta {
-    int item, type, u, blk, chunk, nchunks, nb, pad;
+    int item, type, u, blk, split, chunk, nchunks, nb, sbuf, sc, pad[2];
 };
 
 struct AccMeta {
-    int item, type, u, blk, nb, pad[3];
+    int item, type, u, blk, split, nb, pad[2];
 };
 
 // --- tcgen05 wrappers -------------------------------------------------------
@@ -126,21 +158,49 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+        : "memory");
+}
+
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
 
-__device__ void decode_item(const Params& p, int V, int item, int& type, int& v, int& blk) {
+// exchange slot of (accumulator row m, token n): rows of 16 floats, columns
+// xor-swizzled by the row so that a warp reading one token's column hits
+// distinct banks
+__device__ __forceinline__ int xch_at(int m, int n) { return m * 16 + (n ^ (m & 15)); }
+
+// item -> (type, expert, tile, split): the gate/up items of expert i (tile-major,
+// splits adjacent), then the down items of expert i - lag
+__device__ void decode_item(const Params& p, int V, int item, int& type, int& v, int& blk, int& split) {
+    const int n_gi = p.n_gu * S;
     int rest = item;
+    split = 0;
     for (int i = 0; i < V + p.lag; i++) {
         if (i < V) {
-            if (rest < p.n_gu) {
+            if (rest < n_gi) {
                 type = IT_GU;
                 v = i;
-                blk = rest;
+                blk = rest / S;
+                split = rest - blk * S;
                 return;
             }
-            rest -= p.n_gu;
+            rest -= n_gi;
         }
         const int vd = i - p.lag;
         if (vd >= 0 && vd < V) {
@@ -158,64 +218,64 @@ __device__ void decode_item(const Params& p, int V, int item, int& type, int& v,
     blk = 0;
 }
 
+// bounded wait until *flag >= target; false (with the timeout bit set) if it gave up
+__device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t target) {
+    if (ld_acquire(flag) >= target) return true;
+    const uint64_t t0 = global_ns();
+    while (ld_acquire(flag) < target) {
+        if (timed_out(p.ctrl)) return false;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+            return false;
+        }
+        __nanosleep(128);
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------------------
 
-__device__ void producer(const Params& p, int U, unsigned char* smem, uint64_t* full, uint64_t* empty, Meta* meta) {
-    for (int m = 0; m < 3; m++) {
-        tma_prefetch_desc(&p.a_map[m]);
-        tma_prefetch_desc(&p.s_map[m]);
-    }
-    const int total = U * (p.n_gu + p.n_dn);
+template <int NBM>
+__device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned char* smem, unsigned char* scbuf,
+                         uint64_t* full, uint64_t* empty, Meta* meta) {
+    using C = Cfg<NBM>;
+    tma_prefetch_desc(&p.a_gu);
+    tma_prefetch_desc(&p.a_dn);
+    tma_prefetch_desc(&p.s_gu);
+    tma_prefetch_desc(&p.s_dn);
+    const int total = U * (p.n_gu * S + p.n_dn);
     uint32_t stage = 0, phase = 0, pending = 0, pending_par = 0;
     bool ok = true;
-    while (ok) {
-        const int item = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
-        if (item >= total) break;
-        int type, u, blk;
-        decode_item(p, U, item, type, u, blk);
-        const int e = __ldg(p.uexp + u);
-        int z = __ldg(p.expert_slot + e);
-        if (z < 0 || z >= p.n_slots) {
-            set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
-            z = 0;
-        }
-        if (p.slot_ready != nullptr && ld_acquire(p.slot_ready + z) == 0u) {
-            const uint64_t t0 = global_ns();
-            while (ld_acquire(p.slot_ready + z) == 0u) {
-                if (timed_out(p.ctrl)) break;
-                if (global_ns() - t0 > WAIT_LIMIT_NS) {
-                    set_error(p.ctrl, MOE_EBIT_TIMEOUT);
-                    break;
-                }
-                __nanosleep(256);
-            }
-        }
-        const int o0 = __ldg(p.off + u), r = __ldg(p.off + u + 1) - o0;
-        if (type == IT_DN) {
+    int item = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
+    for (int seq = 0; ok && item < total; seq++) {
+        int type, u, blk, split;
+        decode_item(p, U, item, type, u, blk, split);
+        const uint32_t mu = umeta[u];
+        const int z = (int)(mu & ((1u << SLOT_BITS) - 1u)), o0 = (int)((mu >> SLOT_BITS) & 511u), r = (int)(mu >> 27);
+        if (p.slot_ready != nullptr) ok = wait_at_least(p, p.slot_ready + z, 1u);
+        const bool gu = type == IT_GU;
+        if (ok && !gu) {
             // the expert's SwiGLU activations must be complete before TMA reads them
-            if (ld_acquire(p.gu_done + u) < (uint32_t)p.n_gu) {
-                const uint64_t t0 = global_ns();
-                while (ld_acquire(p.gu_done + u) < (uint32_t)p.n_gu) {
-                    if (timed_out(p.ctrl)) break;
-                    if (global_ns() - t0 > WAIT_LIMIT_NS) {
-                        set_error(p.ctrl, MOE_EBIT_TIMEOUT);
-                        break;
-                    }
-                    __nanosleep(128);
-                }
-            }
+            ok = wait_at_least(p, p.gu_done + u, (uint32_t)p.n_gu);
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
-        const bool gu = type == IT_GU;
-        const int nch = (gu ? p.d : p.f) / KC;
-        const int nb = gu ? p.nbx : round16(3 * r);
-        const int box_rows = gu ? p.nbx : NB_MAX;
+        if (!ok) break;
+        const int kr = gu ? p.d / S : p.f;     // K range of the item
+        const int kbase = gu ? split * kr : 0;
+        const int nch = kr / KC;
+        const int sc = kr / 32;                // scale bytes per row of the item
+        const int nb = gu ? p.nbx : round16(3 * r);   // activation rows loaded = MMA N
         const int brow = gu ? 0 : 3 * o0;
         const int row0 = gu ? blk * 64 : blk * 128;
+        const int sbuf = seq & 1;
+        unsigned char* sa = scbuf + sbuf * C::SCB;
+        unsigned char* sb = sa + SA_BYTES;
         // an unpacked 4-bit code box counts its packed (global) bytes: half its shared-memory size
-        const uint32_t tx = (uint32_t)(A_BYTES / 2 + 128 * 16 + 2 * box_rows * 128 + box_rows * 16);
-        const CUtensorMap* bmap = gu ? &p.x_map : &p.h_map;
-        const CUtensorMap* bsmap = gu ? &p.xs_map : &p.hs_map;
+        const uint32_t tx = (uint32_t)(A_BYTES / 2 + 2 * nb * 128);
+        const uint32_t tx_sc = (uint32_t)(128 * sc + nb * sc);
+        const CUtensorMap* bmap = gu ? &p.x_map : &p.h_map[nb / 16 - 1];
+        const CUtensorMap* bsmap = gu ? &p.xs_map : &p.hs_map[nb / 16 - 1];
+        int next = total;
         for (int c = 0; c < nch; c++) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                 set_error(p.ctrl, MOE_EBIT_TIMEOUT);
@@ -228,56 +288,62 @@ __device__ void producer(const Params& p, int U, unsigned char* smem, uint64_t* 
             mt.type = type;
             mt.u = u;
             mt.blk = blk;
+            mt.split = split;
             mt.chunk = c;
             mt.nchunks = nch;
             mt.nb = nb;
-            mbar_arrive_expect_tx(&full[stage], tx);
-            unsigned char* st = smem + (size_t)stage * STAGE;
-            const int xs = (c * (KC / 32)) & ~15;  // 16-byte scale box holding this stage's 8 scale bytes
-            for (int kb2 = 0; kb2 < 2; kb2++) {
-                const int x = c * KC + kb2 * 128;
-                if (gu) {
-                    tma_load_3d(st + kb2 * 16384, &p.a_map[0], &full[stage], x, row0, z);
-                    tma_load_3d(st + kb2 * 16384 + 8192, &p.a_map[1], &full[stage], x, row0, z);
-                } else {
-                    tma_load_3d(st + kb2 * 16384, &p.a_map[2], &full[stage], x, row0, z);
-                }
-                tma_load_3d(st + OFF_B + kb2 * B_BOX, bmap, &full[stage], x, brow, 0);
+            mt.sbuf = sbuf;
+            mt.sc = sc;
+            mbar_arrive_expect_tx(&full[stage], tx + (c == 0 ? tx_sc : 0u));
+            unsigned char* st = smem + (size_t)stage * C::STAGE;
+            if (c == 0) {
+                // the item's scales into its buffer, which item seq-2 used last: every
+                // item has at least NST stages, so that item's scales have all been
+                // moved to tensor memory before this stage was released
+                if (gu)
+                    tma_load_4d(sa, &p.s_gu, &full[stage], kbase / 32, row0, 0, z);
+                else
+                    tma_load_3d(sa, &p.s_dn, &full[stage], 0, row0, z);
+                tma_load_3d(sb, bsmap, &full[stage], kbase / 32, brow, 0);
             }
-            if (gu) {
-                tma_load_3d(st + OFF_AS, &p.s_map[0], &full[stage], xs, row0, z);
-                tma_load_3d(st + OFF_AS + 64 * 16, &p.s_map[1], &full[stage], xs, row0, z);
-            } else {
-                tma_load_3d(st + OFF_AS, &p.s_map[2], &full[stage], xs, row0, z);
-            }
-            tma_load_3d(st + OFF_BS, bsmap, &full[stage], xs, brow, 0);
+            const int kc = (kbase + c * KC) / 128;   // first 128-K chunk of the stage
+            if (gu)
+                tma_load_5d(st, &p.a_gu, &full[stage], 0, row0, 0, kc, z);
+            else
+                tma_load_4d(st, &p.a_dn, &full[stage], 0, row0, kc, z);
+            tma_load_3d(st + A_BYTES, bmap, &full[stage], 0, brow, kc);
             pending |= 1u << stage;
             pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == NST) {
+            if (++stage == C::NST) {
                 stage = 0;
                 phase ^= 1u;
             }
+            // the next claim, issued now and read after the item: its latency hides
+            // behind this item's stages
+            if (c == 0) next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
         }
+        item = next;
     }
-    if (ok) {
-        if (mbar_wait(&empty[stage], phase ^ 1u)) {
-            pending &= ~(1u << stage);
-            meta[stage].item = -1;
-            mbar_arrive(&full[stage]);
-        } else {
-            set_error(p.ctrl, MOE_EBIT_TIMEOUT);
-        }
+    // tell the consumers there is nothing more (after an error too, if a stage frees up)
+    if (mbar_wait(&empty[stage], phase ^ 1u)) {
+        pending &= ~(1u << stage);
+        meta[stage].item = -1;
+        mbar_arrive(&full[stage]);
+    } else {
+        set_error(p.ctrl, MOE_EBIT_TIMEOUT);
     }
-    for (int s = 0; s < NST; s++)
+    for (int s = 0; s < C::NST; s++)
         if (pending & (1u << s)) mbar_wait(&full[s], (pending_par >> s) & 1u);
 }
 
-// warps 2..5: each stage's E8M0 scales from shared to tensor memory.  Scale of
-// row m (A: weight row, B: activation row) for the stage's K blocks 4*set..4*set+3
-// is byte (kb % 4) of the 32-bit word at lane m % 32, column base + set*4 + m / 32;
-// each warp writes the copy in its own lane quadrant.
-__device__ void scale_mover(const Params& p, unsigned char* smem, uint32_t tbase, uint64_t* full, uint64_t* sfr,
+// warps 2..5: each stage's E8M0 scales from the item's scale buffer to tensor
+// memory.  Scale of row m (A: weight row, B: activation row) for the stage's K
+// blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word at lane m % 32,
+// column base + set*4 + m / 32; each warp writes the copy in its own lane quadrant.
+template <int NBM>
+__device__ void scale_mover(const Params& p, unsigned char* scbuf, uint32_t tbase, uint64_t* full, uint64_t* sfr,
                             const Meta* meta) {
+    using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
     uint32_t stage = 0, phase = 0;
     while (true) {
@@ -287,8 +353,9 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, uint32_t tbase
         }
         const Meta m = meta[stage];
         if (m.item < 0) break;
-        const uint32_t st = smem_u32(smem + (size_t)stage * STAGE);
-        const int kb_off = (m.chunk * (KC / 32)) & 15;
+        const uint32_t sa = smem_u32(scbuf + m.sbuf * C::SCB);
+        const uint32_t sb = sa + SA_BYTES;
+        const int kb_off = m.chunk * (KC / 32);
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 #pragma unroll
         for (int set = 0; set < 2; set++) {
@@ -296,17 +363,17 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, uint32_t tbase
 #pragma unroll
             for (int c = 0; c < 4; c++) {
                 const int row = 32 * c + lane;
-                wa[c] = lds32(st + OFF_AS + row * 16 + kb_off + 4 * set);
-                wb[c] = row < m.nb ? lds32(st + OFF_BS + row * 16 + kb_off + 4 * set) : 0u;
+                wa[c] = lds32(sa + row * m.sc + kb_off + 4 * set);
+                wb[c] = row < m.nb ? lds32(sb + row * m.sc + kb_off + 4 * set) : 0u;
             }
             tm_st4(tbase + TM_SFA + stage * 8 + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
-            tm_st4(tbase + TM_SFB + stage * 8 + set * 4 + lane_base, wb[0], wb[1], wb[2], wb[3]);
+            tm_st4(tbase + C::TM_SFB + stage * 8 + set * 4 + lane_base, wb[0], wb[1], wb[2], wb[3]);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfr[stage]);
-        if (++stage == NST) {
+        if (++stage == C::NST) {
             stage = 0;
             phase ^= 1u;
         }
@@ -314,13 +381,15 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, uint32_t tbase
 }
 
 // warp 1, one thread: eight MMAs (K = 32 each) per stage into the item's accumulator
+template <int NBM>
 __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase, uint64_t* full, uint64_t* empty,
                            uint64_t* sfr, uint64_t* acc_full, uint64_t* acc_empty, uint64_t* done, const Meta* meta,
                            AccMeta* am) {
+    using C = Cfg<NBM>;
     uint32_t stage = 0, phase = 0, it = 0;
     bool ok = true;
     while (true) {
-        if (!mbar_wait(&full[stage], phase) ) {
+        if (!mbar_wait(&full[stage], phase)) {
             set_error(p.ctrl, MOE_EBIT_TIMEOUT);
             ok = false;
             break;
@@ -346,15 +415,17 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
             a.type = m.type;
             a.u = m.u;
             a.blk = m.blk;
+            a.split = m.split;
             a.nb = m.nb;
         }
-        const uint32_t st = smem_u32(smem + (size_t)stage * STAGE);
+        const uint32_t st = smem_u32(smem + (size_t)stage * C::STAGE);
+        const uint32_t b_half = (uint32_t)m.nb * 128;   // the B box's second 128-K half
 #pragma unroll
         for (int ks = 0; ks < KC / 32; ks++) {
             const uint64_t ad = sdesc(st + (ks >> 2) * 16384 + (ks & 3) * 32);
-            const uint64_t bd = sdesc(st + OFF_B + (ks >> 2) * B_BOX + (ks & 3) * 32);
+            const uint64_t bd = sdesc(st + A_BYTES + (ks >> 2) * b_half + (ks & 3) * 32);
             mma_mx(tbase + TM_ACC + b * 64, ad, bd, idesc(m.nb, ks & 3), tbase + TM_SFA + stage * 8 + (ks >> 2) * 4,
-                   tbase + TM_SFB + stage * 8 + (ks >> 2) * 4, (m.chunk | ks) != 0);
+                   tbase + C::TM_SFB + stage * 8 + (ks >> 2) * 4, (m.chunk | ks) != 0);
         }
         mma_commit(&empty[stage]);
         if (m.chunk == m.nchunks - 1) {
@@ -362,7 +433,7 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
             mma_commit(&acc_full[b]);   // completes when the accumulator is final
             it++;
         }
-        if (++stage == NST) {
+        if (++stage == C::NST) {
             stage = 0;
             phase ^= 1u;
         }
@@ -382,8 +453,10 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
     mbar_wait(done, 0);
 }
 
-__device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint64_t* acc_full, uint64_t* acc_empty,
-                         const AccMeta* am) {
+// warps 6..9: TMEM lane quadrant q = warp % 4, accumulator row m = 32q + lane
+template <int NBM>
+__device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase, float* xch, int* eflag,
+                         uint64_t* acc_full, uint64_t* acc_empty, const AccMeta* am) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
     const int N = p.n_rows, k = p.k;
     uint32_t it = 0;
@@ -396,22 +469,22 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint64_t* 
         fence_after();
         const AccMeta a = am[b];
         if (a.item < 0) break;
-        uint32_t v[48];
+        uint32_t v[NBM];
         const uint32_t ta = tbase + TM_ACC + b * 64 + ((uint32_t)(32 * q) << 16);
         {
             uint32_t t16[16];
             tm_ld16(ta, t16);
 #pragma unroll
             for (int i = 0; i < 16; i++) v[i] = t16[i];
-            if (a.nb > 16) {
+            if (NBM > 16 && a.nb > 16) {
                 tm_ld16(ta + 16, t16);
 #pragma unroll
-                for (int i = 0; i < 16; i++) v[16 + i] = t16[i];
+                for (int i = 0; i < 16; i++) v[(16 + i) % NBM] = t16[i];
             }
-            if (a.nb > 32) {
+            if (NBM > 32 && a.nb > 32) {
                 tm_ld16(ta + 32, t16);
 #pragma unroll
-                for (int i = 0; i < 16; i++) v[32 + i] = t16[i];
+                for (int i = 0; i < 16; i++) v[(32 + i) % NBM] = t16[i];
             }
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         }
@@ -419,45 +492,71 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint64_t* 
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
         const int m = 32 * q + lane;
-        const int o0 = __ldg(p.off + a.u), r = __ldg(p.off + a.u + 1) - o0;
+        const uint32_t mu = umeta[a.u];
+        const int o0 = (int)((mu >> SLOT_BITS) & 511u), r = (int)(mu >> 27);
         if (a.type == IT_GU) {
             // the 3 term columns of token n summed in order; rows 0..63 gate, 64..127 up
 #pragma unroll
-            for (int n = 0; n < 16; n++)
+            for (int n = 0; n < NBM / 3; n++)
                 if (n < N)
-                    xch[m * 16 + n] = __uint_as_float(v[3 * n]) + __uint_as_float(v[3 * n + 1]) +
-                                      __uint_as_float(v[3 * n + 2]);
+                    xch[xch_at(m, n)] = __uint_as_float(v[3 * n]) + __uint_as_float(v[3 * n + 1]) +
+                                        __uint_as_float(v[3 * n + 2]);
             epi_sync();
-            const int j0 = a.blk * 64;
-            bool wrote = false;
+            // this split's sums for the expert's pairs: part[tile][split][pair][128]
+            const size_t tile_base = (size_t)a.blk * S * p.nk;
             for (int task = ew; task < 2 * r; task += 4) {
-                const int col = task >> 1, jb = task & 1;
+                const int col = task >> 1, half = task & 1;
                 const int P = o0 + col;
                 const int n = __ldg(p.pair + P) / k;
-                const int j = 32 * jb + lane;
-                const float g = xch[j * 16 + n], u = xch[(64 + j) * 16 + n];
-                const float hv = g / (1.f + expf(-g)) * u;
-                if (p.debug) {
-                    const size_t o = (size_t)(p.n_shared * N + P) * p.f + j0 + j;
-                    p.dbg_g[o] = g;
-                    p.dbg_u[o] = u;
-                }
-                uint32_t qv[3], sb[3];
-                mx3_split(hv, qv, sb);
-#pragma unroll
-                for (int t = 0; t < 3; t++) {
-                    p.h_mx[(size_t)(3 * P + t) * p.f + j0 + j] = (uint8_t)qv[t];
-                    if (lane == 0) p.h_sc[(size_t)(3 * P + t) * (p.f / 32) + (j0 >> 5) + jb] = (uint8_t)sb[t];
-                }
-                wrote = true;
+                const int row = 64 * half + lane;
+                float* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + P) * 128;
+                dst[row] = xch[xch_at(row, n)];
+                dst[row + 32] = xch[xch_at(row + 32, n)];
             }
-            if (wrote) __threadfence();
+            __threadfence();
             epi_sync();
-            if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.u, 1u);
+            if (ew == 0 && lane == 0)
+                *eflag = atomicAdd(p.gu_cnt + (size_t)a.u * p.n_gu + a.blk, 1u) == (uint32_t)(S - 1);
+            epi_sync();
+            if (*eflag) {
+                // the tile's last split: sum the splits in split order, then SwiGLU
+                __threadfence();
+                const int j0 = a.blk * 64;
+                bool wrote = false;
+                for (int task = ew; task < 2 * r; task += 4) {
+                    const int col = task >> 1, jb = task & 1;
+                    const int P = o0 + col;
+                    const int j = 32 * jb + lane;
+                    float g = 0.f, u = 0.f;
+#pragma unroll
+                    for (int s = 0; s < S; s++) {
+                        const float* src = p.gu_part + (tile_base + (size_t)s * p.nk + P) * 128;
+                        g += __ldcg(src + j);
+                        u += __ldcg(src + 64 + j);
+                    }
+                    const float hv = g / (1.f + expf(-g)) * u;
+                    if (p.debug) {
+                        const size_t o = (size_t)(p.n_shared * N + P) * p.f + j0 + j;
+                        p.dbg_g[o] = g;
+                        p.dbg_u[o] = u;
+                    }
+                    uint32_t qv[3], sbits[3];
+                    mx3_split(hv, qv, sbits);
+#pragma unroll
+                    for (int t = 0; t < 3; t++) {
+                        p.h_mx[(size_t)(3 * P + t) * p.f + j0 + j] = (uint8_t)qv[t];
+                        if (lane == 0) p.h_sc[(size_t)(3 * P + t) * (p.f / 32) + (j0 >> 5) + jb] = (uint8_t)sbits[t];
+                    }
+                    wrote = true;
+                }
+                if (wrote) __threadfence();
+                epi_sync();
+                if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.u, 1u);
+            }
         } else {
             const int m0 = a.blk * 128;
 #pragma unroll
-            for (int col = 0; col < NB_MAX / 3; col++) {
+            for (int col = 0; col < NBM / 3; col++) {
                 if (col < r) {
                     const float y = __uint_as_float(v[3 * col]) + __uint_as_float(v[3 * col + 1]) +
                                     __uint_as_float(v[3 * col + 2]);
@@ -470,25 +569,31 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint64_t* 
     }
 }
 
+template <int NBM>
 __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_constant__ Params p) {
+    using C = Cfg<NBM>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    float* xch = reinterpret_cast<float*>(smem + (size_t)NST * STAGE);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(xch + XCH_FLOATS);
+    unsigned char* scbuf = smem + (size_t)C::NST * C::STAGE;
+    float* xch = reinterpret_cast<float*>(scbuf + 2 * C::SCB);
+    uint32_t* umeta = reinterpret_cast<uint32_t*>(xch + XCH_FLOATS);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(umeta + MAX_U);
     uint64_t* full = bars;
-    uint64_t* empty = full + NST;
-    uint64_t* sfr = empty + NST;
-    uint64_t* acc_full = sfr + NST;
+    uint64_t* empty = full + C::NST;
+    uint64_t* sfr = empty + C::NST;
+    uint64_t* acc_full = sfr + C::NST;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     Meta* meta = reinterpret_cast<Meta*>(done + 1);
-    AccMeta* am = reinterpret_cast<AccMeta*>(meta + NST);
+    AccMeta* am = reinterpret_cast<AccMeta*>(meta + C::NST);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(am + 2);
+    int* eflag = reinterpret_cast<int*>(tslot + 1);
     __shared__ int s_last;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int U = min((int)p.ctrl[CTRL_UNIQUE], MAX_U);
     if (tid == 0) {
-        for (int s = 0; s < NST; s++) {
+        for (int s = 0; s < C::NST; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sfr[s], 4);
@@ -505,20 +610,29 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
                      "r"(TM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // every expert's slot and pair range, packed (all loads in flight at once)
+    for (int u = tid; u < U; u += NTHREADS) {
+        int z = __ldg(p.expert_slot + __ldg(p.uexp + u));
+        const int o0 = __ldg(p.off + u), r = __ldg(p.off + u + 1) - o0;
+        if (z < 0 || z >= p.n_slots) {
+            set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
+            z = 0;
+        }
+        umeta[u] = (uint32_t)z | ((uint32_t)o0 << SLOT_BITS) | ((uint32_t)r << 27);
+    }
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tbase = *tslot;
-    const int U = (int)p.ctrl[CTRL_UNIQUE];
 
     if (warp == 0) {
-        if (lane == 0) producer(p, U, smem, full, empty, meta);
+        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, smem, scbuf, full, empty, meta);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
+        if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
-        scale_mover(p, smem, tbase, full, sfr, meta);
+        scale_mover<NBM>(p, scbuf, tbase, full, sfr, meta);
     } else {
-        epilogue(p, tbase, xch, acc_full, acc_empty, am);
+        epilogue<NBM>(p, umeta, tbase, xch, eflag, acc_full, acc_empty, am);
     }
 
     fence_before();
@@ -534,6 +648,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     if (s_last) {
         __threadfence();
         for (int i = tid; i < U; i += NTHREADS) p.gu_done[i] = 0;
+        for (int i = tid; i < U * p.n_gu; i += NTHREADS) p.gu_cnt[i] = 0;
         if (tid == 0) {
             p.ctrl[CTRL_WORK_TC] = 0;
             p.ctrl[CTRL_EXIT_TC] = 0;
@@ -562,25 +677,51 @@ static EncodeTiledFn encode_fn() {
     return fn;
 }
 
-static bool map3(CUtensorMap* m, CUtensorMapDataType type, const void* addr, uint64_t d0, uint64_t d1, uint64_t d2,
-                 uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, bool swizzle) {
+// tiled map of rank 3 to 5: dims[0] contiguous, byte strides of dims 1..rank-1
+static bool map_nd(CUtensorMap* m, CUtensorMapDataType type, const void* addr, int rank, const uint64_t* dims,
+                   const uint64_t* strides, const uint32_t* box, bool swizzle) {
     EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {s1, s2};
-    const cuuint32_t box[3] = {b0, b1, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, type, 3, const_cast<void*>(addr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (!enc || rank < 3 || rank > 5) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5] = {1, 1, 1, 1, 1};
+    for (int i = 0; i < rank; i++) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; i++) gs[i] = strides[i];
+    return enc(m, type, (cuuint32_t)rank, const_cast<void*>(addr), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int NBM>
+static int launch(const Params& p, cudaStream_t stream) {
+    using C = Cfg<NBM>;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(tc_expert_kernel<NBM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        attr = true;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return MOE_ERR_CUDA;
+    tc_expert_kernel<NBM><<<sms, NTHREADS, C::SMEM, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace tc
 
-// Shapes the block-scaled path serves: both contraction lengths multiples of the
-// 256-element stage, and blocks of at most 16 rows (48 activation columns).
+// Shapes the block-scaled path serves: gate/up K splits that are multiples of 512
+// elements with a scale row that fits the per-item buffer, a down K range that is
+// a multiple of 512 (scale row likewise), at least as many stages per item as the
+// ring holds, and blocks of at most 16 rows (48 activation columns).
 bool tc_expert_supported(int d, int f, int n_rows) {
-    return d % 256 == 0 && f % 256 == 0 && d >= 256 && f >= 256 && n_rows >= 1 && n_rows <= 16;
+    using namespace tc;
+    return d % (512 * S) == 0 && d / S / 32 <= SC_MAX && d / S / KC >= MAX_NST && f % 512 == 0 &&
+           f / 32 <= SC_MAX && f / KC >= MAX_NST && n_rows >= 1 && n_rows <= 16;
 }
 
 int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool* routed, const int32_t* expert_slot,
@@ -588,42 +729,70 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
                      cudaStream_t stream) {
     using namespace tc;
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
+    if (routed->n_slots > (1 << SLOT_BITS) || n_rows * k > MAX_U) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
     static Params p;
     memset(&p, 0, sizeof(p));
+    // slab planes: [gate codes | gate scales | up codes | up scales | down codes | down scales]
     const char* pool = static_cast<const char*>(routed->base);
-    const int64_t per = (int64_t)f * d / 2 + (int64_t)f * (d / 32);
-    const char* planes_c[3] = {pool, pool + per, pool + 2 * per};
-    const char* planes_s[3] = {pool + (int64_t)f * d / 2, pool + per + (int64_t)f * d / 2,
-                               pool + 2 * per + (int64_t)d * f / 2};
-    const int rows[3] = {f, f, d}, kk[3] = {d, d, f}, brows[3] = {64, 64, 128};
-    for (int m = 0; m < 3; m++) {
-        if (!map3(&p.a_map[m], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, planes_c[m], kk[m], rows[m], routed->n_slots,
-                  kk[m] / 2, routed->slot_bytes, 128, brows[m], true))
-            return MOE_ERR_UNSUPPORTED;
-        if (!map3(&p.s_map[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, planes_s[m], kk[m] / 32, rows[m], routed->n_slots,
-                  kk[m] / 32, routed->slot_bytes, 16, brows[m], false))
-            return MOE_ERR_UNSUPPORTED;
+    const uint64_t per = (uint64_t)f * d / 2 + (uint64_t)f * (d / 32);  // one gate or up matrix with its scales
+    const uint64_t slot = (uint64_t)routed->slot_bytes, ns = (uint64_t)routed->n_slots;
+    const char* down_c = pool + 2 * per;
+    const char* down_s = down_c + (uint64_t)d * f / 2;
+    const CUtensorMapDataType U4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    {   // 128-K chunks of a code row are 64 bytes apart
+        const uint64_t dims[5] = {128, (uint64_t)f, 2, (uint64_t)d / 128, ns};
+        const uint64_t str[4] = {(uint64_t)d / 2, per, 64, slot};
+        const uint32_t box[5] = {128, 64, 2, KC / 128, 1};
+        if (!map_nd(&p.a_gu, U4, pool, 5, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
+    }
+    {
+        const uint64_t dims[4] = {(uint64_t)d / 32, (uint64_t)f, 2, ns}, str[3] = {(uint64_t)d / 32, per, slot};
+        const uint32_t box[4] = {(uint32_t)(d / S / 32), 64, 2, 1};
+        if (!map_nd(&p.s_gu, U8, pool + (uint64_t)f * d / 2, 4, dims, str, box, false)) return MOE_ERR_UNSUPPORTED;
+    }
+    {
+        const uint64_t dims[4] = {128, (uint64_t)d, (uint64_t)f / 128, ns}, str[3] = {(uint64_t)f / 2, 64, slot};
+        const uint32_t box[4] = {128, 128, KC / 128, 1};
+        if (!map_nd(&p.a_dn, U4, down_c, 4, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)f / 32, (uint64_t)d, ns}, str[2] = {(uint64_t)f / 32, slot};
+        const uint32_t box[3] = {(uint32_t)(f / 32), 128, 1};
+        if (!map_nd(&p.s_dn, U8, down_s, 3, dims, str, box, false)) return MOE_ERR_UNSUPPORTED;
     }
     const int nbx = ((3 * n_rows + 15) / 16) * 16;
     const uint64_t rx = L.mx_rows_x, rh = L.mx_rows_h;
-    if (!map3(&p.x_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base + L.x_mx, d, rx, 1, d, rx * d, 128, nbx, true) ||
-        !map3(&p.xs_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base + L.x_sc, d / 32, rx, 1, d / 32, rx * (d / 32), 16, nbx,
-              false) ||
-        !map3(&p.h_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base + L.h_mx, f, rh, 1, f, rh * f, 128, NB_MAX, true) ||
-        !map3(&p.hs_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base + L.h_sc, f / 32, rh, 1, f / 32, rh * (f / 32), 16, NB_MAX,
-              false))
-        return MOE_ERR_UNSUPPORTED;
+    {
+        const uint64_t dx[3] = {128, rx, (uint64_t)d / 128}, sx[2] = {(uint64_t)d, 128};
+        const uint32_t bx[3] = {128, (uint32_t)nbx, KC / 128};
+        const uint64_t dxs[3] = {(uint64_t)d / 32, rx, 1}, sxs[2] = {(uint64_t)d / 32, rx * (d / 32)};
+        const uint32_t bxs[3] = {(uint32_t)(d / S / 32), (uint32_t)nbx, 1};
+        if (!map_nd(&p.x_map, U8, base + L.x_mx, 3, dx, sx, bx, true) ||
+            !map_nd(&p.xs_map, U8, base + L.x_sc, 3, dxs, sxs, bxs, false))
+            return MOE_ERR_UNSUPPORTED;
+        for (int i = 0; i < 3; i++) {
+            const uint32_t rows = 16 * (i + 1);
+            const uint64_t dh[3] = {128, rh, (uint64_t)f / 128}, sh[2] = {(uint64_t)f, 128};
+            const uint32_t bh[3] = {128, rows, KC / 128};
+            const uint64_t dhs[3] = {(uint64_t)f / 32, rh, 1}, shs[2] = {(uint64_t)f / 32, rh * (f / 32)};
+            const uint32_t bhs[3] = {(uint32_t)(f / 32), rows, 1};
+            if (!map_nd(&p.h_map[i], U8, base + L.h_mx, 3, dh, sh, bh, true) ||
+                !map_nd(&p.hs_map[i], U8, base + L.h_sc, 3, dhs, shs, bhs, false))
+                return MOE_ERR_UNSUPPORTED;
+        }
+    }
     p.d = d;
     p.f = f;
     p.k = k;
     p.n_rows = n_rows;
     p.n_shared = n_shared;
     p.nbx = nbx;
+    p.nk = n_rows * k;
     p.n_gu = f / 64;
     p.n_dn = d / 128;
-    p.lag = 4;
+    p.lag = 8;
     p.debug = (mode & MOE_MODE_DEBUG_GU) ? 1 : 0;
 
     p.expert_slot = expert_slot;
@@ -634,24 +803,14 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.off = reinterpret_cast<const int*>(base + L.off);
     p.pair = reinterpret_cast<const int*>(base + L.pair);
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
+    p.gu_cnt = reinterpret_cast<uint32_t*>(base + L.gu_cnt);
+    p.gu_part = reinterpret_cast<float*>(base + L.gu_part);
     p.h_mx = reinterpret_cast<uint8_t*>(base + L.h_mx);
     p.h_sc = reinterpret_cast<uint8_t*>(base + L.h_sc);
     p.y_part = y_part;
     p.dbg_g = reinterpret_cast<float*>(base + L.dbg_g);
     p.dbg_u = reinterpret_cast<float*>(base + L.dbg_u);
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(tc_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        attr = true;
-    }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return MOE_ERR_CUDA;
-    tc_expert_kernel<<<sms, NTHREADS, SMEM, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return nbx <= 16 ? launch<16>(p, stream) : launch<48>(p, stream);
 }
 
 }  // namespace moe

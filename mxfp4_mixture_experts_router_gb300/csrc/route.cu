@@ -53,54 +53,56 @@ struct RouteParams {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Activation preparation for the expert kernel: x16 = f16(x * 2^-p), p chosen
-// from the row's largest magnitude so the row sits inside the f16 range.  Rows of
-// up to 8192 elements stay in registers between the max and the conversion (all
-// 16-byte loads issued before any is used); longer rows are read twice.
-__device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float* red) {
-    constexpr int PER = 4;  // 16-byte chunks per thread and pass
-    const int tid = threadIdx.x;
-    const int nv = d / 8;
+// E4M3 split of one 1024-element chunk of row n (four blocks per warp, loads
+// first), and the chunk's max |x| published for the row's f16 copy
+constexpr int RT_CHUNK = 1024;
+__device__ void prep_chunk_mx(const RouteParams& p, int n, int c) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nblk = p.d / 32;
+    const uint16_t* x = p.x + (size_t)n * p.d;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int blk = c * (RT_CHUNK / 32) + warp * 4 + i;
+        v[i] = blk < nblk ? bf16_lo(__ldg(x + blk * 32 + lane)) : 0.f;
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const int blk = c * (RT_CHUNK / 32) + warp * 4 + i;
+        if (blk >= nblk) continue;
+        mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        uint32_t q[3], sb[3];
+        mx3_split(v[i], q, sb);
+#pragma unroll
+        for (int t = 0; t < 3; t++) {
+            p.x_mx[(size_t)(3 * n + t) * p.d + blk * 32 + lane] = (uint8_t)q[t];
+            if (lane == 0) p.x_sc[(size_t)(3 * n + t) * nblk + blk] = (uint8_t)sb[t];
+        }
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0 && mx != 0u) atomicMax(p.ctrl + CTRL_XMAX + n, mx);
+}
+
+// Activation preparation for the f16 (shared-expert) path: x16 = f16(x * 2^-p),
+// p chosen from the row's largest magnitude (published by the CTAs that read the
+// row) so the row sits inside the f16 range; vectorised, all loads of a pass first.
+__device__ void prep_row_x16(const uint16_t* x, int d, uint32_t maxbits, __half* x16, int* xexp) {
+    const int p = f16_scale_exponent(maxbits);
+    const float s = exp2i(-p);
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     uint4* ov = reinterpret_cast<uint4*>(x16);
-    const bool resident = nv <= PER * (int)blockDim.x;
-    uint4 v[PER];
-    uint32_t mx = 0;
-    for (int base = 0; base < nv; base += PER * blockDim.x) {
+    const int nv = d / 8;
+    for (int base = 0; base < nv; base += 4 * blockDim.x) {
+        uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < PER; j++) {
-            const int c = base + j * blockDim.x + tid;
+        for (int j = 0; j < 4; j++) {
+            const int c = base + j * blockDim.x + threadIdx.x;
             v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int j = 0; j < PER; j++) {
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int t = 0; t < 4; t++) mx = max(mx, max((w[t] & 0x7FFFu) << 16, w[t] & 0x7FFF0000u));
-        }
-    }
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((tid & 31) == 0) red[tid >> 5] = __uint_as_float(mx);
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t m = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); w++) m = max(m, __float_as_uint(red[w]));
-        red[32] = __uint_as_float((uint32_t)f16_scale_exponent(m));
-    }
-    __syncthreads();
-    const int p = (int)__float_as_uint(red[32]);
-    const float s = exp2i(-p);
-    for (int base = 0; base < nv; base += PER * blockDim.x) {
-        if (!resident) {
-#pragma unroll
-            for (int j = 0; j < PER; j++) {
-                const int c = base + j * blockDim.x + tid;
-                v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < PER; j++) {
-            const int c = base + j * blockDim.x + tid;
+        for (int j = 0; j < 4; j++) {
+            const int c = base + j * blockDim.x + threadIdx.x;
             if (c >= nv) continue;
             const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
             uint32_t o[4];
@@ -112,24 +114,7 @@ __device__ void prep_row(const uint16_t* x, int d, __half* x16, int* xexp, float
             ov[c] = make_uint4(o[0], o[1], o[2], o[3]);
         }
     }
-    if (tid == 0) *xexp = p;
-    __syncthreads();
-}
-
-// Row x as three E4M3 terms with per-32 E8M0 block scales (rows 3n, 3n+1, 3n+2 of
-// the MX activation buffer): one warp per 32-element block.
-__device__ void prep_row_mx(const uint16_t* x, int d, int n, uint8_t* x_mx, uint8_t* x_sc) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int blk = warp; blk < d / 32; blk += nw) {
-        const float v = bf16_lo(__ldg(x + blk * 32 + lane));
-        uint32_t q[3], sb[3];
-        mx3_split(v, q, sb);
-#pragma unroll
-        for (int t = 0; t < 3; t++) {
-            x_mx[(size_t)(3 * n + t) * d + blk * 32 + lane] = (uint8_t)q[t];
-            if (lane == 0) x_sc[(size_t)(3 * n + t) * (d / 32) + blk] = (uint8_t)sb[t];
-        }
-    }
+    if (threadIdx.x == 0) *xexp = p;
 }
 
 __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N][32][17]*/) {
@@ -187,6 +172,33 @@ __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N]
         }
     }
     __syncthreads();
+    // publish each row's max |x| over this slice, and split the slice's 32-element
+    // blocks of rows n = eg (mod n_eg) into E4M3 terms (all from the staged copy)
+    for (int n = warp; n < p.N; n += RT_THREADS / 32) {
+        uint32_t mx = 0;
+        for (int c = 0; c < per_lane; c++) mx = max(mx, __float_as_uint(xs[(n * 32 + lane) * 17 + c]) & 0x7FFFFFFFu);
+        for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) atomicMax(p.ctrl + CTRL_XMAX + n, mx);
+    }
+    {
+        const int nblk = KS / 32;
+        int task = warp;
+        for (int n = eg; n < p.N; n += p.n_eg) {
+            for (; task < nblk; task += RT_THREADS / 32) {
+                const int el = task * 32 + lane;  // element of the slice
+                const float v = xs[(n * 32 + el / per_lane) * 17 + el % per_lane];
+                uint32_t q[3], sb[3];
+                mx3_split(v, q, sb);
+                const int blk = (k0 >> 5) + task;
+#pragma unroll
+                for (int t = 0; t < 3; t++) {
+                    p.x_mx[(size_t)(3 * n + t) * p.d + k0 + el] = (uint8_t)q[t];
+                    if (lane == 0) p.x_sc[(size_t)(3 * n + t) * (p.d / 32) + blk] = (uint8_t)sb[t];
+                }
+            }
+            task -= nblk;
+        }
+    }
     for (int jb = 0; jb < 2; jb++) {
         if (jb == 1) load_batch(1);
         for (int n = 0; n < p.N; n++) {
@@ -239,70 +251,70 @@ __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N]
 
 // Order-preserving image of a logit: a larger key means a larger value; NaN maps
 // below every number and -0 to +0.
-__device__ __forceinline__ uint32_t order_key(float v) {
+// Selection key of a logit: larger ranks higher, +0 and -0 equal, NaN (1) below
+// every number, 0 = no candidate.
+__device__ __forceinline__ uint32_t sel_key(float v) {
     uint32_t b = __float_as_uint(v);
     b = (b == 0x80000000u) ? 0u : b;
-    uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return isnan(v) ? 0u : ord;
+    const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return isnan(v) ? 1u : ord;
 }
 
-__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
-
-// largest of 32 keys by a pairwise tree (depth 5)
-__device__ __forceinline__ uint64_t tree_max32(const uint64_t (&k)[32]) {
-    uint64_t m16[16], m8[8], m4[4];
-#pragma unroll
-    for (int i = 0; i < 16; i++) m16[i] = umax64(k[2 * i], k[2 * i + 1]);
-#pragma unroll
-    for (int i = 0; i < 8; i++) m8[i] = umax64(m16[2 * i], m16[2 * i + 1]);
-#pragma unroll
-    for (int i = 0; i < 4; i++) m4[i] = umax64(m8[2 * i], m8[2 * i + 1]);
-    return umax64(umax64(m4[0], m4[1]), umax64(m4[2], m4[3]));
+// the logit a key came from (-0 comes back as +0)
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
-    const uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, o);
-    const uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), o);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-// top-k of one row by one warp.  A candidate's key is (order_key(logit) << 32) |
-// (0xFFFFFFFF - expert): the larger key ranks higher (larger logit, then lower
-// index, NaN last); 0 means "no candidate".  Lane l holds experts l, l+32, ...;
-// each round the warp takes the largest key and the lane that held it rescans.
+// top-k of one row by one warp.  Lane l holds the keys of experts l, l+32, ...
+// and its largest key with the lowest such expert.  Each round two warp
+// reductions find the largest key and, among the lanes holding it, the lowest
+// expert (ties go to the lower index); that lane drops the key and rescans.
 __device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2) {
     const int lane = threadIdx.x & 31;
-    float v[32];
+    uint32_t key[32];
 #pragma unroll
     for (int t = 0; t < 32; t++) {  // every load in flight before any is used
-        const int e = min(lane + 32 * t, p.E - 1);
-        v[t] = from_l2 ? __ldcg(lrow + e) : lrow[e];
+        const int e = lane + 32 * t;
+        const float v = (e < p.E) ? (from_l2 ? __ldcg(lrow + e) : lrow[e]) : 0.f;
+        key[t] = (e < p.E) ? sel_key(v) : 0u;
     }
-    uint64_t key[32];
     bool any_nan = false;
 #pragma unroll
-    for (int t = 0; t < 32; t++) {
-        const int e = lane + 32 * t;
-        const bool ok = e < p.E;
-        any_nan |= ok && isnan(v[t]);
-        key[t] = ok ? (((uint64_t)order_key(v[t]) << 32) | (uint32_t)(0xFFFFFFFFu - (uint32_t)e)) : 0ull;
-    }
+    for (int t = 0; t < 32; t++) any_nan |= key[t] == 1u;
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(p.ctrl, MOE_EBIT_NAN);
-    uint64_t local = tree_max32(key);
-    uint64_t mine = 0ull;
+    auto rescan = [&](uint32_t& lmax, int& lfirst) {
+        uint32_t m16[16], m8[8], m4[4];
+#pragma unroll
+        for (int i = 0; i < 16; i++) m16[i] = max(key[2 * i], key[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 8; i++) m8[i] = max(m16[2 * i], m16[2 * i + 1]);
+#pragma unroll
+        for (int i = 0; i < 4; i++) m4[i] = max(m8[2 * i], m8[2 * i + 1]);
+        lmax = max(max(m4[0], m4[1]), max(m4[2], m4[3]));
+        lfirst = 31;
+#pragma unroll
+        for (int t = 31; t >= 0; t--) lfirst = (key[t] == lmax) ? t : lfirst;
+    };
+    uint32_t lmax;
+    int lfirst;
+    rescan(lmax, lfirst);
+    uint32_t my_key = 0u;
+    int my_idx = 0;
     for (int j = 0; j < p.k; j++) {
-        uint64_t best = local;
+        const uint32_t m = __reduce_max_sync(0xffffffffu, lmax);
+        const uint32_t w = __reduce_min_sync(0xffffffffu, lmax == m ? (uint32_t)(lfirst * 32 + lane) : 0xFFFFFFFFu);
+        if (lane == j) {
+            my_key = m;
+            my_idx = (int)w;
+        }
+        if ((int)(w & 31u) == lane) {
+            const int tw = (int)(w >> 5);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) best = umax64(best, shfl_xor_u64(best, o));
-        if (lane == j) mine = best;
-        if (best == local) {
-#pragma unroll
-            for (int t = 0; t < 32; t++) key[t] = (key[t] == best) ? 0ull : key[t];
-            local = tree_max32(key);
+            for (int t = 0; t < 32; t++) key[t] = (t == tw) ? 0u : key[t];
+            rescan(lmax, lfirst);
         }
     }
-    const int my_idx = (int)(0xFFFFFFFFu - (uint32_t)mine);
-    const float my_val = (lane < p.k) ? (from_l2 ? __ldcg(lrow + my_idx) : lrow[my_idx]) : 0.f;
+    const float my_val = (lane < p.k) ? key_value(my_key) : 0.f;
     // weights: exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in slot order
     const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
     const float ex = (lane < p.k) ? expf(my_val - l0) : 0.f;
@@ -391,14 +403,25 @@ __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, 
 __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams p) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(smem_raw);
-    __shared__ float red[40];
     __shared__ int s_flag;
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
 
-    if (p.x != nullptr && b < p.N) {
-        prep_row(p.x + (size_t)b * p.d, p.d, p.x16 + (size_t)b * p.d, p.xexp + b, red);
-        prep_row_mx(p.x + (size_t)b * p.d, p.d, b, p.x_mx, p.x_sc);
+    if (p.x != nullptr && p.n_gemv_ctas == 0) {  // caller logits: one CTA per (row, chunk)
+        const int nc = (p.d + RT_CHUNK - 1) / RT_CHUNK;
+        const int n = b / nc, c = b - n * nc;
+        prep_chunk_mx(p, n, c);
+        // the row's last chunk writes its f16 copy
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_flag = (atomicAdd(p.ctrl + RT_TICKET_EG + n, 1u) == (uint32_t)(nc - 1));
+        __syncthreads();
+        if (s_flag) {
+            __threadfence();
+            prep_row_x16(p.x + (size_t)n * p.d, p.d, __ldcg(p.ctrl + CTRL_XMAX + n), p.x16 + (size_t)n * p.d,
+                         p.xexp + n);
+            if (tid == 0) p.ctrl[RT_TICKET_EG + n] = 0;
+        }
     }
 
     bool group_finisher = false;
@@ -437,6 +460,11 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
                     p.logits[(size_t)n * p.E + e] = a;
                 }
             }
+            // every slice of this group is done, and every CTA published every row's
+            // max: write the f16 copies of rows n = eg (mod n_eg)
+            for (int n = eg; n < p.N; n += p.n_eg)
+                prep_row_x16(p.x + (size_t)n * p.d, p.d, __ldcg(p.ctrl + CTRL_XMAX + n), p.x16 + (size_t)n * p.d,
+                             p.xexp + n);
             if (tid == 0) p.ctrl[RT_TICKET_EG + eg] = 0;
             group_finisher = true;
         }
@@ -463,6 +491,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     int* s_off = reinterpret_cast<int*>(s_bits + 1024);
     int* s_idx = s_off + 1024;
     group_block(p, s_cnt, s_bits, s_off, s_idx);
+    for (int n = tid; n < RT_MAX_ROWS; n += RT_THREADS) p.ctrl[CTRL_XMAX + n] = 0;
     if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
 }
 
@@ -517,7 +546,8 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     // the partial logits must fit in the h buffer: n_ks * N * E floats
     if ((size_t)p.n_ks * n_rows * E * 4 > L.dbg_g - L.h) return MOE_ERR_UNSUPPORTED;
     p.n_gemv_ctas = logits_in ? 0 : p.n_ks * p.n_eg;
-    int grid = p.n_gemv_ctas > n_rows ? p.n_gemv_ctas : n_rows;
+    const int prep_ctas = (logits_in && x) ? n_rows * ((d + RT_CHUNK - 1) / RT_CHUNK) : n_rows;
+    int grid = p.n_gemv_ctas > prep_ctas ? p.n_gemv_ctas : prep_ctas;
     const size_t smem = (size_t)RT_MAX_ROWS * 32 * 17 * 4;  // padded x slice (also covers the grouping tables)
     static bool attr_set = false;
     if (!attr_set) {

@@ -118,9 +118,11 @@ class MoeLayer:
         The graph reads the block from the given device buffers (x, residual and, if
         given, logits_in): refill them and call ``graph.replay()`` per block; the
         output lands in ``self.out``.  Kernel parameters, including the TMA tensor
-        maps, are fixed at capture time.  With events=True, four timing events are
-        recorded inside the graph (before route, before experts, before combine, after
-        combine) and returned; the events are None if the runtime refuses them."""
+        maps, are fixed at capture time.  With events=True the expert step is issued
+        as two calls (shared experts, then routed experts) and five timing events are
+        recorded inside the graph (before route, before the shared experts, before the
+        routed experts, before combine, after combine) and returned; the events are
+        None if the runtime refuses them."""
         import torch as _torch
         n = x.shape[0] if n_rows is None else n_rows
         side = _torch.cuda.Stream()
@@ -136,17 +138,20 @@ class MoeLayer:
             self.route(n, x, logits_in=logits_in)
             if evs:
                 evs[1].record()
-            self.experts(n, mode=mode)
-            if evs:
+                self.experts(n, mode=mode | B.MOE_MODE_SHARED_ONLY)
                 evs[2].record()
+                self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
+                evs[3].record()
+            else:
+                self.experts(n, mode=mode)
             self.combine(n, residual)
             if evs:
-                evs[3].record()
+                evs[4].record()
 
         evs = None
         if events:
             try:  # external events are the ones a graph's event-record nodes can time
-                evs = [_torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                evs = [_torch.cuda.Event(enable_timing=True, external=True) for _ in range(5)]
             except TypeError:
                 evs = None
         g = _torch.cuda.CUDAGraph()

@@ -35,7 +35,7 @@ def test_one_row_matches_oracle(tiny):
     g = tiny.run(x, x)
     o = tiny.oracle(x, x)
     _check_routing(g, o, TINY.top_k)
-    assert_close_to_oracle(g["out"], o["out_bf16"], "tiny 1 row")
+    assert_close_to_oracle(g["out"], o, "tiny 1 row")
 
 
 @pytest.mark.parametrize("n", [1, 2, 4, 16])
@@ -45,7 +45,7 @@ def test_blocks_match_oracle(tiny, n):
     g = tiny.run(x, res)
     o = tiny.oracle(x, res)
     _check_routing(g, o, TINY.top_k)
-    assert_close_to_oracle(g["out"], o["out_bf16"], f"tiny block of {n}")
+    assert_close_to_oracle(g["out"], o, f"tiny block of {n}")
     # per (row, slot) expert outputs
     for r in range(n):
         for j in range(TINY.top_k):
@@ -79,7 +79,7 @@ def test_topk_bit_exact_on_given_logits(tiny, sigma):
     w = orc.routing_weights(logits.astype(np.float64), want)
     np.testing.assert_allclose(g["w"], w, rtol=2e-6, atol=1e-7)
     o = tiny.oracle(x, x, logits=logits)
-    assert_close_to_oracle(g["out"], o["out_bf16"], f"tiny sigma {sigma}")
+    assert_close_to_oracle(g["out"], o, f"tiny sigma {sigma}")
 
 
 def test_topk_ties_signed_zero_and_nan(tiny):
@@ -156,7 +156,7 @@ def test_shared_experts_tiny():
         res = syn.x_rows(10, range(n), TINY.d_model, tag=syn.TAG_RESIDUAL)
         g = lay.run(x, res)
         o = lay.oracle(x, res)
-        assert_close_to_oracle(g["out"], o["out_bf16"], f"tiny shared block {n}")
+        assert_close_to_oracle(g["out"], o, f"tiny shared block {n}")
         sy = lay.layer.shared_y(n).cpu().numpy()
         xf = orc.bf16_bits_to_float(x)
         for s in range(2):
