@@ -17,7 +17,8 @@
 //   warp 0      producer: claims work items in order and TMA-loads them into a
 //               ring of shared-memory stages
 //   warp 1      one thread issues the MMAs and the commits
-//   warps 2..5  move each stage's block scales from shared to tensor memory
+//   warps 2..5  load each stage's activation rows and scales, move the block
+//               scales to tensor memory
 //   warps 6..9  epilogue: read the TMEM accumulators (double-buffered), reduce
 //               the K splits of a gate/up tile, finish SwiGLU and re-split h into
 //               E4M3 terms, or write the outputs.
@@ -27,13 +28,15 @@
 // activations are read only after every gate/up tile of its expert is finished
 // (bounded wait).
 //
-// The single producer thread sets the pace, so its loop does little: a TMA box
-// costs a roughly fixed time whatever its size, and a stage is one box of code
-// rows (128 rows x 256 K: gate and up rows and both 128-K halves arrive through
-// a 5-D tensor map) and one box of activation rows; the scales of a whole item
-// arrive in one box per operand into a per-item buffer; every expert's slot and
-// pair range sit in shared memory (read by all threads at the start), and the
-// next item's claim is issued while the current item streams.
+// The TMA engine moves about 18 bytes a cycle per SM and costs a roughly fixed
+// time per box, so it carries only the weights: a stage is one box of code rows
+// (128 rows x 256 K: gate and up rows and both 128-K halves arrive through a 5-D
+// tensor map) and the scales of a whole item arrive in one box into a per-item
+// buffer.  The small activation operand (rows of the block or of the expert's
+// pairs, from L2) and its scales are loaded by the scale-mover warps one stage
+// ahead into registers and written in the swizzled layout the MMA reads.  Every
+// expert's slot and pair range sit in shared memory (read by all threads at the
+// start), and the next item's claim is issued while the current item streams.
 #include "common.cuh"
 
 namespace moe {
@@ -48,9 +51,6 @@ constexpr int MAX_U = 512;                  // experts of one block (N*k <= 16*3
 constexpr int META_BYTES = MAX_U * 4;       // packed (slot, first pair, pairs) per expert
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
-constexpr uint32_t TM_COLS = 256;
-constexpr uint32_t TM_ACC = 0;    // accumulators: columns [0, 64) and [64, 128)
-constexpr uint32_t TM_SFA = 128;  // A scales: + stage*8 + set*4 (four 32-row columns); B scales follow
 constexpr int S = TC_GU_SPLIT;
 constexpr int MAX_NST = 5;
 constexpr int SLOT_BITS = 18;     // packed expert entry: slot | first pair << 18 | pairs << 27
@@ -62,13 +62,22 @@ struct Cfg {
     static constexpr int NST = NBM == 16 ? 5 : 4;      // ring stages
     static constexpr int B_BYTES = 2 * NBM * 128;      // B of a stage: two K halves of up to NBM rows x 128 B
     static constexpr int STAGE = A_BYTES + B_BYTES;    // a multiple of 1024
-    static constexpr int SB_BYTES = NBM * SC_MAX;      // B scales of an item
-    static constexpr int SCB = SA_BYTES + SB_BYTES;    // one per-item scale buffer (two, by item parity)
+    static constexpr int SCB = SA_BYTES;               // one per-item A-scale buffer (two, by item parity)
+    // tensor memory: two accumulator sets (double-buffered across items), each of
+    // NACC accumulators that take the stage's MMAs in turn (independent MMAs
+    // overlap in the tensor pipe; the epilogue sums them in order; the same NACC
+    // in both configurations keeps a row's arithmetic independent of the block),
+    // then the A and B scale columns of every stage
+    static constexpr int ACC_COLS = NBM == 16 ? 16 : 64;
+    static constexpr int NACC = 2;
+    static constexpr uint32_t ACC_SET = NACC * ACC_COLS;
+    static constexpr uint32_t TM_SFA = 2 * ACC_SET;    // A scales: + stage*8 + set*4 (four 32-row columns)
     static constexpr uint32_t TM_SFB = TM_SFA + NST * 8;
+    static constexpr uint32_t TM_COLS = TM_SFB + NST * 8 <= 256 ? 256 : 512;
     static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
-    static_assert(TM_SFB + NST * 8 <= TM_COLS, "tensor memory columns");
+    static_assert(TM_SFB + NST * 8 <= TM_COLS && NBM <= ACC_COLS, "tensor memory columns");
     static_assert(NST <= MAX_NST, "ring");
 };
 
@@ -79,10 +88,6 @@ struct Params {
     CUtensorMap a_dn;       // down codes {128 K, d rows, f/128, slot}
     CUtensorMap s_gu;       // gate and up E8M0 scales {d/32, f rows, 2, slot}
     CUtensorMap s_dn;       // down scales {f/32, d rows, slot}
-    CUtensorMap x_map;      // E4M3 terms of the block's rows (row 3n+t): {128 K, rows, d/128}
-    CUtensorMap xs_map;     // their scales {d/32, rows}
-    CUtensorMap h_map[3];   // E4M3 terms of the pairs' SwiGLU activations (row 3P+t), boxes of 16/32/48 rows
-    CUtensorMap hs_map[3];  // their scales
     int d, f, k, n_rows, n_shared, nbx, nk;
     int n_gu, n_dn, lag, debug;
     const int* expert_slot;
@@ -95,7 +100,9 @@ struct Params {
     uint32_t* gu_done;
     uint32_t* gu_cnt;
     float* gu_part;
-    uint8_t* h_mx;
+    const uint8_t* x_mx;   // E4M3 terms of the block's rows (row 3n+t) [rows][d] and scales [rows][d/32]
+    const uint8_t* x_sc;
+    uint8_t* h_mx;         // E4M3 terms of the pairs' SwiGLU activations (row 3P+t) [rows][f], scales [rows][f/32]
     uint8_t* h_sc;
     float* y_part;
     float* dbg_g;
@@ -103,7 +110,7 @@ struct Params {
 };
 
 struct Meta {
-    int item, type, u, blk, split, chunk, nchunks, nb, sbuf, sc, pad[2];
+    int item, type, u, blk, split, chunk, nchunks, nb, sbuf, sc, kbase, nrow, brow, pad[3];
 };
 
 struct AccMeta {
@@ -237,7 +244,7 @@ __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t ta
 
 template <int NBM>
 __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned char* smem, unsigned char* scbuf,
-                         uint64_t* full, uint64_t* empty, Meta* meta) {
+                         uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf, Meta* meta) {
     using C = Cfg<NBM>;
     tma_prefetch_desc(&p.a_gu);
     tma_prefetch_desc(&p.a_dn);
@@ -245,6 +252,7 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
     tma_prefetch_desc(&p.s_dn);
     const int total = U * (p.n_gu * S + p.n_dn);
     uint32_t stage = 0, phase = 0, pending = 0, pending_par = 0;
+    uint32_t sc_any = 0u, sc_cnt = 0u;  // per scale buffer: armed at all, and the parity of its arm count
     bool ok = true;
     int item = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
     for (int seq = 0; ok && item < total; seq++) {
@@ -269,12 +277,9 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
         const int row0 = gu ? blk * 64 : blk * 128;
         const int sbuf = seq & 1;
         unsigned char* sa = scbuf + sbuf * C::SCB;
-        unsigned char* sb = sa + SA_BYTES;
         // an unpacked 4-bit code box counts its packed (global) bytes: half its shared-memory size
-        const uint32_t tx = (uint32_t)(A_BYTES / 2 + 2 * nb * 128);
-        const uint32_t tx_sc = (uint32_t)(128 * sc + nb * sc);
-        const CUtensorMap* bmap = gu ? &p.x_map : &p.h_map[nb / 16 - 1];
-        const CUtensorMap* bsmap = gu ? &p.xs_map : &p.hs_map[nb / 16 - 1];
+        const uint32_t tx = (uint32_t)(A_BYTES / 2);
+        const uint32_t tx_sc = (uint32_t)(128 * sc);
         int next = total;
         for (int c = 0; c < nch; c++) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -294,24 +299,31 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
             mt.nb = nb;
             mt.sbuf = sbuf;
             mt.sc = sc;
-            mbar_arrive_expect_tx(&full[stage], tx + (c == 0 ? tx_sc : 0u));
-            unsigned char* st = smem + (size_t)stage * C::STAGE;
+            mt.kbase = kbase;
+            mt.nrow = gu ? 3 * p.n_rows : 3 * r;
+            mt.brow = brow;
             if (c == 0) {
                 // the item's scales into its buffer, which item seq-2 used last: every
                 // item has at least NST stages, so that item's scales have all been
                 // moved to tensor memory before this stage was released
+                mbar_arrive_expect_tx(&scf[sbuf], tx_sc);
                 if (gu)
-                    tma_load_4d(sa, &p.s_gu, &full[stage], kbase / 32, row0, 0, z);
+                    tma_load_4d(sa, &p.s_gu, &scf[sbuf], kbase / 32, row0, 0, z);
                 else
-                    tma_load_3d(sa, &p.s_dn, &full[stage], 0, row0, z);
-                tma_load_3d(sb, bsmap, &full[stage], kbase / 32, brow, 0);
+                    tma_load_3d(sa, &p.s_dn, &scf[sbuf], 0, row0, z);
+                sc_any |= 1u << sbuf;
+                sc_cnt ^= 1u << sbuf;
             }
+            // the stage is this item's now: the scale movers may prepare it while
+            // its codes are in flight
+            mbar_arrive(&mready[stage]);
+            mbar_arrive_expect_tx(&full[stage], tx);
+            unsigned char* st = smem + (size_t)stage * C::STAGE;
             const int kc = (kbase + c * KC) / 128;   // first 128-K chunk of the stage
             if (gu)
                 tma_load_5d(st, &p.a_gu, &full[stage], 0, row0, 0, kc, z);
             else
                 tma_load_4d(st, &p.a_dn, &full[stage], 0, row0, kc, z);
-            tma_load_3d(st + A_BYTES, bmap, &full[stage], 0, brow, kc);
             pending |= 1u << stage;
             pending_par = (pending_par & ~(1u << stage)) | (phase << stage);
             if (++stage == C::NST) {
@@ -328,51 +340,115 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
     if (mbar_wait(&empty[stage], phase ^ 1u)) {
         pending &= ~(1u << stage);
         meta[stage].item = -1;
+        mbar_arrive(&mready[stage]);
         mbar_arrive(&full[stage]);
     } else {
         set_error(p.ctrl, MOE_EBIT_TIMEOUT);
     }
+    // no copy may still be in flight when the CTA exits
     for (int s = 0; s < C::NST; s++)
         if (pending & (1u << s)) mbar_wait(&full[s], (pending_par >> s) & 1u);
+    for (int b = 0; b < 2; b++)
+        if (sc_any & (1u << b)) mbar_wait(&scf[b], ((sc_cnt >> b) & 1u) ^ 1u);
 }
 
-// warps 2..5: each stage's E8M0 scales from the item's scale buffer to tensor
+// One stage's activation operand, held in registers between its loads and its
+// stores: chunk j = t + 128 i (row j / 16, 16-byte piece j % 16 of the row's
+// 256 K) of this thread t, and the stage's 8 scale bytes of rows lane and
+// 32 + lane (every warp loads the scales its own lane quadrant needs).
+template <int NBM>
+struct BStage {
+    uint4 d[NBM / 8];
+    uint2 s[2];
+};
+
+template <int NBM>
+__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b) {
+    const bool gu = m.type == IT_GU;
+    const uint8_t* src = gu ? p.x_mx : p.h_mx;
+    const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
+    const int ld = gu ? p.d : p.f;
+    const int k0 = m.kbase + chunk * KC;
+#pragma unroll
+    for (int i = 0; i < NBM / 8; i++) {
+        const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
+        b.d[i] = row < m.nrow ? __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(m.brow + row) * ld + k0 + c16 * 16))
+                              : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        const int row = 32 * c + lane;
+        b.s[c] = (row < m.nrow && row < NBM)
+                     ? __ldcg(reinterpret_cast<const uint2*>(ssrc + (size_t)(m.brow + row) * (ld / 32) + k0 / 32))
+                     : make_uint2(0, 0);
+    }
+}
+
+// warps 2..5: per stage, the activation rows into the stage's B area (the
+// 128-byte-swizzled K-major layout the MMA reads: two 128-K halves of nb rows,
+// piece cc of row r at 16 * (cc ^ (r % 8))) and every E8M0 scale into tensor
 // memory.  Scale of row m (A: weight row, B: activation row) for the stage's K
 // blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word at lane m % 32,
-// column base + set*4 + m / 32; each warp writes the copy in its own lane quadrant.
+// column base + set*4 + m / 32; each warp writes the copy in its own lane
+// quadrant.  A stage is prepared as soon as the producer has claimed it (its
+// codes may still be in flight); the next stage's activations are loaded ahead
+// when it belongs to the same item.
 template <int NBM>
-__device__ void scale_mover(const Params& p, unsigned char* scbuf, uint32_t tbase, uint64_t* full, uint64_t* sfr,
-                            const Meta* meta) {
+__device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char* scbuf, uint32_t tbase,
+                            uint64_t* mready, uint64_t* scf, uint64_t* sfr, const Meta* meta) {
     using C = Cfg<NBM>;
-    const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3;
+    const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
     uint32_t stage = 0, phase = 0;
+    uint32_t scph = 0;  // parity of the next phase of each scale buffer
+    BStage<NBM> b;
+    int have_item = -1, have_chunk = -1;
     while (true) {
-        if (!mbar_wait(&full[stage], phase)) {
+        if (__shfl_sync(0xffffffffu, mbar_wait(&mready[stage], phase) ? 1 : 0, 0) == 0) {
             if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
             break;
         }
         const Meta m = meta[stage];
         if (m.item < 0) break;
+        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b);
+        unsigned char* bst = smem + (size_t)stage * C::STAGE + A_BYTES;
+#pragma unroll
+        for (int i = 0; i < NBM / 8; i++) {
+            const int j = t + 128 * i, row = j >> 4, c16 = j & 15, kh = c16 >> 3, cc = c16 & 7;
+            if (row < m.nrow)
+                *reinterpret_cast<uint4*>(bst + kh * (m.nb * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = b.d[i];
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (m.chunk == 0) {  // the item's A scales have landed
+            if (__shfl_sync(0xffffffffu, mbar_wait(&scf[m.sbuf], (scph >> m.sbuf) & 1u) ? 1 : 0, 0) == 0) {
+                if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                break;
+            }
+            scph ^= 1u << m.sbuf;
+        }
         const uint32_t sa = smem_u32(scbuf + m.sbuf * C::SCB);
-        const uint32_t sb = sa + SA_BYTES;
         const int kb_off = m.chunk * (KC / 32);
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 #pragma unroll
         for (int set = 0; set < 2; set++) {
-            uint32_t wa[4], wb[4];
+            uint32_t wa[4];
 #pragma unroll
-            for (int c = 0; c < 4; c++) {
-                const int row = 32 * c + lane;
-                wa[c] = lds32(sa + row * m.sc + kb_off + 4 * set);
-                wb[c] = row < m.nb ? lds32(sb + row * m.sc + kb_off + 4 * set) : 0u;
-            }
-            tm_st4(tbase + TM_SFA + stage * 8 + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
-            tm_st4(tbase + C::TM_SFB + stage * 8 + set * 4 + lane_base, wb[0], wb[1], wb[2], wb[3]);
+            for (int c = 0; c < 4; c++) wa[c] = lds32(sa + (32 * c + lane) * m.sc + kb_off + 4 * set);
+            const uint32_t w0 = set ? b.s[0].y : b.s[0].x, w1 = set ? b.s[1].y : b.s[1].x;
+            tm_st4(tbase + C::TM_SFA + stage * 8 + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
+            tm_st4(tbase + C::TM_SFB + stage * 8 + set * 4 + lane_base, w0, w1, 0u, 0u);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfr[stage]);
+        // the next stage of the same item: its activations are known now
+        if (m.chunk + 1 < m.nchunks) {
+            b_load<NBM>(p, m, m.chunk + 1, t, lane, b);
+            have_item = m.item;
+            have_chunk = m.chunk + 1;
+        } else {
+            have_item = -1;
+        }
         if (++stage == C::NST) {
             stage = 0;
             phase ^= 1u;
@@ -424,8 +500,9 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
         for (int ks = 0; ks < KC / 32; ks++) {
             const uint64_t ad = sdesc(st + (ks >> 2) * 16384 + (ks & 3) * 32);
             const uint64_t bd = sdesc(st + A_BYTES + (ks >> 2) * b_half + (ks & 3) * 32);
-            mma_mx(tbase + TM_ACC + b * 64, ad, bd, idesc(m.nb, ks & 3), tbase + TM_SFA + stage * 8 + (ks >> 2) * 4,
-                   tbase + C::TM_SFB + stage * 8 + (ks >> 2) * 4, (m.chunk | ks) != 0);
+            mma_mx(tbase + b * C::ACC_SET + (ks % C::NACC) * C::ACC_COLS, ad, bd, idesc(m.nb, ks & 3),
+                   tbase + C::TM_SFA + stage * 8 + (ks >> 2) * 4, tbase + C::TM_SFB + stage * 8 + (ks >> 2) * 4,
+                   m.chunk != 0 || ks >= C::NACC);
         }
         mma_commit(&empty[stage]);
         if (m.chunk == m.nchunks - 1) {
@@ -457,6 +534,7 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
 template <int NBM>
 __device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase, float* xch, int* eflag,
                          uint64_t* acc_full, uint64_t* acc_empty, const AccMeta* am) {
+    using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
     const int N = p.n_rows, k = p.k;
     uint32_t it = 0;
@@ -469,25 +547,33 @@ __device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase,
         fence_after();
         const AccMeta a = am[b];
         if (a.item < 0) break;
-        uint32_t v[NBM];
-        const uint32_t ta = tbase + TM_ACC + b * 64 + ((uint32_t)(32 * q) << 16);
-        {
-            uint32_t t16[16];
-            tm_ld16(ta, t16);
+        // the item's result: its accumulators summed in order
+        float acc[NBM];
 #pragma unroll
-            for (int i = 0; i < 16; i++) v[i] = t16[i];
-            if (NBM > 16 && a.nb > 16) {
-                tm_ld16(ta + 16, t16);
+        for (int i = 0; i < NBM; i++) acc[i] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; i++) v[(16 + i) % NBM] = t16[i];
-            }
-            if (NBM > 32 && a.nb > 32) {
-                tm_ld16(ta + 32, t16);
+        for (int ai = 0; ai < C::NACC; ai++) {
+            const uint32_t ta = tbase + b * C::ACC_SET + ai * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
+            uint32_t t16[NBM];
 #pragma unroll
-                for (int i = 0; i < 16; i++) v[(32 + i) % NBM] = t16[i];
+            for (int h = 0; h < NBM / 16; h++) {
+                uint32_t w[16];
+                if (h == 0 || a.nb > 16 * h) {
+                    tm_ld16(ta + 16 * h, w);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; i++) w[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; i++) t16[16 * h + i] = w[i];
             }
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int i = 0; i < NBM; i++) acc[i] += __uint_as_float(t16[i]);
         }
+        uint32_t v[NBM];
+#pragma unroll
+        for (int i = 0; i < NBM; i++) v[i] = __float_as_uint(acc[i]);
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
@@ -581,7 +667,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     uint64_t* full = bars;
     uint64_t* empty = full + C::NST;
     uint64_t* sfr = empty + C::NST;
-    uint64_t* acc_full = sfr + C::NST;
+    uint64_t* mready = sfr + C::NST;
+    uint64_t* scf = mready + C::NST;
+    uint64_t* acc_full = scf + 2;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     Meta* meta = reinterpret_cast<Meta*>(done + 1);
@@ -597,7 +685,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sfr[s], 4);
+            mbar_init(&mready[s], 1);
         }
+        mbar_init(&scf[0], 1);
+        mbar_init(&scf[1], 1);
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 2);
             mbar_init(&acc_empty[b], 4);
@@ -607,7 +698,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                     "r"(TM_COLS));
+                     "r"(C::TM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     // every expert's slot and pair range, packed (all loads in flight at once)
@@ -626,11 +717,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const uint32_t tbase = *tslot;
 
     if (warp == 0) {
-        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, smem, scbuf, full, empty, meta);
+        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, smem, scbuf, full, empty, mready, scf, meta);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
-        scale_mover<NBM>(p, scbuf, tbase, full, sfr, meta);
+        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sfr, meta);
     } else {
         epilogue<NBM>(p, umeta, tbase, xch, eflag, acc_full, acc_empty, am);
     }
@@ -638,7 +729,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(TM_COLS));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(C::TM_COLS));
     // the last CTA to finish leaves the counters clean for the next call
     if (tid == 0) {
         __threadfence();
@@ -763,26 +854,6 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
         if (!map_nd(&p.s_dn, U8, down_s, 3, dims, str, box, false)) return MOE_ERR_UNSUPPORTED;
     }
     const int nbx = ((3 * n_rows + 15) / 16) * 16;
-    const uint64_t rx = L.mx_rows_x, rh = L.mx_rows_h;
-    {
-        const uint64_t dx[3] = {128, rx, (uint64_t)d / 128}, sx[2] = {(uint64_t)d, 128};
-        const uint32_t bx[3] = {128, (uint32_t)nbx, KC / 128};
-        const uint64_t dxs[3] = {(uint64_t)d / 32, rx, 1}, sxs[2] = {(uint64_t)d / 32, rx * (d / 32)};
-        const uint32_t bxs[3] = {(uint32_t)(d / S / 32), (uint32_t)nbx, 1};
-        if (!map_nd(&p.x_map, U8, base + L.x_mx, 3, dx, sx, bx, true) ||
-            !map_nd(&p.xs_map, U8, base + L.x_sc, 3, dxs, sxs, bxs, false))
-            return MOE_ERR_UNSUPPORTED;
-        for (int i = 0; i < 3; i++) {
-            const uint32_t rows = 16 * (i + 1);
-            const uint64_t dh[3] = {128, rh, (uint64_t)f / 128}, sh[2] = {(uint64_t)f, 128};
-            const uint32_t bh[3] = {128, rows, KC / 128};
-            const uint64_t dhs[3] = {(uint64_t)f / 32, rh, 1}, shs[2] = {(uint64_t)f / 32, rh * (f / 32)};
-            const uint32_t bhs[3] = {(uint32_t)(f / 32), rows, 1};
-            if (!map_nd(&p.h_map[i], U8, base + L.h_mx, 3, dh, sh, bh, true) ||
-                !map_nd(&p.hs_map[i], U8, base + L.h_sc, 3, dhs, shs, bhs, false))
-                return MOE_ERR_UNSUPPORTED;
-        }
-    }
     p.d = d;
     p.f = f;
     p.k = k;
@@ -805,6 +876,8 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
     p.gu_cnt = reinterpret_cast<uint32_t*>(base + L.gu_cnt);
     p.gu_part = reinterpret_cast<float*>(base + L.gu_part);
+    p.x_mx = reinterpret_cast<const uint8_t*>(base + L.x_mx);
+    p.x_sc = reinterpret_cast<const uint8_t*>(base + L.x_sc);
     p.h_mx = reinterpret_cast<uint8_t*>(base + L.h_mx);
     p.h_sc = reinterpret_cast<uint8_t*>(base + L.h_sc);
     p.y_part = y_part;
