@@ -201,6 +201,24 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
  *  y_part       fp32 [n_rows][k][d] output of each (row, slot)
  *  The shared experts' outputs go to the workspace (moe_ws_offsets.shared_y).
  */
+/*
+ * The shared experts alone, straight from the block's rows: they depend on x
+ * only, not on the routing ("Run Kimi K3 and K3.1 Pro Locally": every token
+ * also runs the 2 shared experts; their matmuls load each weight once for all
+ * rows), so this call may run on a second stream while moe_route runs, joining
+ * before moe_combine.  It keeps its own copy of the activations and its own
+ * counters in the workspace, so it never races with moe_route or with the
+ * routed part of moe_expert_block (MOE_MODE_ROUTED_ONLY) on the same workspace.
+ *
+ *  x        bf16 [n_rows][d] (device, 16-byte aligned)
+ *  shared   pool of n_shared (1..8) Q8_0 shared experts in slots 0..n_shared-1
+ *  Output: shared_y in the workspace (moe_ws_offsets.shared_y), the same values
+ *  moe_expert_block writes there.  Errors as moe_expert_block.
+ */
+MOE_API int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x,
+                       const moe_pool* shared, int32_t n_shared,
+                       void* ws, int32_t n_rows_max, void* stream);
+
 MOE_API int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mode,
                      const moe_pool* routed, const int32_t* expert_slot,
                      const uint32_t* slot_ready,

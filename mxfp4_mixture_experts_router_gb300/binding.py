@@ -37,7 +37,7 @@ MOE_DTYPE_F32 = 1
 EXPORTED = [
     "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
-    "q8_0_block_matmul_noalloc",
+    "q8_0_block_matmul_noalloc", "moe_shared_experts",
 ]
 
 
@@ -85,6 +85,7 @@ def lib() -> ctypes.CDLL:
         L.moe_workspace_offsets.argtypes = [D, I32, I32, ctypes.POINTER(MoeWsOffsets)]
         L.moe_route.argtypes = [D, I32, P, P, P, P, P, P, P, I32, I32, P]
         L.moe_expert_block.argtypes = [D, I32, I32, PL, P, P, PL, I32, P, I32, P, P]
+        L.moe_shared_experts.argtypes = [D, I32, P, PL, I32, P, I32, P]
         L.moe_combine.argtypes = [D, I32, P, P, P, P, I32, P, P]
         L.q8_0_workspace_size.argtypes = [I32, I32, I32]
         L.q8_0_workspace_size.restype = SZ
@@ -146,6 +147,12 @@ def moe_route(d: MoeDesc, n_rows: int, x, w_router, logits_in, logits_out, topk_
     _check(lib().moe_route(ctypes.byref(d), n_rows, _ptr(x), _ptr(w_router), _ptr(logits_in),
                            _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w), _ptr(ws), n_rows_max,
                            n_shared, _stream(stream)), "moe_route")
+
+
+def moe_shared_experts(d: MoeDesc, n_rows: int, x, shared: MoePool, n_shared: int, ws, n_rows_max: int,
+                       stream=None):
+    _check(lib().moe_shared_experts(ctypes.byref(d), n_rows, _ptr(x), ctypes.byref(shared), n_shared, _ptr(ws),
+                                    n_rows_max, _stream(stream)), "moe_shared_experts")
 
 
 def moe_expert_block(d: MoeDesc, n_rows: int, mode: int, routed: MoePool, expert_slot, slot_ready,

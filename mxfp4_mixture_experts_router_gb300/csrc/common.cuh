@@ -26,6 +26,8 @@ enum Ctrl : int {
     CTRL_ROWS = 5,       // rows of the routed block
     CTRL_WORK_TC = 6,    // next work item of the block-scaled tensor-core expert kernel
     CTRL_EXIT_TC = 7,    // its finished CTAs
+    CTRL_WORK_SH = 8,    // next work item of the shared-expert call (runs beside routing)
+    CTRL_EXIT_SH = 9,    // its finished CTAs
     CTRL_XMAX = 64,      // [64, 96): per-row max |x| bits published by the router GEMV CTAs
     CTRL_WORDS = 128
 };
@@ -35,7 +37,7 @@ constexpr int TC_GU_SPLIT = 2;
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, xmaxs, gu_done_sh, hmax_sh, h_sh, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -75,8 +77,22 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     // [routed pairs][64 gate + 64 up] floats, and one arrival counter per (expert, tile)
     L.gu_part = take((size_t)(f / 64) * TC_GU_SPLIT * (N * k) * 128 * 4);
     L.gu_cnt = take((size_t)E * (f / 64) * 4);
+    // the shared-expert call's own activation copy and counters: it runs beside
+    // the routing kernel, which resets the layer's counters
+    L.x16s = take((size_t)N * d * 2);
+    L.xexps = take((size_t)N * 4);
+    L.xmaxs = take((size_t)N * 4);
+    L.gu_done_sh = take(64 * 4);
+    L.hmax_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * 4);
+    L.h_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
     L.total = o;
     return L;
+}
+
+// Dynamic shared memory above the default limit for a kernel.
+template <class K>
+inline cudaError_t kernel_smem_attrs(K* kernel, int dyn) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
 }
 
 // ---------------------------------------------------------------------------

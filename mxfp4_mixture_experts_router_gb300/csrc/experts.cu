@@ -61,6 +61,7 @@ struct ExParams {
     int n_gu, n_dn, lag;
     int debug_gu, accum;
     int routed_off;  // layer job without the routed experts (they run on the block-scaled path)
+    int work_word, exit_word;  // ctrl words of this launch's work counter and exit counter
     const int* expert_slot;
     const uint32_t* slot_ready;
     int n_slots;
@@ -464,7 +465,7 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
     uint32_t pending = 0, pending_par = 0;  // stages with copies not yet known to be consumed
     bool ok = true;
     while (ok) {
-        const int item = (int)atomicAdd(p.ctrl + CTRL_WORK, 1u);
+        const int item = (int)atomicAdd(p.ctrl + p.work_word, 1u);
         if (item >= total) break;
         int type, v, blk;
         decode_item(p, V, item, type, v, blk);
@@ -799,7 +800,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
     consumer_sync<EX_CT>();
     if (tid == 0) {
         __threadfence();
-        s_last = atomicAdd(p.ctrl + CTRL_EXIT, 1u) == gridDim.x - 1;
+        s_last = atomicAdd(p.ctrl + p.exit_word, 1u) == gridDim.x - 1;
     }
     consumer_sync<EX_CT>();
     if (s_last) {
@@ -807,8 +808,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         for (int i = tid; i < V; i += EX_CT) p.gu_done[i] = 0;
         for (int64_t i = tid; i < p.pairs_cap; i += EX_CT) p.hmax[i] = 0;
         if (tid == 0) {
-            p.ctrl[CTRL_WORK] = 0;
-            p.ctrl[CTRL_EXIT] = 0;
+            p.ctrl[p.work_word] = 0;
+            p.ctrl[p.exit_word] = 0;
         }
     }
 }
@@ -923,9 +924,7 @@ template <int FR, int FS, bool FAST>
 static int launch_variant(const ExParams& p, cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(expert_kernel<FR, FS, FAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)EX_SMEM) != cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (kernel_smem_attrs(expert_kernel<FR, FS, FAST>, (int)EX_SMEM) != cudaSuccess) return MOE_ERR_CUDA;
         attr = true;
     }
     const int grid = sm_count() * EX_CTAS_PER_SM;
@@ -1022,6 +1021,8 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     p.out_shared = reinterpret_cast<float*>(base + L.shared_y);
     p.y_part = y_part;
     p.pairs_cap = L.pairs;
+    p.work_word = CTRL_WORK;
+    p.exit_word = CTRL_EXIT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (only_shared && n_shared == 0) return MOE_OK;
     if (tc_expert_supported(d, f, n_rows)) {
@@ -1037,6 +1038,61 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     }
     if (only_shared) p.routed_off = 1;
     if (only_routed) p.n_shared = 0;
+    return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
+}
+
+__global__ void q8_prep_kernel(int k_in, const void* x, int x_dtype, int swiglu, __half* x16, int* xexp,
+                               uint32_t* hmax, float* h);
+
+extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const moe_pool* shared,
+                                  int32_t n_shared, void* ws, int32_t n_rows_max, void* stream) {
+    if (!desc || !ws || !x || !shared) return MOE_ERR_INVALID_ARG;
+    const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
+    if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
+        return MOE_ERR_UNSUPPORTED;
+    if (n_rows < 1 || n_rows > 16 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
+    if (n_shared < 1 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
+    if (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared) return MOE_ERR_INVALID_ARG;
+    if (((uintptr_t)ws & 255) || ((uintptr_t)x & 15)) return MOE_ERR_INVALID_ARG;
+
+    const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
+    char* base = static_cast<char*>(ws);
+    static ExParams p;
+    memset(&p, 0, sizeof(p));
+    if (!pool_maps(&p.map[6], &p.geom[2], shared, d, f)) return MOE_ERR_UNSUPPORTED;
+    for (int i = 0; i < 6; i++) p.map[i] = p.map[6 + i];  // no routed experts in this launch
+    p.geom[0] = p.geom[2];
+    p.geom[1] = p.geom[3];
+    p.job = J_LAYER;
+    p.fmt_routed = MOE_FMT_MXFP4;
+    p.fmt_shared = MOE_FMT_Q8_0;
+    p.k_gu = d;
+    p.m_gu = f;
+    p.k_dn = f;
+    p.m_dn = d;
+    p.top_k = k;
+    p.n_rows = n_rows;
+    p.n_shared = n_shared;
+    p.n_gu = f / 16;
+    p.n_dn = d / 64;
+    p.lag = 4;
+    p.routed_off = 1;
+    p.n_slots = 1;
+    p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
+    p.x16 = reinterpret_cast<const __half*>(base + L.x16s);
+    p.xexp = reinterpret_cast<const int*>(base + L.xexps);
+    p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_sh);
+    p.hmax = reinterpret_cast<uint32_t*>(base + L.hmax_sh);
+    p.h = reinterpret_cast<float*>(base + L.h_sh);  // shared pairs: rows [0, n_shared * N)
+    p.out_shared = reinterpret_cast<float*>(base + L.shared_y);
+    p.pairs_cap = (int64_t)n_shared * n_rows_max;
+    p.work_word = CTRL_WORK_SH;
+    p.exit_word = CTRL_EXIT_SH;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    q8_prep_kernel<<<n_rows, 256, 0, s>>>(d, x, MOE_DTYPE_BF16, 1, reinterpret_cast<__half*>(base + L.x16s),
+                                          reinterpret_cast<int*>(base + L.xexps),
+                                          reinterpret_cast<uint32_t*>(base + L.xmaxs), nullptr);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }
 
@@ -1167,6 +1223,8 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
     p.out_shared = y;
     p.dbg_g = p.dbg_u = nullptr;
     p.pairs_cap = 0;  // hmax rows are rewritten by the preparation kernel on every call
+    p.work_word = CTRL_WORK;
+    p.exit_word = CTRL_EXIT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     q8_prep_kernel<<<n_rows, 256, 0, s>>>(k_in, x, x_dtype, swiglu ? 1 : 0, reinterpret_cast<__half*>(base + L.x16),
                                           reinterpret_cast<int*>(base + L.xexp),

@@ -790,9 +790,7 @@ static int launch(const Params& p, cudaStream_t stream) {
     using C = Cfg<NBM>;
     static bool attr = false;
     if (!attr) {
-        if (cudaFuncSetAttribute(tc_expert_kernel<NBM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (kernel_smem_attrs(tc_expert_kernel<NBM>, (int)C::SMEM) != cudaSuccess) return MOE_ERR_CUDA;
         attr = true;
     }
     int dev = 0, sms = 0;

@@ -265,64 +265,164 @@ __device__ __forceinline__ float key_value(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// top-k of one row by one warp.  Lane l holds the keys of experts l, l+32, ...
-// and its largest key with the lowest such expert.  Each round two warp
-// reductions find the largest key and, among the lanes holding it, the lowest
-// expert (ties go to the lower index); that lane drops the key and rescans.
-__device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2) {
-    const int lane = threadIdx.x & 31;
+// expert held by key t of `lane` (t = 4 i + j): e = 128 i + 4 lane + j when the
+// row was read as float4 (E % 4 == 0), else e = lane + 32 t; either way a lane's
+// experts increase with t
+__device__ __forceinline__ int key_expert(int t, int lane, bool vec) {
+    return vec ? 128 * (t >> 2) + 4 * lane + (t & 3) : lane + 32 * t;
+}
+
+// top-k of one row by one warp, with ties going to the lower index.  Every load
+// is issued before any is used.  The k-th largest key T is found bit by bit
+// (most significant first) from warp-wide counts of the keys >= a candidate,
+// stopping as soon as exactly k keys qualify; keys above T are all taken and the
+// keys equal to T are taken in index order.  The k winners are then ranked
+// (larger key first, then lower index) through shared memory `sel` (2k words).
+__device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2, uint32_t* sel) {
+    const int lane = threadIdx.x & 31, K = p.k;
+    const bool vec = (p.E & 3) == 0 && ((uintptr_t)lrow & 15) == 0;
     uint32_t key[32];
+    if (vec) {
+        float4 v[8];
 #pragma unroll
-    for (int t = 0; t < 32; t++) {  // every load in flight before any is used
-        const int e = lane + 32 * t;
-        const float v = (e < p.E) ? (from_l2 ? __ldcg(lrow + e) : lrow[e]) : 0.f;
-        key[t] = (e < p.E) ? sel_key(v) : 0u;
+        for (int i = 0; i < 8; i++) {
+            const int e0 = 128 * i + 4 * lane;
+            v[i] = e0 < p.E ? (from_l2 ? __ldcg(reinterpret_cast<const float4*>(lrow + e0))
+                                       : __ldg(reinterpret_cast<const float4*>(lrow + e0)))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const bool ok = 128 * i + 4 * lane < p.E;
+            key[4 * i + 0] = ok ? sel_key(v[i].x) : 0u;
+            key[4 * i + 1] = ok ? sel_key(v[i].y) : 0u;
+            key[4 * i + 2] = ok ? sel_key(v[i].z) : 0u;
+            key[4 * i + 3] = ok ? sel_key(v[i].w) : 0u;
+        }
+    } else {
+        float v[32];
+#pragma unroll
+        for (int t = 0; t < 32; t++) {
+            const int e = lane + 32 * t;
+            v[t] = e < p.E ? (from_l2 ? __ldcg(lrow + e) : __ldg(lrow + e)) : 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < 32; t++) key[t] = lane + 32 * t < p.E ? sel_key(v[t]) : 0u;
     }
     bool any_nan = false;
 #pragma unroll
     for (int t = 0; t < 32; t++) any_nan |= key[t] == 1u;
     if (__any_sync(0xffffffffu, any_nan) && lane == 0) set_error(p.ctrl, MOE_EBIT_NAN);
-    auto rescan = [&](uint32_t& lmax, int& lfirst) {
-        uint32_t m16[16], m8[8], m4[4];
+
+    // T: the largest value with at least K keys >= T
+    uint32_t T = 0u;
+    for (int bit = 31; bit >= 0; bit--) {
+        const uint32_t cand = T | (1u << bit);
+        uint32_t c = 0;
 #pragma unroll
-        for (int i = 0; i < 16; i++) m16[i] = max(key[2 * i], key[2 * i + 1]);
+        for (int t = 0; t < 32; t++) c += key[t] >= cand ? 1u : 0u;
+        c = __reduce_add_sync(0xffffffffu, c);
+        if (c >= (uint32_t)K) T = cand;
+        if (c == (uint32_t)K) break;  // exactly K keys are >= cand: they are the top K
+    }
+    uint32_t n_gt = 0, n_ge = 0;
 #pragma unroll
-        for (int i = 0; i < 8; i++) m8[i] = max(m16[2 * i], m16[2 * i + 1]);
+    for (int t = 0; t < 32; t++) {
+        n_gt += key[t] > T ? 1u : 0u;
+        n_ge += key[t] >= T ? 1u : 0u;
+    }
+    n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+    n_ge = __reduce_add_sync(0xffffffffu, n_ge);
+    uint32_t take_eq = 0xFFFFFFFFu;  // bit t: key t equal to T is taken
+    if (n_ge > (uint32_t)K) {
+        // ties at T: take them in index order until K are selected
+        int need = K - (int)n_gt;
+        take_eq = 0u;
+        // index order: blocks i, then lanes, then j (vec: experts 128 i + 4 lane + j);
+        // t, then lanes otherwise
+        if (vec) {
 #pragma unroll
-        for (int i = 0; i < 4; i++) m4[i] = max(m8[2 * i], m8[2 * i + 1]);
-        lmax = max(max(m4[0], m4[1]), max(m4[2], m4[3]));
-        lfirst = 31;
+            for (int i = 0; i < 8; i++) {
+                if (need <= 0) break;
+                uint32_t cnt = 0;
 #pragma unroll
-        for (int t = 31; t >= 0; t--) lfirst = (key[t] == lmax) ? t : lfirst;
-    };
-    uint32_t lmax;
-    int lfirst;
-    rescan(lmax, lfirst);
-    uint32_t my_key = 0u;
-    int my_idx = 0;
-    for (int j = 0; j < p.k; j++) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, lmax);
-        const uint32_t w = __reduce_min_sync(0xffffffffu, lmax == m ? (uint32_t)(lfirst * 32 + lane) : 0xFFFFFFFFu);
-        if (lane == j) {
-            my_key = m;
-            my_idx = (int)w;
-        }
-        if ((int)(w & 31u) == lane) {
-            const int tw = (int)(w >> 5);
+                for (int j = 0; j < 4; j++) cnt += key[4 * i + j] == T ? 1u : 0u;
+                // lanes below this one hold lower indices in block i
+                uint32_t before = cnt;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t up = __shfl_up_sync(0xffffffffu, before, o);
+                    if (lane >= o) before += up;
+                }
+                before -= cnt;  // exclusive
+                const uint32_t tot = __shfl_sync(0xffffffffu, before + cnt, 31);
+                int mine = need - (int)before;  // how many of this lane's ties in block i are taken
 #pragma unroll
-            for (int t = 0; t < 32; t++) key[t] = (t == tw) ? 0u : key[t];
-            rescan(lmax, lfirst);
+                for (int j = 0; j < 4; j++) {
+                    if (key[4 * i + j] == T && mine > 0) {
+                        take_eq |= 1u << (4 * i + j);
+                        mine--;
+                    }
+                }
+                need -= (int)min(tot, (uint32_t)max(need, 0));
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 32; t++) {
+                if (need <= 0) break;
+                const uint32_t bal = __ballot_sync(0xffffffffu, key[t] == T);
+                const uint32_t before = __popc(bal & ((1u << lane) - 1u));
+                if (key[t] == T && (int)before < need) take_eq |= 1u << t;
+                need -= min(__popc(bal), need);
+            }
         }
     }
-    const float my_val = (lane < p.k) ? key_value(my_key) : 0.f;
+    // compact the K winners (order irrelevant here), then rank them
+    uint32_t mine = 0;
+#pragma unroll
+    for (int t = 0; t < 32; t++) mine += (key[t] > T || (key[t] == T && (take_eq >> t) & 1u)) ? 1u : 0u;
+    uint32_t at = mine;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t up = __shfl_up_sync(0xffffffffu, at, o);
+        if (lane >= o) at += up;
+    }
+    at -= mine;
+#pragma unroll
+    for (int t = 0; t < 32; t++) {
+        if (key[t] > T || (key[t] == T && (take_eq >> t) & 1u)) {
+            sel[at] = key[t];
+            sel[K + at] = (uint32_t)key_expert(t, lane, vec);
+            at++;
+        }
+    }
+    __syncwarp();
+    uint32_t wk = 0u, wi = 0u;
+    int rank = 0;
+    if (lane < K) {
+        wk = sel[lane];
+        wi = sel[K + lane];
+        for (int j = 0; j < K; j++) {
+            const uint32_t kj = sel[j], ij = sel[K + j];
+            rank += (kj > wk || (kj == wk && ij < wi)) ? 1 : 0;
+        }
+    }
+    __syncwarp();
+    if (lane < K) {
+        sel[rank] = wk;
+        sel[K + rank] = wi;
+    }
+    __syncwarp();
+    const uint32_t my_key = lane < K ? sel[lane] : 0u;
+    const int my_idx = lane < K ? (int)sel[K + lane] : 0;
+    __syncwarp();
+    const float my_val = (lane < K) ? key_value(my_key) : 0.f;
     // weights: exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in slot order
     const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
-    const float ex = (lane < p.k) ? expf(my_val - l0) : 0.f;
+    const float ex = (lane < K) ? expf(my_val - l0) : 0.f;
     float sum = 0.f;
-    for (int j = 0; j < p.k; j++) sum += __shfl_sync(0xffffffffu, ex, j);
-    if (lane < p.k) {
-        p.topk_idx[(size_t)n * p.k + lane] = my_idx;
-        p.topk_w[(size_t)n * p.k + lane] = ex / sum;
+    for (int j = 0; j < K; j++) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < K) {
+        p.topk_idx[(size_t)n * K + lane] = my_idx;
+        p.topk_w[(size_t)n * K + lane] = ex / sum;
     }
 }
 
@@ -483,7 +583,9 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     // last CTA: selection, weights and grouping for every row
     const int warp = tid >> 5;
     const float* L = p.logits_in ? p.logits_in : p.logits;
-    for (int n = warp; n < p.N; n += RT_THREADS / 32) topk_row(p, L + (size_t)n * p.E, n, p.logits_in == nullptr);
+    uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw + 32768) + warp * 64;  // 2k words per warp
+    for (int n = warp; n < p.N; n += RT_THREADS / 32)
+        topk_row(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, sel);
     __threadfence();
     __syncthreads();
     int* s_cnt = reinterpret_cast<int*>(smem_raw);
@@ -551,9 +653,7 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     const size_t smem = (size_t)RT_MAX_ROWS * 32 * 17 * 4;  // padded x slice (also covers the grouping tables)
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
+        if (kernel_smem_attrs(route_kernel, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
         attr_set = true;
     }
     route_kernel<<<grid, RT_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(p);

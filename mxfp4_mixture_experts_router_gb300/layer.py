@@ -97,6 +97,11 @@ class MoeLayer:
                            self.shared_pool_desc(), self.n_shared, self.ws, self.n_rows_max, self.y_part,
                            stream)
 
+    def shared_experts(self, n_rows: int, x, stream=None):
+        """The shared experts from x alone (independent of routing)."""
+        B.moe_shared_experts(self.desc, n_rows, x, self.shared_pool_desc(), self.n_shared, self.ws,
+                             self.n_rows_max, stream)
+
     def combine(self, n_rows: int, residual, stream=None):
         shared_y = self.ws.data_ptr() + self.offsets.shared_y if self.n_shared else None
         B.moe_combine(self.desc, n_rows, residual, self.y_part, self.topk_w, shared_y, self.n_shared,
@@ -104,12 +109,51 @@ class MoeLayer:
 
     def forward(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
                 stream=None):
-        """Run one block: x, residual bf16 bits [N][d] on the device; returns out bits [N][d]."""
+        """Run one block: x, residual bf16 bits [N][d] on the device; returns out bits [N][d].
+
+        The shared experts run on a side stream while the block is routed (they need
+        x only); the routed experts follow the routing, and the combine waits for both."""
         n = x.shape[0] if n_rows is None else n_rows
-        self.route(n, x, logits_in=logits_in, stream=stream)
-        self.experts(n, mode=mode, stream=stream)
-        self.combine(n, residual, stream=stream)
+        self._block(n, x, residual, logits_in, mode, None)
         return self.out[:n]
+
+    def _side(self):
+        if getattr(self, "_side_stream", None) is None:
+            self._side_stream = torch.cuda.Stream(device=self.device)
+        return self._side_stream
+
+    def _block(self, n, x, residual, logits_in, mode, evs):
+        """route (+ shared experts beside it) -> routed experts -> combine on the current
+        stream; evs, if given: 5 events recorded before the routing, after it, after
+        the join with the shared experts, after the routed experts, after the combine."""
+        main = torch.cuda.current_stream()
+        concurrent = self.n_shared > 0 and (mode & 0xFF) == B.MOE_MODE_DECODE and not (mode & B.MOE_MODE_DEBUG_GU)
+        if evs:
+            evs[0].record()
+        if concurrent:
+            side = self._side()
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                self.shared_experts(n, x)
+        self.route(n, x, logits_in=logits_in)
+        if evs:
+            evs[1].record()
+        if concurrent:
+            main.wait_stream(side)
+            if evs:
+                evs[2].record()
+            self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
+        elif evs:
+            self.experts(n, mode=mode | B.MOE_MODE_SHARED_ONLY)
+            evs[2].record()
+            self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
+        else:
+            self.experts(n, mode=mode)
+        if evs:
+            evs[3].record()
+        self.combine(n, residual)
+        if evs:
+            evs[4].record()
 
     def capture(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
                 events: bool = False):
@@ -118,11 +162,11 @@ class MoeLayer:
         The graph reads the block from the given device buffers (x, residual and, if
         given, logits_in): refill them and call ``graph.replay()`` per block; the
         output lands in ``self.out``.  Kernel parameters, including the TMA tensor
-        maps, are fixed at capture time.  With events=True the expert step is issued
-        as two calls (shared experts, then routed experts) and five timing events are
-        recorded inside the graph (before route, before the shared experts, before the
-        routed experts, before combine, after combine) and returned; the events are
-        None if the runtime refuses them."""
+        maps, are fixed at capture time.  The graph runs the shared experts on a side
+        stream beside the routing, as forward() does.  With events=True five timing
+        events are recorded inside the graph (before the routing, after it, after the
+        join with the shared experts, after the routed experts, after the combine) and
+        returned; the events are None if the runtime refuses them."""
         import torch as _torch
         n = x.shape[0] if n_rows is None else n_rows
         side = _torch.cuda.Stream()
@@ -133,20 +177,7 @@ class MoeLayer:
         _torch.cuda.synchronize()
 
         def body(evs):
-            if evs:
-                evs[0].record()
-            self.route(n, x, logits_in=logits_in)
-            if evs:
-                evs[1].record()
-                self.experts(n, mode=mode | B.MOE_MODE_SHARED_ONLY)
-                evs[2].record()
-                self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
-                evs[3].record()
-            else:
-                self.experts(n, mode=mode)
-            self.combine(n, residual)
-            if evs:
-                evs[4].record()
+            self._block(n, x, residual, logits_in, mode, evs)
 
         evs = None
         if events:

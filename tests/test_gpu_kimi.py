@@ -6,6 +6,7 @@ runners-up of the GEMV-routed rows), each streamed once per block."""
 
 import numpy as np
 import pytest
+import torch
 
 import moe_synth as syn
 from gpu_util import SeededLayer, assert_close_to_oracle, topk_gap
@@ -76,3 +77,41 @@ def test_verification_block_matches_oracle(kimi):
     for i, r in enumerate(rows):
         one = {"out": o["out"][i:i + 1], "out_bf16": o["out_bf16"][i:i + 1]}
         assert_close_to_oracle(g["out"][r:r + 1], one, f"kimi block row {r}")
+
+
+def _route_only(lay, logits):
+    """Routing alone through moe_route (caller logits), at the layer's width."""
+    n = logits.shape[0]
+    x = syn.x_rows(SEED + 7, range(n), KIMI.d_model)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.uint16)
+    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    lay.layer.route(n, xd, logits_in=ld)
+    torch.cuda.synchronize()
+    return lay.layer.topk_idx[:n].cpu().numpy(), lay.layer.topk_w[:n].cpu().numpy()
+
+
+def test_topk_ties_at_full_width(kimi):
+    """Ties at the top-16 boundary spread over the whole 896-wide row (so across the
+    kernel's float4 blocks and lanes): the lower index wins, as in the oracle."""
+    lay, _, _ = kimi
+    E, k = KIMI.n_experts, KIMI.top_k
+    rng = np.random.default_rng(11)
+    lg = np.zeros((7, E), dtype=np.float32)                   # row 0: all equal
+    lg[1] = np.round(rng.normal(size=E) * 2) / 4               # few levels: many ties at the boundary
+    lg[2] = -1.0
+    lg[2, 100:900:37] = 3.0                                    # 22 equal winners for 16 places
+    lg[3] = rng.normal(size=E).astype(np.float32)
+    lg[3, ::3] = 0.0
+    lg[3, 1::3] = -0.0                                         # +0 and -0 tie
+    lg[3, rng.permutation(E)[:10]] = 9.0
+    lg[4] = 0.5
+    lg[4, -40:] = 5.0                                          # 40 tied leaders at the highest indices
+    lg[5] = rng.normal(size=E).astype(np.float32)
+    lg[5, [3, 400, 895]] = np.nan                              # NaN ranks last
+    lg[6] = rng.normal(size=E).astype(np.float32)              # plain
+    idx, w = _route_only(lay, lg)
+    want = orc.select_topk(lg.astype(np.float64), k)
+    assert np.array_equal(idx, want)
+    ok = ~np.isnan(lg).any(axis=1)
+    np.testing.assert_allclose(w[ok], orc.routing_weights(lg.astype(np.float64), want)[ok], rtol=2e-6, atol=1e-7)
+    lay.layer.error_bits()  # the NaN row sets the NaN bit; read and clear it

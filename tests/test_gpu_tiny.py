@@ -166,6 +166,27 @@ def test_shared_experts_tiny():
             assert err < 1e-4, (n, s, err)
 
 
+def test_shared_experts_beside_routing_match_the_sequential_layer():
+    """moe_shared_experts on a side stream beside moe_route (what forward() does)
+    gives the same bits as the shared experts run after the routing on one stream."""
+    lay = SeededLayer(TINY_SHARED, seed=11, n_rows_max=16)
+    L = lay.layer
+    for n in (1, 7, 16):
+        x = to_dev_u16(syn.x_rows(11, range(n), TINY.d_model))
+        res = to_dev_u16(syn.x_rows(11, range(n), TINY.d_model, tag=syn.TAG_RESIDUAL))
+        L.route(n, x)
+        L.experts(n)
+        L.combine(n, res)
+        torch.cuda.synchronize()
+        seq_out = L.out[:n].clone()
+        seq_shared = L.shared_y(n).clone()
+        conc_out = L.forward(x, res).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(L.shared_y(n), seq_shared), n
+        assert torch.equal(conc_out, seq_out), n
+        assert L.error_bits() == 0
+
+
 def test_slot_ready_flag_never_set_times_out_cleanly():
     """A slab whose ready flag nothing sets: the kernel gives up after its bounded
     wait, records MOE_EBIT_TIMEOUT and returns; the context stays usable."""
@@ -180,3 +201,21 @@ def test_slot_ready_flag_never_set_times_out_cleanly():
     lay.layer.slot_ready = None
     ref = lay.run(x, x)
     assert np.array_equal(ok["out"], ref["out"])
+
+
+def test_topk_expert_count_not_a_multiple_of_four():
+    """The scalar-load top-k path (30 experts): exact against the oracle, ties included."""
+    sh = syn.Shape(d_model=256, d_ff=64, n_experts=30, top_k=4, group=32, n_shared=0)
+    lay = SeededLayer(sh, seed=2, n_rows_max=8)
+    rng = np.random.default_rng(5)
+    lg = rng.normal(size=(5, sh.n_experts)).astype(np.float32)
+    lg[1] = 0.0
+    lg[2] = np.round(lg[2] * 2) / 2
+    lg[3, -6:] = 4.0
+    x = syn.x_rows(6, range(5), sh.d_model)
+    g = lay.run(x, x, logits=lg)
+    want = orc.select_topk(lg.astype(np.float64), sh.top_k)
+    assert np.array_equal(g["idx"], want)
+    np.testing.assert_allclose(g["w"], orc.routing_weights(lg.astype(np.float64), want), rtol=2e-6, atol=1e-7)
+    o = lay.oracle(x, x, logits=lg)
+    assert_close_to_oracle(g["out"], o, "30 experts")
