@@ -37,7 +37,7 @@ constexpr int TC_GU_SPLIT = 2;
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, xmaxs, gu_done_sh, hmax_sh, h_sh, total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -81,7 +81,6 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     // the routing kernel, which resets the layer's counters
     L.x16s = take((size_t)N * d * 2);
     L.xexps = take((size_t)N * 4);
-    L.xmaxs = take((size_t)N * 4);
     L.gu_done_sh = take(64 * 4);
     L.hmax_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * 4);
     L.h_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);

@@ -1041,8 +1041,52 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }
 
-__global__ void q8_prep_kernel(int k_in, const void* x, int x_dtype, int swiglu, __half* x16, int* xexp,
-                               uint32_t* hmax, float* h);
+// f16 copy of bf16 rows scaled by 2^-p, p from each row's largest magnitude (the
+// same rule as the routing kernel's copy): one CTA per row, the row held in
+// registers between its max and its conversion (16-byte loads, all issued first).
+constexpr int F16_ROW_PER = 4;  // 16-byte chunks per thread: rows of up to 8192 elements at 256 threads
+__global__ void __launch_bounds__(256) rows_to_f16_kernel(int d, const uint16_t* __restrict__ x, __half* x16,
+                                                          int* xexp) {
+    const int n = blockIdx.x, tid = threadIdx.x, nv = d / 8;
+    const uint4* xv = reinterpret_cast<const uint4*>(x + (size_t)n * d);
+    uint4 v[F16_ROW_PER];
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const int c = j * 256 + tid;
+        v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) mx = max(mx, max((w[t] & 0x7FFFu) << 16, w[t] & 0x7FFF0000u));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    __shared__ uint32_t s_max[8];
+    if ((tid & 31) == 0) s_max[tid >> 5] = mx;
+    __syncthreads();
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < 8; w++) m = max(m, s_max[w]);
+    const int p = f16_scale_exponent(m);
+    const float sc = exp2i(-p);
+    uint4* ov = reinterpret_cast<uint4*>(x16 + (size_t)n * d);
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const int c = j * 256 + tid;
+        if (c >= nv) continue;
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * sc, __uint_as_float(w[t] & 0xFFFF0000u) * sc);
+            o[t] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        ov[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0) xexp[n] = p;
+}
 
 extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const moe_pool* shared,
                                   int32_t n_shared, void* ws, int32_t n_rows_max, void* stream) {
@@ -1054,6 +1098,7 @@ extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const ui
     if (n_shared < 1 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
     if (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared) return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)ws & 255) || ((uintptr_t)x & 15)) return MOE_ERR_INVALID_ARG;
+    if (d > F16_ROW_PER * 256 * 8) return MOE_ERR_UNSUPPORTED;
 
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
@@ -1089,9 +1134,8 @@ extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const ui
     p.work_word = CTRL_WORK_SH;
     p.exit_word = CTRL_EXIT_SH;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    q8_prep_kernel<<<n_rows, 256, 0, s>>>(d, x, MOE_DTYPE_BF16, 1, reinterpret_cast<__half*>(base + L.x16s),
-                                          reinterpret_cast<int*>(base + L.xexps),
-                                          reinterpret_cast<uint32_t*>(base + L.xmaxs), nullptr);
+    rows_to_f16_kernel<<<n_rows, 256, 0, s>>>(d, x, reinterpret_cast<__half*>(base + L.x16s),
+                                              reinterpret_cast<int*>(base + L.xexps));
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }

@@ -130,12 +130,17 @@ class MoeLayer:
         concurrent = self.n_shared > 0 and (mode & 0xFF) == B.MOE_MODE_DECODE and not (mode & B.MOE_MODE_DEBUG_GU)
         if evs:
             evs[0].record()
+        if concurrent:  # the shared experts branch off here, before the routing
+            fork = torch.cuda.Event()
+            fork.record(main)
+        # the routing is issued first so that its CTAs are placed before the
+        # persistent shared-expert kernel fills the SMs
+        self.route(n, x, logits_in=logits_in)
         if concurrent:
             side = self._side()
-            side.wait_stream(main)
+            side.wait_event(fork)
             with torch.cuda.stream(side):
                 self.shared_experts(n, x)
-        self.route(n, x, logits_in=logits_in)
         if evs:
             evs[1].record()
         if concurrent:
