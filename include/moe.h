@@ -72,6 +72,12 @@ extern "C" {
                                       streams that join before moe_combine */
 
 /* weight formats of a pool */
+/* bits of a slot's ready flag (moe_expert_block's slot_ready; the device expert cache
+   sets them as the slab's two upload chunks land) */
+#define MOE_SLOT_GATE_UP 1u     /* gate and up planes (and their scales) are in the slot */
+#define MOE_SLOT_DOWN 2u        /* down planes (and scales) are in the slot */
+#define MOE_SLOT_READY 3u       /* the whole slab */
+
 #define MOE_FMT_MXFP4 0
 #define MOE_FMT_Q8_0 1
 
@@ -194,8 +200,10 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
  *  routed       pool holding the routed experts (host struct, MXFP4)
  *  expert_slot  int32 [E] slot of each expert in `routed` (device)
  *  slot_ready   uint32 [routed->n_slots] flags, or NULL when every slot is
- *               resident: an expert's slab is read only after its flag is
- *               non-zero (bounded wait; MOE_EBIT_TIMEOUT when it runs out)
+ *               resident: an expert's gate/up planes are read only after its
+ *               flag has MOE_SLOT_GATE_UP, its down planes only after it has
+ *               MOE_SLOT_DOWN (bounded waits; MOE_EBIT_TIMEOUT when one runs
+ *               out); a resident slot holds MOE_SLOT_READY
  *  shared       pool of n_shared Q8_0 shared experts in slots 0..n_shared-1,
  *               or NULL with n_shared == 0
  *  y_part       fp32 [n_rows][k][d] output of each (row, slot)
@@ -291,6 +299,56 @@ MOE_API int moe_get_error(void* ws, void* stream, uint32_t* bits);
 
 /* Number of SMs the persistent kernels size their grids for (0 if no device). */
 MOE_API int32_t moe_device_sm_count(void);
+
+/*
+ * Device expert cache (host side).  A pool of n_slots device slots (the routed
+ * pool of moe_expert_block) holds (layer, expert) slabs; misses are uploaded from
+ * pinned host memory while the expert kernels run, which start on each expert's
+ * work as its data lands (its ready flag, MOE_SLOT_* bits).
+ *
+ * Pages: "Run Kimi 3.1 locally on one GPU", section "One GPU, three storage
+ * tiers" (experts streamed from the lower tier as the router asks for them; the
+ * NVMe tier itself is out of scope, pinned host memory stands in for it).
+ *
+ * moe_cache_create: slot_base/slot_bytes/n_slots describe the device pool;
+ *   slot_ready uint32 [n_slots] device flags (zeroed here); n_streams upload
+ *   streams (0: planning only -- slot assignment and miss reporting without any
+ *   CUDA call, pointers may be NULL); policy MOE_CACHE_LRU or
+ *   MOE_CACHE_KEEP_MULTI_ROW (LRU that first passes over slots whose last block
+ *   used them on two rows or more).  The cache owns its streams and events.
+ * moe_cache_request: the `count` distinct experts (host int32) one layer of a
+ *   block needs, with the number of the block's rows using each (host int32, or
+ *   NULL = 1) and each expert's pinned host slab (host array of pointers; unused
+ *   when planning only).  Writes each expert's slot (host int32 [count]) and
+ *   whether it was uploaded (host int32 [count], may be NULL).  For the misses it
+ *   writes 0 to the victims' flags on compute_stream (after every earlier kernel
+ *   there, so after every reader of the old slab), then on the upload streams
+ *   copies gate+up, sets MOE_SLOT_GATE_UP, copies down, sets MOE_SLOT_READY.
+ *   Launch the expert kernels for this layer on compute_stream after the call.
+ *   count > n_slots: MOE_ERR_UNSUPPORTED.
+ * moe_cache_sync waits for the uploads; moe_cache_destroy syncs and frees.
+ */
+#define MOE_CACHE_LRU 0
+#define MOE_CACHE_KEEP_MULTI_ROW 1
+
+typedef struct moe_cache moe_cache;
+
+typedef struct moe_cache_stats {
+    int64_t requests;
+    int64_t hits;
+    int64_t misses;
+    int64_t evictions;
+    int64_t bytes_uploaded;
+} moe_cache_stats;
+
+MOE_API int moe_cache_create(const moe_desc* desc, void* slot_base, int64_t slot_bytes, int32_t n_slots,
+                     uint32_t* slot_ready, int32_t n_streams, int32_t policy, moe_cache** out /* host */);
+MOE_API int moe_cache_request(moe_cache* cache, int32_t layer, int32_t count, const int32_t* experts,
+                      const int32_t* rows, const void* const* host_src, int32_t* slot_out,
+                      int32_t* miss_out, void* compute_stream);
+MOE_API int moe_cache_stats_get(const moe_cache* cache, moe_cache_stats* out /* host */);
+MOE_API int moe_cache_sync(moe_cache* cache);
+MOE_API int moe_cache_destroy(moe_cache* cache);
 
 #ifdef __cplusplus
 }

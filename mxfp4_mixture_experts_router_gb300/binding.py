@@ -24,6 +24,9 @@ MOE_EBIT_BAD_SLOT = 0x4
 MOE_MODE_DECODE = 0
 MOE_MODE_PREFILL = 1
 MOE_MODE_DEBUG_GU = 0x100
+MOE_SLOT_GATE_UP = 1
+MOE_SLOT_DOWN = 2
+MOE_SLOT_READY = 3
 MOE_MODE_SHARED_ONLY = 0x200
 MOE_MODE_ROUTED_ONLY = 0x400
 MOE_FMT_MXFP4 = 0
@@ -33,11 +36,14 @@ MOE_EPI_ACCUM = 1
 MOE_EPI_SWIGLU = 2
 MOE_DTYPE_BF16 = 0
 MOE_DTYPE_F32 = 1
+MOE_CACHE_LRU = 0
+MOE_CACHE_KEEP_MULTI_ROW = 1
 
 EXPORTED = [
     "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
     "q8_0_block_matmul_noalloc", "moe_shared_experts",
+    "moe_cache_create", "moe_cache_request", "moe_cache_stats_get", "moe_cache_sync", "moe_cache_destroy",
 ]
 
 
@@ -54,6 +60,10 @@ class MoePool(ctypes.Structure):
 class MoeWsOffsets(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("error_word", "n_unique", "uexp", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y")]
+
+
+class MoeCacheStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("requests", "hits", "misses", "evictions", "bytes_uploaded")]
 
 
 class MoeError(RuntimeError):
@@ -86,6 +96,11 @@ def lib() -> ctypes.CDLL:
         L.moe_route.argtypes = [D, I32, P, P, P, P, P, P, P, I32, I32, P]
         L.moe_expert_block.argtypes = [D, I32, I32, PL, P, P, PL, I32, P, I32, P, P]
         L.moe_shared_experts.argtypes = [D, I32, P, PL, I32, P, I32, P]
+        L.moe_cache_create.argtypes = [D, P, ctypes.c_int64, I32, P, I32, I32, ctypes.POINTER(P)]
+        L.moe_cache_request.argtypes = [P, I32, I32, P, P, P, P, P, P]
+        L.moe_cache_stats_get.argtypes = [P, ctypes.POINTER(MoeCacheStats)]
+        L.moe_cache_sync.argtypes = [P]
+        L.moe_cache_destroy.argtypes = [P]
         L.moe_combine.argtypes = [D, I32, P, P, P, P, I32, P, P]
         L.q8_0_workspace_size.argtypes = [I32, I32, I32]
         L.q8_0_workspace_size.restype = SZ
@@ -197,3 +212,54 @@ def moe_get_error(ws, stream=None) -> int:
 
 def moe_device_sm_count() -> int:
     return lib().moe_device_sm_count()
+
+
+# --- device expert cache -----------------------------------------------------
+
+def moe_cache_create(d: MoeDesc, slot_base, slot_bytes: int, n_slots: int, slot_ready, n_streams: int,
+                     policy: int) -> int:
+    """Opaque cache handle (an int).  n_streams = 0: planning only (no CUDA calls)."""
+    h = ctypes.c_void_p(0)
+    _check(lib().moe_cache_create(ctypes.byref(d), _ptr(slot_base), slot_bytes, n_slots, _ptr(slot_ready),
+                                  n_streams, policy, ctypes.byref(h)), "moe_cache_create")
+    return h.value
+
+
+def moe_cache_request(handle: int, layer: int, experts, rows=None, host_src=None, stream=None):
+    """experts, rows: int32 numpy arrays; host_src: numpy uint64 array of pinned host
+    addresses, or None.  Returns (slots, uploaded) int32 numpy arrays."""
+    import numpy as np
+    e = np.ascontiguousarray(experts, dtype=np.int32)
+    n = int(e.shape[0])
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    src = None if host_src is None else np.ascontiguousarray(host_src, dtype=np.uint64)
+    slots = np.empty(n, dtype=np.int32)
+    miss = np.empty(n, dtype=np.int32)
+    _check(lib().moe_cache_request(ctypes.c_void_p(handle), layer, n, e.ctypes.data,
+                                   None if r is None else r.ctypes.data,
+                                   None if src is None else src.ctypes.data, slots.ctypes.data,
+                                   miss.ctypes.data, _cache_stream(stream)), "moe_cache_request")
+    return slots, miss
+
+
+def _cache_stream(stream):
+    """The caller's stream; with none given, the current one when a GPU is present (a
+    planning-only cache makes no CUDA call and ignores it)."""
+    if stream is not None:
+        return _stream(stream)
+    import torch
+    return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+
+
+def moe_cache_stats(handle: int) -> dict:
+    st = MoeCacheStats()
+    _check(lib().moe_cache_stats_get(ctypes.c_void_p(handle), ctypes.byref(st)), "moe_cache_stats_get")
+    return {n: getattr(st, n) for n, _ in MoeCacheStats._fields_}
+
+
+def moe_cache_sync(handle: int):
+    _check(lib().moe_cache_sync(ctypes.c_void_p(handle)), "moe_cache_sync")
+
+
+def moe_cache_destroy(handle: int):
+    _check(lib().moe_cache_destroy(ctypes.c_void_p(handle)), "moe_cache_destroy")

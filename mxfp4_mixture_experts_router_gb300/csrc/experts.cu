@@ -480,9 +480,11 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
                 set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
                 z = 0;
             }
-            if (p.slot_ready != nullptr && ld_acquire(p.slot_ready + z) == 0u) {
+            // gate/up items need the slot's gate/up planes (bit 0), down items its down planes (bit 1)
+            const uint32_t need = type == IT_GU ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN;
+            if (p.slot_ready != nullptr && (ld_acquire(p.slot_ready + z) & need) == 0u) {
                 const uint64_t t0 = global_ns();
-                while (ld_acquire(p.slot_ready + z) == 0u) {
+                while ((ld_acquire(p.slot_ready + z) & need) == 0u) {
                     // once any wait of this launch has run out, later ones give up at once
                     if (timed_out(p.ctrl)) break;
                     if (global_ns() - t0 > WAIT_LIMIT_NS) {

@@ -225,6 +225,21 @@ __device__ void decode_item(const Params& p, int V, int item, int& type, int& v,
     blk = 0;
 }
 
+// bounded wait until (*flag & bits) != 0; false (with the timeout bit set) if it gave up
+__device__ bool wait_bits(const Params& p, const uint32_t* flag, uint32_t bits) {
+    if ((ld_acquire(flag) & bits) != 0u) return true;
+    const uint64_t t0 = global_ns();
+    while ((ld_acquire(flag) & bits) == 0u) {
+        if (timed_out(p.ctrl)) return false;
+        if (global_ns() - t0 > WAIT_LIMIT_NS) {
+            set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+            return false;
+        }
+        __nanosleep(256);
+    }
+    return true;
+}
+
 // bounded wait until *flag >= target; false (with the timeout bit set) if it gave up
 __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t target) {
     if (ld_acquire(flag) >= target) return true;
@@ -260,8 +275,9 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
         decode_item(p, U, item, type, u, blk, split);
         const uint32_t mu = umeta[u];
         const int z = (int)(mu & ((1u << SLOT_BITS) - 1u)), o0 = (int)((mu >> SLOT_BITS) & 511u), r = (int)(mu >> 27);
-        if (p.slot_ready != nullptr) ok = wait_at_least(p, p.slot_ready + z, 1u);
         const bool gu = type == IT_GU;
+        // gate/up items need the slot's gate/up planes (bit 0), down items its down planes (bit 1)
+        if (p.slot_ready != nullptr) ok = wait_bits(p, p.slot_ready + z, gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN);
         if (ok && !gu) {
             // the expert's SwiGLU activations must be complete before TMA reads them
             ok = wait_at_least(p, p.gu_done + u, (uint32_t)p.n_gu);

@@ -51,6 +51,14 @@ class MoeLayer:
         self.n_slots = n_slots
         self.pool = torch.empty(n_slots * self.slot_bytes, dtype=torch.uint8, device=self.device)
 
+    def attach_pool(self, pool: torch.Tensor, slot_bytes: int, n_slots: int, slot_ready=None):
+        """Use an external routed-expert slot pool (a device expert cache) and its
+        per-slot ready flags."""
+        self.pool = pool
+        self.slot_bytes = slot_bytes
+        self.n_slots = n_slots
+        self.slot_ready = slot_ready
+
     def put_slab(self, slot: int, slab):
         """Copy one MXFP4 slab (numpy uint8 or tensor) into a pool slot."""
         t = torch.as_tensor(slab, dtype=torch.uint8)

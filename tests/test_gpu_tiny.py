@@ -195,7 +195,7 @@ def test_slot_ready_flag_never_set_times_out_cleanly():
     lay.layer.slot_ready = torch.zeros(lay.layer.n_slots, dtype=torch.int32, device="cuda")
     lay.run(x, x)
     assert lay.layer.error_bits() & B.MOE_EBIT_TIMEOUT
-    lay.layer.slot_ready.fill_(1)
+    lay.layer.slot_ready.fill_(B.MOE_SLOT_READY)
     ok = lay.run(x, x)
     assert lay.layer.error_bits() == 0
     lay.layer.slot_ready = None
