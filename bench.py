@@ -435,6 +435,108 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": "ok", "rows": len(rows), "pool_experts": len(experts)}))
 
 
+def host_topk(logits: np.ndarray, k: int) -> np.ndarray:
+    """The experts each row selects, as the routing kernel selects them (larger logit
+    first, ties to the lower index): what the cache client needs before the layer runs."""
+    order = np.lexsort((np.broadcast_to(np.arange(logits.shape[1]), logits.shape), -logits), axis=1)
+    return order[:, :k]
+
+
+def run_cache_bench(args):
+    """Stacked decode through the device expert cache: `layers` Kimi-shaped MoE layers,
+    8-row blocks, (layer, expert) -> one of `bodies` seeded bodies in a pinned host pool,
+    a device cache of `slots` slots filled on 8 upload streams; logits per layer = a fixed
+    per-layer popularity N(0,1) + a block base that drifts as AR(1) (rho 0.9) + row noise
+    N(0, 0.5).  Both eviction policies run on the same sequence of blocks."""
+    import torch
+    from concurrent.futures import ThreadPoolExecutor
+
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+    from mxfp4_mixture_experts_router_gb300.cache import DeviceExpertCache
+    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+
+    build_mod.build()
+    sh = syn.KIMI
+    E, k, d = sh.n_experts, sh.top_k, sh.d_model
+    L, NB, N, slots = args.cache_layers, args.cache_bodies, 8, args.cache_slots
+    t0 = time.perf_counter()
+    host = torch.empty((NB, SLAB), dtype=torch.uint8).pin_memory()
+
+    def fill(b):
+        host[b].copy_(torch.from_numpy(syn.mxfp4_body_slab(SEED, b, sh)))
+
+    with ThreadPoolExecutor(max_workers=max(2, min(16, os.cpu_count() or 2))) as ex:
+        list(ex.map(fill, range(NB)))
+    setup_s = time.perf_counter() - t0
+    base = host.data_ptr()
+    body = np.array([[syn.body_of(l, e, NB) for e in range(E)] for l in range(L)], dtype=np.uint64)
+    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=N, n_shared=0)
+    x = torch.from_numpy(syn.x_rows(SEED, range(N), d).view(np.int16)).cuda().view(torch.uint16)
+    stage = [torch.empty((L, N, E), dtype=torch.float32).pin_memory() for _ in range(2)]
+    stage_done = [None, None]
+    ld = torch.empty((N, E), dtype=torch.float32, device="cuda")
+    rho, W, K = 0.9, args.cache_warmup, args.cache_blocks
+    out = {}
+    for policy, name in ((B.MOE_CACHE_LRU, "lru"), (B.MOE_CACHE_KEEP_MULTI_ROW, "keep_multi_row")):
+        rng = np.random.default_rng(SEED + 1)
+        bias = rng.normal(size=(L, E)).astype(np.float32)
+        state = rng.normal(size=(L, E)).astype(np.float32)
+        cache = DeviceExpertCache(d, sh.d_ff, E, k, n_slots=slots, n_streams=8, policy=policy)
+        stream = torch.cuda.current_stream()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        unique = 0
+        st0 = None
+        for blk in range(W + K):
+            state = rho * state + np.sqrt(1 - rho * rho) * rng.normal(size=(L, E)).astype(np.float32)
+            lg = bias[:, None, :] + state[:, None, :] + 0.5 * rng.normal(size=(L, N, E)).astype(np.float32)
+            buf = blk & 1
+            if stage_done[buf] is not None:
+                stage_done[buf].synchronize()
+            stage[buf].copy_(torch.from_numpy(lg))
+            if blk == W:
+                torch.cuda.synchronize()
+                cache.sync()
+                st0 = cache.stats()
+                t_wall = time.perf_counter()
+                ev0.record()
+            for l in range(L):
+                idx = host_topk(lg[l], k)
+                experts, rows = np.unique(idx, return_counts=True)
+                if blk >= W:
+                    unique += experts.size
+                ptrs = base + body[l, experts] * np.uint64(SLAB)
+                cache.prepare(l, experts, rows, ptrs, lay, stream)
+                ld.copy_(stage[buf][l], non_blocking=True)
+                lay.forward(x, x, logits_in=ld)
+            ev = torch.cuda.Event()
+            ev.record()
+            stage_done[buf] = ev
+        ev1.record()
+        torch.cuda.synchronize()
+        cache.sync()
+        wall = time.perf_counter() - t_wall
+        sec = ev0.elapsed_time(ev1) * 1e-3
+        st = cache.stats()
+        err = lay.error_bits()
+        up = st["bytes_uploaded"] - st0["bytes_uploaded"]
+        hits, miss = st["hits"] - st0["hits"], st["misses"] - st0["misses"]
+        out[name] = {"tok_s": round(N * K / sec, 2), "block_ms": round(sec / K * 1e3, 2),
+                     "h2d_gbs": round(up / sec / 1e9, 1), "hbm_expert_gbs": round(unique * SLAB / sec / 1e9, 1),
+                     "hits": hits, "misses": miss, "hit_rate": round(hits / max(1, hits + miss), 4),
+                     "unique_experts_per_layer": round(unique / (K * L), 1), "error_bits": err,
+                     "wall_s": round(wall, 3)}
+        cache.close()
+    best = max(out.values(), key=lambda v: v["tok_s"])
+    return {"metric": "stacked decode tok/s through the device expert cache (8-row blocks, all drafts accepted)",
+            "value": best["tok_s"], "unit": "tok/s", "n_gpus": 1, "higher_is_better": True,
+            "config": {"workload": f"{L} Kimi K3.1 MoE layers (routed experts only), 8-row blocks, "
+                                   f"{NB} seeded bodies in a pinned host pool ({NB * SLAB / 1e9:.1f} GB), "
+                                   f"{slots}-slot device cache ({slots * SLAB / 1e9:.1f} GB), 8 upload streams",
+                       "blocks": K, "warmup_blocks": W},
+            "policies": out, "setup_s": round(setup_s, 1), "data": "synthetic"}
+
+
 def run_reference(args):
     """The CPU oracle timed on this host's cores: each step is the oracle's expert MLP
     of one (row, selected expert) pair of the workload (17,547,264 expert bytes)."""
@@ -465,7 +567,18 @@ def main():
     ap.add_argument("--profile-case", action="store_true",
                     help="run the small ncu case (a few layers, <1 GB on the device) and exit")
     ap.add_argument("--profile-rows", type=int, default=1)
+    ap.add_argument("--cache-bench", action="store_true",
+                    help="stacked decode through the device expert cache (one JSON line) and exit")
+    ap.add_argument("--cache-layers", type=int, default=92)
+    ap.add_argument("--cache-bodies", type=int, default=1024)
+    ap.add_argument("--cache-slots", type=int, default=1567)
+    ap.add_argument("--cache-blocks", type=int, default=4)
+    ap.add_argument("--cache-warmup", type=int, default=2)
     args = ap.parse_args()
+
+    if args.cache_bench:
+        print(json.dumps(run_cache_bench(args)))
+        return
 
     if args.profile_case:
         run_profile_case(args)

@@ -314,8 +314,9 @@ MOE_API int32_t moe_device_sm_count(void);
  *   slot_ready uint32 [n_slots] device flags (zeroed here); n_streams upload
  *   streams (0: planning only -- slot assignment and miss reporting without any
  *   CUDA call, pointers may be NULL); policy MOE_CACHE_LRU or
- *   MOE_CACHE_KEEP_MULTI_ROW (LRU that first passes over slots whose last block
- *   used them on two rows or more).  The cache owns its streams and events.
+ *   MOE_CACHE_KEEP_MULTI_ROW (keep the experts used by two rows or more: evict
+ *   the least recently used slot whose last block used it on one row, and when
+ *   every candidate was used by several rows, the most recently used one).  The cache owns its streams and events.
  * moe_cache_request: the `count` distinct experts (host int32) one layer of a
  *   block needs, with the number of the block's rows using each (host int32, or
  *   NULL = 1) and each expert's pinned host slab (host array of pointers; unused

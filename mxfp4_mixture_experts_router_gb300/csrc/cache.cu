@@ -7,15 +7,18 @@
 // lower tier is pinned host memory (the NVMe tier is out of scope).
 //
 // Host side only.  A request names the experts one layer of a block needs; hits
-// keep their slot, misses take a free slot or evict one (plain LRU, or LRU that
-// first passes over slots whose last block used them on at least two rows).
+// keep their slot, misses take a free slot or evict one: plain LRU, or "keep the
+// experts used by two rows or more": the least recently used slot whose last
+// block used it on a single row, and when every candidate was used by several
+// rows, the most recently used of them (so a working set larger than the cache
+// keeps the longer-held experts instead of cycling through all of them).
 // For the misses, in this order:
 //   compute stream: each victim's ready flag is written 0 (after every earlier
 //                   kernel on that stream, so after every reader of the old slab)
 //   compute stream: an event is recorded
 //   upload stream (one of n, round robin): waits for the event, copies the
 //                   slab's gate+up part, sets MOE_SLOT_GATE_UP, copies the down
-//                   part, sets MOE_SLOT_DOWN
+//                   part, sets MOE_SLOT_READY (both bits)
 // The expert kernels wait (bounded) for the bit each work item needs, so the
 // gate/up work on an expert starts while its down part is still in flight.
 // With zero upload streams the cache only plans (slot assignment and misses,
@@ -68,9 +71,10 @@ void touch(moe_cache* c, int32_t s) {
     sl.pos = c->order.begin();
 }
 
-// a slot for a miss of request `seq`: a free one, else the least recently used
-// slot that this request does not use (under MOE_CACHE_KEEP_MULTI_ROW, first
-// among slots whose last block used them on fewer than two rows)
+// a slot for a miss of request `seq`, never one this request uses: a free one;
+// else under MOE_CACHE_LRU the least recently used; under
+// MOE_CACHE_KEEP_MULTI_ROW the least recently used single-row slot, and failing
+// that the most recently used slot
 int32_t pick_victim(moe_cache* c, int64_t seq) {
     if (!c->free_slots.empty()) {
         const int32_t s = c->free_slots.back();
@@ -82,6 +86,9 @@ int32_t pick_victim(moe_cache* c, int64_t seq) {
             const moe_cache::Slot& sl = c->slots[*it];
             if (sl.last != seq && sl.rows < 2) return *it;
         }
+        for (auto it = c->order.begin(); it != c->order.end(); ++it)
+            if (c->slots[*it].last != seq) return *it;
+        return -1;
     }
     for (auto it = c->order.rbegin(); it != c->order.rend(); ++it)
         if (c->slots[*it].last != seq) return *it;

@@ -3,8 +3,9 @@ eviction policies, through the library's cache in planning mode (no upload
 streams, so no CUDA call is made and these tests run without a GPU).
 
 The expected behaviour is a small independent model of the policies written
-here: plain LRU, and LRU that first passes over slots whose last block used them
-on two rows or more; a request never evicts one of its own experts."""
+here: plain LRU, and "keep the experts used by two rows or more" (the least
+recently used single-row slot, else the most recently used slot); a request
+never evicts one of its own experts."""
 
 import numpy as np
 import pytest
@@ -59,8 +60,9 @@ class Model:
                 cands = [s for s in self.order if s not in mine]
                 if self.keep:
                     few = [s for s in cands if self.rows[s] < 2]
-                    cands = few or cands
-                s = cands[0]
+                    s = few[0] if few else cands[-1]
+                else:
+                    s = cands[0]
                 del self.where[self.key[s]]
                 self.evictions += 1
             self.key[s] = (layer, e)
@@ -129,6 +131,15 @@ def test_random_traffic_matches_the_model():
         reqs.append((layer, experts, rows))
     for pol in (B.MOE_CACHE_LRU, B.MOE_CACHE_KEEP_MULTI_ROW):
         run_both(10, pol, reqs)
+
+
+def test_keep_multi_row_holds_a_working_set_larger_than_the_cache():
+    # a cyclic scan over 3 layers x 4 multi-row experts with 8 slots: LRU never hits,
+    # keeping the longer-held experts does
+    reqs = [(t % 3, [0, 1, 2, 3], [2, 2, 2, 2]) for t in range(30)]
+    lru = run_both(8, B.MOE_CACHE_LRU, reqs)
+    keep = run_both(8, B.MOE_CACHE_KEEP_MULTI_ROW, reqs)
+    assert lru["hits"] == 0 and keep["hits"] > 30
 
 
 def test_more_experts_than_slots_is_refused():
