@@ -72,11 +72,14 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.x_sc = take((size_t)L.mx_rows_x * (d / 32));
     L.h_mx = take((size_t)L.mx_rows_h * f);
     L.h_sc = take((size_t)L.mx_rows_h * (f / 32));
-    L.gu_done_tc = take((size_t)E * 4);
-    // split-K gate/up partial sums of the block-scaled kernel: [f/64 tiles][TC_GU_SPLIT]
-    // [routed pairs][64 gate + 64 up] floats, and one arrival counter per (expert, tile)
+    // the block-scaled kernel works on chunks of at most 16 pairs of one expert:
+    // at most E + N*k/16 of them; one finished-tile counter per chunk
+    const int64_t chunks = E + (N * k + 15) / 16;
+    L.gu_done_tc = take((size_t)chunks * 4);
+    // split-K gate/up partial sums: [f/64 tiles][TC_GU_SPLIT][routed pairs][64 gate + 64 up]
+    // floats, and one arrival counter per (chunk, tile)
     L.gu_part = take((size_t)(f / 64) * TC_GU_SPLIT * (N * k) * 128 * 4);
-    L.gu_cnt = take((size_t)E * (f / 64) * 4);
+    L.gu_cnt = take((size_t)chunks * (f / 64) * 4);
     // the shared-expert call's own activation copy and counters: it runs beside
     // the routing kernel, which resets the layer's counters
     L.x16s = take((size_t)N * d * 2);

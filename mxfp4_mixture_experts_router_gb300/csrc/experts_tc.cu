@@ -47,13 +47,11 @@ constexpr int A_BYTES = 128 * KC;           // 128 rows x 256 codes, one byte ea
 constexpr int SC_MAX = 112;                 // scale bytes per row of one item (its K range / 32)
 constexpr int SA_BYTES = 128 * SC_MAX;      // A scales of an item
 constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens (xor-swizzled)
-constexpr int MAX_U = 512;                  // experts of one block (N*k <= 16*32)
-constexpr int META_BYTES = MAX_U * 4;       // packed (slot, first pair, pairs) per expert
+constexpr int CHUNK = 16;                   // pairs of one expert per work item (48 MMA columns)
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
 constexpr int MAX_NST = 5;
-constexpr int SLOT_BITS = 18;     // packed expert entry: slot | first pair << 18 | pairs << 27
 
 // Two configurations: blocks of up to 5 rows (16 activation rows, 5-stage ring)
 // and of up to 16 rows (48 activation rows, 4-stage ring).
@@ -74,6 +72,9 @@ struct Cfg {
     static constexpr uint32_t TM_SFA = 2 * ACC_SET;    // A scales: + stage*8 + set*4 (four 32-row columns)
     static constexpr uint32_t TM_SFB = TM_SFA + NST * 8;
     static constexpr uint32_t TM_COLS = TM_SFB + NST * 8 <= 256 ? 256 : 512;
+    // per expert: (slot, first pair | pairs << 16) and the prefix of its chunk counts
+    static constexpr int MAX_U = NBM == 16 ? 256 : 1024;
+    static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + 12;
     static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -88,7 +89,7 @@ struct Params {
     CUtensorMap a_dn;       // down codes {128 K, d rows, f/128, slot}
     CUtensorMap s_gu;       // gate and up E8M0 scales {d/32, f rows, 2, slot}
     CUtensorMap s_dn;       // down scales {f/32, d rows, slot}
-    int d, f, k, n_rows, n_shared, nbx, nk;
+    int d, f, k, n_rows, n_shared, nk;
     int n_gu, n_dn, lag, debug;
     const int* expert_slot;
     const uint32_t* slot_ready;
@@ -109,12 +110,15 @@ struct Params {
     float* dbg_u;
 };
 
+// one stage: item, type, chunk id (work unit of <= CHUNK pairs of one expert), tile,
+// split, stage index within the item, the item's stages, MMA N, scale buffer and
+// row pitch, K base, activation rows, first activation row (down) / first pair
 struct Meta {
-    int item, type, u, blk, split, chunk, nchunks, nb, sbuf, sc, kbase, nrow, brow, pad[3];
+    int item, type, c, blk, split, chunk, nchunks, nb, sbuf, sc, kbase, nrow, brow, p0, pad[2];
 };
 
 struct AccMeta {
-    int item, type, u, blk, split, nb, pad[2];
+    int item, type, c, blk, split, nb, p0, rc;
 };
 
 // --- tcgen05 wrappers -------------------------------------------------------
@@ -192,37 +196,49 @@ __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
 // distinct banks
 __device__ __forceinline__ int xch_at(int m, int n) { return m * 16 + (n ^ (m & 15)); }
 
-// item -> (type, expert, tile, split): the gate/up items of expert i (tile-major,
-// splits adjacent), then the down items of expert i - lag
+// item -> (type, chunk, tile, split).  Groups i = 0 .. V+lag-1 hold the gate/up
+// items of chunk i (tile-major, splits adjacent; if i < V) followed by the down
+// items of chunk i - lag (if that is a chunk), so a chunk's down items come lag
+// chunks after its gate/up items.  Closed form over the three runs of group sizes.
 __device__ void decode_item(const Params& p, int V, int item, int& type, int& v, int& blk, int& split) {
-    const int n_gi = p.n_gu * S;
-    int rest = item;
+    const int n_gi = p.n_gu * S, n_dn = p.n_dn, lag = p.lag;
     split = 0;
-    for (int i = 0; i < V + p.lag; i++) {
-        if (i < V) {
-            if (rest < n_gi) {
-                type = IT_GU;
-                v = i;
-                blk = rest / S;
-                split = rest - blk * S;
-                return;
-            }
-            rest -= n_gi;
+    auto gu_at = [&](int g, int rest) {
+        type = IT_GU;
+        v = g;
+        blk = rest / S;
+        split = rest - blk * S;
+    };
+    auto dn_at = [&](int g, int rest) {
+        type = IT_DN;
+        v = g;
+        blk = rest;
+    };
+    if (lag <= V) {
+        const int a = lag * n_gi;                       // groups [0, lag): gate/up only
+        if (item < a) return gu_at(item / n_gi, item % n_gi);
+        const int w = n_gi + n_dn, b = a + (V - lag) * w;   // groups [lag, V): both
+        if (item < b) {
+            const int g = lag + (item - a) / w, rest = (item - a) % w;
+            if (rest < n_gi) return gu_at(g, rest);
+            return dn_at(g - lag, rest - n_gi);
         }
-        const int vd = i - p.lag;
-        if (vd >= 0 && vd < V) {
-            if (rest < p.n_dn) {
-                type = IT_DN;
-                v = vd;
-                blk = rest;
-                return;
-            }
-            rest -= p.n_dn;
-        }
+        const int g = V + (item - b) / n_dn;            // groups [V, V+lag): down only
+        return dn_at(g - lag, (item - b) % n_dn);
     }
-    type = IT_GU;
-    v = 0;
-    blk = 0;
+    const int a = V * n_gi;                             // groups [0, V): gate/up only
+    if (item < a) return gu_at(item / n_gi, item % n_gi);
+    return dn_at((item - a) / n_dn, (item - a) % n_dn);  // groups [lag, lag+V): down only
+}
+
+// the expert holding chunk c: the last u with cp[u] <= c
+__device__ __forceinline__ int chunk_expert(const int* cp, int U, int c) {
+    int lo = 0, hi = U - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cp[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    return lo;
 }
 
 // bounded wait until (*flag & bits) != 0; false (with the timeout bit set) if it gave up
@@ -258,29 +274,34 @@ __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t ta
 // ---------------------------------------------------------------------------
 
 template <int NBM>
-__device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned char* smem, unsigned char* scbuf,
-                         uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf, Meta* meta) {
+__device__ void producer(const Params& p, int U, const uint2* umeta, const int* cp, unsigned char* smem,
+                         unsigned char* scbuf, uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf,
+                         Meta* meta) {
     using C = Cfg<NBM>;
     tma_prefetch_desc(&p.a_gu);
     tma_prefetch_desc(&p.a_dn);
     tma_prefetch_desc(&p.s_gu);
     tma_prefetch_desc(&p.s_dn);
-    const int total = U * (p.n_gu * S + p.n_dn);
+    const int V = cp[U];  // chunks
+    const int total = V * (p.n_gu * S + p.n_dn);
     uint32_t stage = 0, phase = 0, pending = 0, pending_par = 0;
     uint32_t sc_any = 0u, sc_cnt = 0u;  // per scale buffer: armed at all, and the parity of its arm count
     bool ok = true;
     int item = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
     for (int seq = 0; ok && item < total; seq++) {
-        int type, u, blk, split;
-        decode_item(p, U, item, type, u, blk, split);
-        const uint32_t mu = umeta[u];
-        const int z = (int)(mu & ((1u << SLOT_BITS) - 1u)), o0 = (int)((mu >> SLOT_BITS) & 511u), r = (int)(mu >> 27);
+        int type, cid, blk, split;
+        decode_item(p, V, item, type, cid, blk, split);
+        const int u = chunk_expert(cp, U, cid);
+        const uint2 mu = umeta[u];
+        const int z = (int)mu.x, o0 = (int)(mu.y & 0xFFFFu), r = (int)(mu.y >> 16);
+        const int p0 = o0 + CHUNK * (cid - cp[u]);       // the chunk's first pair
+        const int rc = min(CHUNK, o0 + r - p0);          // and its pairs
         const bool gu = type == IT_GU;
         // gate/up items need the slot's gate/up planes (bit 0), down items its down planes (bit 1)
         if (p.slot_ready != nullptr) ok = wait_bits(p, p.slot_ready + z, gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN);
         if (ok && !gu) {
-            // the expert's SwiGLU activations must be complete before TMA reads them
-            ok = wait_at_least(p, p.gu_done + u, (uint32_t)p.n_gu);
+            // the chunk's SwiGLU activations must be complete before they are read
+            ok = wait_at_least(p, p.gu_done + cid, (uint32_t)p.n_gu);
             asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         if (!ok) break;
@@ -288,8 +309,8 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
         const int kbase = gu ? split * kr : 0;
         const int nch = kr / KC;
         const int sc = kr / 32;                // scale bytes per row of the item
-        const int nb = gu ? p.nbx : round16(3 * r);   // activation rows loaded = MMA N
-        const int brow = gu ? 0 : 3 * o0;
+        const int nb = round16(3 * rc);       // activation rows loaded = MMA N
+        const int brow = 3 * p0;               // down: the chunk's rows of h
         const int row0 = gu ? blk * 64 : blk * 128;
         const int sbuf = seq & 1;
         unsigned char* sa = scbuf + sbuf * C::SCB;
@@ -307,7 +328,7 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
             Meta& mt = meta[stage];
             mt.item = item;
             mt.type = type;
-            mt.u = u;
+            mt.c = cid;
             mt.blk = blk;
             mt.split = split;
             mt.chunk = c;
@@ -316,8 +337,9 @@ __device__ void producer(const Params& p, int U, const uint32_t* umeta, unsigned
             mt.sbuf = sbuf;
             mt.sc = sc;
             mt.kbase = kbase;
-            mt.nrow = gu ? 3 * p.n_rows : 3 * r;
+            mt.nrow = 3 * rc;
             mt.brow = brow;
+            mt.p0 = p0;
             if (c == 0) {
                 // the item's scales into its buffer, which item seq-2 used last: every
                 // item has at least NST stages, so that item's scales have all been
@@ -378,8 +400,44 @@ struct BStage {
     uint2 s[2];
 };
 
+// source row of activation row `row` of a stage: gate/up gathers the E4M3 terms of
+// the block rows of the chunk's pairs (3 x the pair's token + term), down reads the
+// chunk's rows of h (3 x pair + term) in place
+__device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row) {
+    if (m.type != IT_GU) return m.brow + row;
+    const int q = row / 3;
+    return 3 * (__ldg(p.pair + m.p0 + q) / p.k) + (row - 3 * q);
+}
+
+// the source rows this thread reads for an item (data rows j / 16 of its chunks j,
+// scale rows lane and 32 + lane), resolved once per item
 template <int NBM>
-__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b) {
+struct BRows {
+    int item = -1;
+    int d[NBM / 8];
+    int s[2];
+};
+
+template <int NBM>
+__device__ __forceinline__ void b_rows(const Params& p, const Meta& m, int t, int lane, BRows<NBM>& r) {
+    if (r.item == m.item) return;
+    r.item = m.item;
+#pragma unroll
+    for (int i = 0; i < NBM / 8; i++) {
+        const int row = (t + 128 * i) >> 4;
+        r.d[i] = row < m.nrow ? b_src_row(p, m, row) : 0;
+    }
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        const int row = 32 * c + lane;
+        r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(p, m, row) : 0;
+    }
+}
+
+template <int NBM>
+__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b,
+                                       BRows<NBM>& rows) {
+    b_rows<NBM>(p, m, t, lane, rows);
     const bool gu = m.type == IT_GU;
     const uint8_t* src = gu ? p.x_mx : p.h_mx;
     const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
@@ -388,14 +446,14 @@ __device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk
 #pragma unroll
     for (int i = 0; i < NBM / 8; i++) {
         const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
-        b.d[i] = row < m.nrow ? __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(m.brow + row) * ld + k0 + c16 * 16))
+        b.d[i] = row < m.nrow ? __ldcg(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * ld + k0 + c16 * 16))
                               : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int c = 0; c < 2; c++) {
         const int row = 32 * c + lane;
         b.s[c] = (row < m.nrow && row < NBM)
-                     ? __ldcg(reinterpret_cast<const uint2*>(ssrc + (size_t)(m.brow + row) * (ld / 32) + k0 / 32))
+                     ? __ldcg(reinterpret_cast<const uint2*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
                      : make_uint2(0, 0);
     }
 }
@@ -417,6 +475,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
     uint32_t stage = 0, phase = 0;
     uint32_t scph = 0;  // parity of the next phase of each scale buffer
     BStage<NBM> b;
+    BRows<NBM> rows;
     int have_item = -1, have_chunk = -1;
     while (true) {
         if (__shfl_sync(0xffffffffu, mbar_wait(&mready[stage], phase) ? 1 : 0, 0) == 0) {
@@ -425,7 +484,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         }
         const Meta m = meta[stage];
         if (m.item < 0) break;
-        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b);
+        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b, rows);
         unsigned char* bst = smem + (size_t)stage * C::STAGE + A_BYTES;
 #pragma unroll
         for (int i = 0; i < NBM / 8; i++) {
@@ -459,7 +518,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         if (lane == 0) mbar_arrive(&sfr[stage]);
         // the next stage of the same item: its activations are known now
         if (m.chunk + 1 < m.nchunks) {
-            b_load<NBM>(p, m, m.chunk + 1, t, lane, b);
+            b_load<NBM>(p, m, m.chunk + 1, t, lane, b, rows);
             have_item = m.item;
             have_chunk = m.chunk + 1;
         } else {
@@ -505,10 +564,12 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
             AccMeta& a = am[b];
             a.item = m.item;
             a.type = m.type;
-            a.u = m.u;
+            a.c = m.c;
             a.blk = m.blk;
             a.split = m.split;
             a.nb = m.nb;
+            a.p0 = m.p0;
+            a.rc = m.nrow / 3;
         }
         const uint32_t st = smem_u32(smem + (size_t)stage * C::STAGE);
         const uint32_t b_half = (uint32_t)m.nb * 128;   // the B box's second 128-K half
@@ -548,11 +609,11 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
 
 // warps 6..9: TMEM lane quadrant q = warp % 4, accumulator row m = 32q + lane
 template <int NBM>
-__device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase, float* xch, int* eflag,
-                         uint64_t* acc_full, uint64_t* acc_empty, const AccMeta* am) {
+__device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag, uint64_t* acc_full,
+                         uint64_t* acc_empty, const AccMeta* am) {
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
-    const int N = p.n_rows, k = p.k;
+    const int N = p.n_rows;
     uint32_t it = 0;
     while (true) {
         const uint32_t b = it & 1u;
@@ -594,13 +655,12 @@ __device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase,
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
         const int m = 32 * q + lane;
-        const uint32_t mu = umeta[a.u];
-        const int o0 = (int)((mu >> SLOT_BITS) & 511u), r = (int)(mu >> 27);
+        const int o0 = a.p0, r = a.rc;  // the chunk's pairs: o0 .. o0 + r - 1, MMA columns 3 per pair
         if (a.type == IT_GU) {
-            // the 3 term columns of token n summed in order; rows 0..63 gate, 64..127 up
+            // the 3 term columns of each pair summed in order; rows 0..63 gate, 64..127 up
 #pragma unroll
             for (int n = 0; n < NBM / 3; n++)
-                if (n < N)
+                if (n < r)
                     xch[xch_at(m, n)] = __uint_as_float(v[3 * n]) + __uint_as_float(v[3 * n + 1]) +
                                         __uint_as_float(v[3 * n + 2]);
             epi_sync();
@@ -609,16 +669,15 @@ __device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase,
             for (int task = ew; task < 2 * r; task += 4) {
                 const int col = task >> 1, half = task & 1;
                 const int P = o0 + col;
-                const int n = __ldg(p.pair + P) / k;
                 const int row = 64 * half + lane;
                 float* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + P) * 128;
-                dst[row] = xch[xch_at(row, n)];
-                dst[row + 32] = xch[xch_at(row + 32, n)];
+                dst[row] = xch[xch_at(row, col)];
+                dst[row + 32] = xch[xch_at(row + 32, col)];
             }
             __threadfence();
             epi_sync();
             if (ew == 0 && lane == 0)
-                *eflag = atomicAdd(p.gu_cnt + (size_t)a.u * p.n_gu + a.blk, 1u) == (uint32_t)(S - 1);
+                *eflag = atomicAdd(p.gu_cnt + (size_t)a.c * p.n_gu + a.blk, 1u) == (uint32_t)(S - 1);
             epi_sync();
             if (*eflag) {
                 // the tile's last split: sum the splits in split order, then SwiGLU
@@ -653,7 +712,7 @@ __device__ void epilogue(const Params& p, const uint32_t* umeta, uint32_t tbase,
                 }
                 if (wrote) __threadfence();
                 epi_sync();
-                if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.u, 1u);
+                if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.c, 1u);
             }
         } else {
             const int m0 = a.blk * 128;
@@ -678,8 +737,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* scbuf = smem + (size_t)C::NST * C::STAGE;
     float* xch = reinterpret_cast<float*>(scbuf + 2 * C::SCB);
-    uint32_t* umeta = reinterpret_cast<uint32_t*>(xch + XCH_FLOATS);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(umeta + MAX_U);
+    uint2* umeta = reinterpret_cast<uint2*>(xch + XCH_FLOATS);
+    int* cp = reinterpret_cast<int*>(umeta + C::MAX_U);  // [MAX_U + 1] chunk prefix
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)C::NST * C::STAGE + 2 * C::SCB + XCH_FLOATS * 4 +
+                                                 ((C::META_BYTES + 15) & ~15));
     uint64_t* full = bars;
     uint64_t* empty = full + C::NST;
     uint64_t* sfr = empty + C::NST;
@@ -695,7 +756,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int U = min((int)p.ctrl[CTRL_UNIQUE], MAX_U);
+    const int U = min((int)p.ctrl[CTRL_UNIQUE], C::MAX_U);
     if (tid == 0) {
         for (int s = 0; s < C::NST; s++) {
             mbar_init(&full[s], 1);
@@ -717,7 +778,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
                      "r"(C::TM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    // every expert's slot and pair range, packed (all loads in flight at once)
+    // every expert's slot and pair range (all loads in flight at once), then the
+    // prefix of its chunk counts (one warp: contiguous runs per lane, then a scan)
     for (int u = tid; u < U; u += NTHREADS) {
         int z = __ldg(p.expert_slot + __ldg(p.uexp + u));
         const int o0 = __ldg(p.off + u), r = __ldg(p.off + u + 1) - o0;
@@ -725,7 +787,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
             set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
             z = 0;
         }
-        umeta[u] = (uint32_t)z | ((uint32_t)o0 << SLOT_BITS) | ((uint32_t)r << 27);
+        umeta[u] = make_uint2((uint32_t)z, (uint32_t)o0 | ((uint32_t)r << 16));
+    }
+    __syncthreads();
+    if (warp == 1) {
+        const int lane = tid & 31, per = (U + 31) / 32, b0 = lane * per, b1 = min(U, b0 + per);
+        int sum = 0;
+        for (int u = b0; u < b1; u++) sum += ((int)(umeta[u].y >> 16) + CHUNK - 1) / CHUNK;
+        int incl = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int up = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += up;
+        }
+        int run = incl - sum;
+        for (int u = b0; u < b1; u++) {
+            cp[u] = run;
+            run += ((int)(umeta[u].y >> 16) + CHUNK - 1) / CHUNK;
+        }
+        if (lane == 31) cp[U] = incl;
     }
     fence_before();
     __syncthreads();
@@ -733,13 +812,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const uint32_t tbase = *tslot;
 
     if (warp == 0) {
-        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, smem, scbuf, full, empty, mready, scf, meta);
+        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, meta);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
         scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sfr, meta);
     } else {
-        epilogue<NBM>(p, umeta, tbase, xch, eflag, acc_full, acc_empty, am);
+        epilogue<NBM>(p, tbase, xch, eflag, acc_full, acc_empty, am);
     }
 
     fence_before();
@@ -754,8 +833,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     __syncthreads();
     if (s_last) {
         __threadfence();
-        for (int i = tid; i < U; i += NTHREADS) p.gu_done[i] = 0;
-        for (int i = tid; i < U * p.n_gu; i += NTHREADS) p.gu_cnt[i] = 0;
+        const int V = cp[U];
+        for (int i = tid; i < V; i += NTHREADS) p.gu_done[i] = 0;
+        for (int i = tid; i < V * p.n_gu; i += NTHREADS) p.gu_cnt[i] = 0;
         if (tid == 0) {
             p.ctrl[CTRL_WORK_TC] = 0;
             p.ctrl[CTRL_EXIT_TC] = 0;
@@ -826,7 +906,7 @@ static int launch(const Params& p, cudaStream_t stream) {
 bool tc_expert_supported(int d, int f, int n_rows) {
     using namespace tc;
     return d % (512 * S) == 0 && d / S / 32 <= SC_MAX && d / S / KC >= MAX_NST && f % 512 == 0 &&
-           f / 32 <= SC_MAX && f / KC >= MAX_NST && n_rows >= 1 && n_rows <= 16;
+           f / 32 <= SC_MAX && f / KC >= MAX_NST && n_rows >= 1;
 }
 
 int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool* routed, const int32_t* expert_slot,
@@ -834,7 +914,10 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
                      cudaStream_t stream) {
     using namespace tc;
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
-    if (routed->n_slots > (1 << SLOT_BITS) || n_rows * k > MAX_U) return MOE_ERR_UNSUPPORTED;
+    // first pair and pair count share one 32-bit word per expert; a block of up to 5
+    // rows runs the 16-column configuration (at most 5 * k experts)
+    if (n_rows * k >= 65536 || E > Cfg<48>::MAX_U || (n_rows <= 5 && n_rows * k > Cfg<16>::MAX_U))
+        return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
     static Params p;
@@ -867,13 +950,11 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
         const uint32_t box[3] = {(uint32_t)(f / 32), 128, 1};
         if (!map_nd(&p.s_dn, U8, down_s, 3, dims, str, box, false)) return MOE_ERR_UNSUPPORTED;
     }
-    const int nbx = ((3 * n_rows + 15) / 16) * 16;
     p.d = d;
     p.f = f;
     p.k = k;
     p.n_rows = n_rows;
     p.n_shared = n_shared;
-    p.nbx = nbx;
     p.nk = n_rows * k;
     p.n_gu = f / 64;
     p.n_dn = d / 128;
@@ -897,7 +978,8 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.y_part = y_part;
     p.dbg_g = reinterpret_cast<float*>(base + L.dbg_g);
     p.dbg_u = reinterpret_cast<float*>(base + L.dbg_u);
-    return nbx <= 16 ? launch<16>(p, stream) : launch<48>(p, stream);
+    // a chunk holds at most min(n_rows, 16) pairs: 3 of them per MMA column triple
+    return n_rows <= 5 ? launch<16>(p, stream) : launch<48>(p, stream);
 }
 
 }  // namespace moe
