@@ -37,7 +37,7 @@ constexpr int TC_GU_SPLIT = 2;
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, rbits, rbits2, rbase, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -87,6 +87,13 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.gu_done_sh = take(64 * 4);
     L.hmax_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * 4);
     L.h_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
+    // grouping of blocks of more than 32 rows: per (32-row group, expert) the bitmap
+    // of rows that selected it (zeroed again after use), its copy, and the offset of
+    // the group's first pair of the expert
+    const int64_t groups = (N + 31) / 32;
+    L.rbits = take((size_t)groups * E * 4);
+    L.rbits2 = take((size_t)groups * E * 4);
+    L.rbase = take((size_t)groups * E * 4);
     L.total = o;
     return L;
 }

@@ -971,10 +971,15 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
         return MOE_ERR_UNSUPPORTED;
     const int base_mode = mode & 0xFF;
-    if (base_mode != MOE_MODE_DECODE) return MOE_ERR_UNSUPPORTED;
+    if (base_mode != MOE_MODE_DECODE && base_mode != MOE_MODE_PREFILL) return MOE_ERR_UNSUPPORTED;
     const bool only_shared = (mode & MOE_MODE_SHARED_ONLY) != 0, only_routed = (mode & MOE_MODE_ROUTED_ONLY) != 0;
     if (only_shared && only_routed) return MOE_ERR_INVALID_ARG;
-    if (n_rows < 1 || n_rows > 16 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
+    if (n_rows < 1 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
+    if (base_mode == MOE_MODE_DECODE && n_rows > 16) return MOE_ERR_UNSUPPORTED;
+    // blocks of more than 16 rows: routed experts on the block-scaled path only (the
+    // shared experts' engine serves up to 16 rows)
+    if (n_rows > 16 && (!tc_expert_supported(d, f, n_rows) || only_shared || (n_shared > 0 && !only_routed)))
+        return MOE_ERR_UNSUPPORTED;
     if (n_shared < 0 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
     if (!pool_ok(desc, routed, MOE_FMT_MXFP4)) return MOE_ERR_INVALID_ARG;
     if (n_shared > 0 && (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared)) return MOE_ERR_INVALID_ARG;

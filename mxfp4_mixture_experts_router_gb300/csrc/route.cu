@@ -46,6 +46,9 @@ struct RouteParams {
     uint8_t* x_mx;        // [3N][d] E4M3 terms of x for the block-scaled expert kernel
     uint8_t* x_sc;        // [3N][d/32] their E8M0 scales
     uint32_t* gu_done_tc;
+    uint32_t* rbits;      // blocks of more than 32 rows: [groups][E] row bitmaps
+    uint32_t* rbits2;
+    int* rbase;
     int v_cap;
     int64_t pairs_cap;
 };
@@ -81,7 +84,7 @@ __device__ void prep_chunk_mx(const RouteParams& p, int n, int c) {
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
-    if (lane == 0 && mx != 0u) atomicMax(p.ctrl + CTRL_XMAX + n, mx);
+    if (lane == 0 && mx != 0u && n < RT_MAX_ROWS) atomicMax(p.ctrl + CTRL_XMAX + n, mx);
 }
 
 // Activation preparation for the f16 (shared-expert) path: x16 = f16(x * 2^-p),
@@ -597,6 +600,115 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
 }
 
+// ---------------------------------------------------------------------------
+// blocks of more than 32 rows (prefill), caller logits: three launches
+// ---------------------------------------------------------------------------
+
+// per row (one warp each): the top-k and its weights, and the row's bit in the
+// bitmap of every expert it selected (its 32-row group); the other CTAs split the
+// rows into E4M3 terms for the expert kernel
+__global__ void __launch_bounds__(RT_THREADS) route_rows_kernel(const RouteParams p, int n_topk_ctas) {
+    __shared__ uint32_t sel[RT_THREADS / 32][64];
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (b < n_topk_ctas) {
+        const int n = b * (RT_THREADS / 32) + warp;
+        if (n >= p.N) return;
+        topk_row(p, p.logits_in + (size_t)n * p.E, n, false, sel[warp]);
+        __syncwarp();
+        if (lane < p.k) {
+            const int e = __ldcg(p.topk_idx + (size_t)n * p.k + lane);
+            if (e >= 0 && e < p.E) atomicOr(p.rbits + (size_t)(n >> 5) * p.E + e, 1u << (n & 31));
+        }
+        return;
+    }
+    if (p.x == nullptr) return;
+    const int nc = (p.d + RT_CHUNK - 1) / RT_CHUNK;
+    const int i = b - n_topk_ctas, n = i / nc, c = i - n * nc;
+    if (n < p.N) prep_chunk_mx(p, n, c);
+}
+
+// one CTA, a thread per expert: the selected experts (ascending), each one's first
+// pair, and per 32-row group the offset of the group's first pair of the expert;
+// the bitmaps are moved to their copy and cleared for the next call
+__global__ void __launch_bounds__(1024) route_count_kernel(const RouteParams p) {
+    __shared__ int s_warp_cnt[32], s_warp_use[32];
+    const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
+    const int G = (p.N + 31) / 32;
+    int cnt = 0;
+    if (e < p.E)
+        for (int g = 0; g < G; g++) cnt += __popc(__ldcg(p.rbits + (size_t)g * p.E + e));
+    const int use = cnt > 0 ? 1 : 0;
+    // exclusive scans of the counts and of the "selected" flags over the experts
+    int ic = cnt, iu = use;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, ic, o), bu = __shfl_up_sync(0xffffffffu, iu, o);
+        if (lane >= o) {
+            ic += a;
+            iu += bu;
+        }
+    }
+    if (lane == 31) {
+        s_warp_cnt[warp] = ic;
+        s_warp_use[warp] = iu;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int wc = s_warp_cnt[lane], wu = s_warp_use[lane];
+        for (int o = 1; o < 32; o <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, wc, o), bu = __shfl_up_sync(0xffffffffu, wu, o);
+            if (lane >= o) {
+                wc += a;
+                wu += bu;
+            }
+        }
+        s_warp_cnt[lane] = wc;
+        s_warp_use[lane] = wu;
+    }
+    __syncthreads();
+    const int before_c = (warp ? s_warp_cnt[warp - 1] : 0) + ic - cnt;
+    const int before_u = (warp ? s_warp_use[warp - 1] : 0) + iu - use;
+    if (e < p.E) {
+        if (use) {
+            p.uexp[before_u] = e;
+            p.off[before_u] = before_c;
+        }
+        int run = before_c;
+        for (int g = 0; g < G; g++) {
+            const size_t at = (size_t)g * p.E + e;
+            const uint32_t bits = __ldcg(p.rbits + at);
+            p.rbase[at] = run;
+            p.rbits2[at] = bits;
+            p.rbits[at] = 0u;
+            run += __popc(bits);
+        }
+    }
+    if (e == (int)blockDim.x - 1) {
+        const int U = s_warp_use[31], NK = s_warp_cnt[31];
+        p.off[U] = NK;
+        p.ctrl[CTRL_UNIQUE] = (uint32_t)U;
+        p.ctrl[CTRL_ROWS] = (uint32_t)p.N;
+        p.ctrl[CTRL_WORK] = 0;
+        p.ctrl[CTRL_EXIT] = 0;
+        p.ctrl[CTRL_WORK_TC] = 0;
+        p.ctrl[CTRL_EXIT_TC] = 0;
+    }
+    for (int i = e; i < p.v_cap; i += blockDim.x) p.gu_done[i] = 0;
+    for (int64_t i = e; i < p.pairs_cap; i += blockDim.x) p.hmax[i] = 0;
+    if (e < RT_MAX_ROWS) p.ctrl[CTRL_XMAX + e] = 0;  // the row maxima of rows < 32 published by the prep
+}
+
+// every (row, slot) pair at its place: the expert's pairs ordered by row
+__global__ void __launch_bounds__(256) route_scatter_kernel(const RouteParams p) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.N * p.k) return;
+    const int n = i / p.k;
+    const int e = __ldcg(p.topk_idx + i);
+    if (e < 0 || e >= p.E) return;
+    const size_t at = (size_t)(n >> 5) * p.E + e;
+    const int rank = __ldcg(p.rbase + at) + __popc(__ldcg(p.rbits2 + at) & ((1u << (n & 31)) - 1u));
+    p.pair[rank] = i;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -609,8 +721,9 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 ||
         k > 32 || k > E)
         return MOE_ERR_UNSUPPORTED;
-    if (n_rows < 1 || n_rows > n_rows_max || n_rows > RT_MAX_ROWS || n_shared < 0) return MOE_ERR_UNSUPPORTED;
+    if (n_rows < 1 || n_rows > n_rows_max || n_shared < 0) return MOE_ERR_UNSUPPORTED;
     if (!logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
+    if (n_rows > RT_MAX_ROWS && !logits_in) return MOE_ERR_UNSUPPORTED;  // the router GEMV serves <= 32 rows
     if (((uintptr_t)ws & 255) || (x && ((uintptr_t)x & 15)) || (w_router && ((uintptr_t)w_router & 15)))
         return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
@@ -639,8 +752,23 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     p.x_mx = reinterpret_cast<uint8_t*>(base + L.x_mx);
     p.x_sc = reinterpret_cast<uint8_t*>(base + L.x_sc);
     p.gu_done_tc = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
+    p.rbits = reinterpret_cast<uint32_t*>(base + L.rbits);
+    p.rbits2 = reinterpret_cast<uint32_t*>(base + L.rbits2);
+    p.rbase = reinterpret_cast<int*>(base + L.rbase);
     p.v_cap = n_shared + (n_rows_max * k < E ? n_rows_max * k : E);
     p.pairs_cap = L.pairs;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (n_rows > RT_MAX_ROWS) {
+        // prefill: top-k and bitmaps per row (+ activation terms), counts and offsets,
+        // then every pair at its place
+        p.n_ks = p.n_eg = p.n_gemv_ctas = 0;
+        const int topk_ctas = (n_rows + RT_THREADS / 32 - 1) / (RT_THREADS / 32);
+        const int prep = x ? n_rows * ((d + RT_CHUNK - 1) / RT_CHUNK) : 0;
+        route_rows_kernel<<<topk_ctas + prep, RT_THREADS, 0, cs>>>(p, topk_ctas);
+        route_count_kernel<<<1, 1024, 0, cs>>>(p);
+        route_scatter_kernel<<<(n_rows * k + 255) / 256, 256, 0, cs>>>(p);
+        return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     const int KS = d < RT_KS ? d : RT_KS;
     p.n_ks = d / KS;
     p.n_eg = (E + RT_EG - 1) / RT_EG;
@@ -656,6 +784,6 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
         if (kernel_smem_attrs(route_kernel, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
         attr_set = true;
     }
-    route_kernel<<<grid, RT_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(p);
+    route_kernel<<<grid, RT_THREADS, smem, cs>>>(p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
