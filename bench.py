@@ -537,6 +537,61 @@ def run_cache_bench(args):
             "policies": out, "setup_s": round(setup_s, 1), "data": "synthetic"}
 
 
+def run_prefill_bench(args):
+    """Prefill blocks of 270 and 1,533 rows through the layer (routed experts on the
+    block-scaled tcgen05 path), all 896 experts resident, independent N(0,1) router
+    logits per row, L2 flushed before every block outside the events."""
+    import torch
+
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+
+    build_mod.build()
+    sh = syn.KIMI
+    E, k, d = sh.n_experts, sh.top_k, sh.d_model
+    sizes = [int(v) for v in args.prefill_rows.split(",")]
+    nmax = max(sizes)
+    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=nmax, n_shared=0)
+    lay.alloc_pool(E)
+    threads = max(2, min(16, os.cpu_count() or 2))
+    for e, slab in syn.mxfp4_slabs_parallel(SEED, range(E), sh, threads=threads):
+        lay.put_slab(e, slab)
+    lay.set_expert_slots(np.arange(E, dtype=np.int32))
+    flush = L2Flush(torch, torch.device("cuda"))
+    peak, peak_kind = load_peaks()
+    res = {}
+    for n in sizes:
+        rng = np.random.default_rng(SEED + n)
+        x = torch.from_numpy(syn.x_rows(SEED, range(n), d).view(np.int16)).cuda().view(torch.uint16)
+        ts, us = [], []
+        for rep in range(args.prefill_warmup + args.prefill_steps):
+            lg = torch.from_numpy(rng.normal(size=(n, E)).astype(np.float32)).cuda()
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            lay.forward(x, x, logits_in=lg, mode=B.MOE_MODE_PREFILL)
+            b.record()
+            torch.cuda.synchronize()
+            if rep >= args.prefill_warmup:
+                ts.append(a.elapsed_time(b) * 1e-3)
+                us.append(int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item()))
+        assert lay.error_bits() == 0
+        t = statistics.median(ts)
+        u = statistics.mean(us)
+        gbs = u * SLAB / t / 1e9
+        res[str(n)] = {"ms_median": round(t * 1e3, 3), "unique_experts": u, "gbs_unique": round(gbs, 1),
+                       "frac_of_hbm_peak": round(gbs / peak, 4),
+                       "tflops": round(2 * 3 * n * k * d * sh.d_ff / t / 1e12, 1)}
+    return {"metric": "prefill layer ms and GB/s on unique MXFP4 expert bytes (routed experts)",
+            "unit": "GB/s", "value": res[str(nmax)]["gbs_unique"], "n_gpus": 1,
+            "config": {"workload": "Kimi K3.1 MoE layer prefill, routed experts only (no shared experts), "
+                                   "all 896 experts resident, independent N(0,1) logits per row",
+                       "rows": sizes, "steps": args.prefill_steps,
+                       "l2": "flushed before every block, outside the events"},
+            "peak_gbs": peak, "peak_kind": peak_kind, "blocks": res, "data": "synthetic"}
+
+
 def run_reference(args):
     """The CPU oracle timed on this host's cores: each step is the oracle's expert MLP
     of one (row, selected expert) pair of the workload (17,547,264 expert bytes)."""
@@ -574,7 +629,16 @@ def main():
     ap.add_argument("--cache-slots", type=int, default=1567)
     ap.add_argument("--cache-blocks", type=int, default=4)
     ap.add_argument("--cache-warmup", type=int, default=2)
+    ap.add_argument("--prefill-bench", action="store_true",
+                    help="prefill blocks through the layer (one JSON line) and exit")
+    ap.add_argument("--prefill-rows", default="270,1533")
+    ap.add_argument("--prefill-steps", type=int, default=5)
+    ap.add_argument("--prefill-warmup", type=int, default=2)
     args = ap.parse_args()
+
+    if args.prefill_bench:
+        print(json.dumps(run_prefill_bench(args)))
+        return
 
     if args.cache_bench:
         print(json.dumps(run_cache_bench(args)))
