@@ -340,12 +340,13 @@ def run_ours(args, rank, world):
                      "kernel": "moe::tc::tc_expert_kernel", "peak_kind": peak_kind,
                      "bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_s * 1e6},
         "segments_us_median": ({name: statistics.median(s_[i] for s_ in seg_ms) * 1e3
-                                for i, name in enumerate(("route", "wait_for_shared_experts", "routed_experts", "combine"))}
+                                for i, name in enumerate(("route", "shared_experts_past_route", "routed_experts", "combine"))}
                                if seg_ms else None),
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
                 "d2h_bytes_per_step": syn.KIMI.d_model * 2},
-        "gpu_launches": K * 3,
-        "timing": "one CUDA graph per step (route, experts, combine), events inside the graph"
+        "gpu_launches": K * 4,
+        "timing": "one CUDA graph per step: route, shared experts, routed experts, combine chained on one "
+                  "stream; timing events at its start and end and, for the segments, on a side branch"
                   if gev is not None else "one CUDA graph per step, events around the replay",
         "clocks": clocks,
         "wall_s_timed_region": wall,

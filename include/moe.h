@@ -32,6 +32,12 @@
  *   the kernel records a bit in the workspace's error word and finishes.  Read
  *   and clear it with moe_get_error().
  * - bf16 and fp16 values are passed as their 16-bit patterns (uint16_t).
+ * - moe_expert_block, moe_shared_experts and moe_combine launch with
+ *   programmatic dependent launch: their kernels may be scheduled while the
+ *   previous kernel on the stream is still running, and wait for it to
+ *   complete before they touch memory, so stream order holds as for plain
+ *   launches; only the launch and the kernels' set-up overlap.  moe_route
+ *   launches plainly and lets the next kernel be scheduled at once.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
@@ -224,6 +230,19 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
  *  moe_expert_block writes there.  Errors as moe_expert_block.
  */
 MOE_API int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x,
+                       const moe_pool* shared, int32_t n_shared,
+                       void* ws, int32_t n_rows_max, void* stream);
+
+/*
+ * moe_shared_experts for the launch that directly follows moe_route of the same
+ * block on the same stream: its kernel starts while the routing runs (x must be
+ * complete before moe_route is enqueued, as moe_route itself needs it) and
+ * completes only after the routing has completed, so the next call on the
+ * stream (moe_expert_block with MOE_MODE_ROUTED_ONLY, then moe_combine) sees
+ * both.  One stream, no events: route -> shared experts -> routed experts ->
+ * combine.  Arguments, output and errors as moe_shared_experts.
+ */
+MOE_API int moe_shared_experts_after_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x,
                        const moe_pool* shared, int32_t n_shared,
                        void* ws, int32_t n_rows_max, void* stream);
 

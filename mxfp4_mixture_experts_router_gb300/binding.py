@@ -42,7 +42,7 @@ MOE_CACHE_KEEP_MULTI_ROW = 1
 EXPORTED = [
     "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
-    "q8_0_block_matmul_noalloc", "moe_shared_experts",
+    "q8_0_block_matmul_noalloc", "moe_shared_experts", "moe_shared_experts_after_route",
     "moe_cache_create", "moe_cache_request", "moe_cache_stats_get", "moe_cache_sync", "moe_cache_destroy",
 ]
 
@@ -96,6 +96,7 @@ def lib() -> ctypes.CDLL:
         L.moe_route.argtypes = [D, I32, P, P, P, P, P, P, P, I32, I32, P]
         L.moe_expert_block.argtypes = [D, I32, I32, PL, P, P, PL, I32, P, I32, P, P]
         L.moe_shared_experts.argtypes = [D, I32, P, PL, I32, P, I32, P]
+        L.moe_shared_experts_after_route.argtypes = [D, I32, P, PL, I32, P, I32, P]
         L.moe_cache_create.argtypes = [D, P, ctypes.c_int64, I32, P, I32, I32, ctypes.POINTER(P)]
         L.moe_cache_request.argtypes = [P, I32, I32, P, P, P, P, P, P]
         L.moe_cache_stats_get.argtypes = [P, ctypes.POINTER(MoeCacheStats)]
@@ -168,6 +169,13 @@ def moe_shared_experts(d: MoeDesc, n_rows: int, x, shared: MoePool, n_shared: in
                        stream=None):
     _check(lib().moe_shared_experts(ctypes.byref(d), n_rows, _ptr(x), ctypes.byref(shared), n_shared, _ptr(ws),
                                     n_rows_max, _stream(stream)), "moe_shared_experts")
+
+
+def moe_shared_experts_after_route(d: MoeDesc, n_rows: int, x, shared: MoePool, n_shared: int, ws,
+                                   n_rows_max: int, stream=None):
+    _check(lib().moe_shared_experts_after_route(ctypes.byref(d), n_rows, _ptr(x), ctypes.byref(shared), n_shared,
+                                                _ptr(ws), n_rows_max, _stream(stream)),
+           "moe_shared_experts_after_route")
 
 
 def moe_expert_block(d: MoeDesc, n_rows: int, mode: int, routed: MoePool, expert_slot, slot_ready,

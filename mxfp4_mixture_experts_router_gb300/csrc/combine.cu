@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(int d, int k, int n
                                                              const float* __restrict__ topk_w,
                                                              const float* __restrict__ shared_y,
                                                              uint16_t* __restrict__ out) {
+    griddep_wait();  // launched while the expert kernels finish
     const int n = blockIdx.y;
     const int c = (blockIdx.x * CB_THREADS + threadIdx.x) * 4;
     if (c >= d) return;
@@ -78,11 +79,12 @@ extern "C" int moe_combine(const moe_desc* desc, int32_t n_rows, const uint16_t*
         return MOE_ERR_INVALID_ARG;
     dim3 grid((d / 4 + CB_THREADS - 1) / CB_THREADS, n_rows);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (k <= 16)
-        combine_kernel<16><<<grid, CB_THREADS, 0, s>>>(d, k, n_shared, n_rows, residual, y_part, topk_w, shared_y, out);
-    else
-        combine_kernel<32><<<grid, CB_THREADS, 0, s>>>(d, k, n_shared, n_rows, residual, y_part, topk_w, shared_y, out);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    const cudaError_t e =
+        k <= 16 ? launch_chained(combine_kernel<16>, grid, dim3(CB_THREADS), 0, s, d, k, n_shared, (int)n_rows, residual,
+                                 y_part, topk_w, shared_y, out)
+                : launch_chained(combine_kernel<32>, grid, dim3(CB_THREADS), 0, s, d, k, n_shared, (int)n_rows, residual,
+                                 y_part, topk_w, shared_y, out);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 extern "C" size_t moe_workspace_size(const moe_desc* desc, int32_t n_rows_max, int32_t n_shared) {

@@ -48,7 +48,9 @@ enum { J_LAYER = 0, J_Q8_SWIGLU = 1, J_Q8_PLAIN = 2 };
 
 struct Geom {
     int row_bytes, bi, cb, nbox, sb, flat, chunks, gps, rows_item;
-    int fast;  // full-width swizzled stages: the unrolled per-warp tile paths apply
+    int fast;    // full-width swizzled stages: the unrolled per-warp tile paths apply
+    int merged;  // the maps were built by pool_maps for such stages: a stage is one TMA
+                 // box of codes (gate and up together) plus one of scales
     uint32_t tx;
 };
 
@@ -62,6 +64,10 @@ struct ExParams {
     int debug_gu, accum;
     int routed_off;  // layer job without the routed experts (they run on the block-scaled path)
     int work_word, exit_word;  // ctrl words of this launch's work counter and exit counter
+    // shared-expert launch: the block's bf16 rows, turned into the f16 copy (x16, xexp)
+    // by the first CTAs to start; null when x16 was written by an earlier kernel
+    const uint16_t* x_rows;
+    int dep_at_end;  // wait for the previous kernel on the stream at the end, not the start
     const int* expert_slot;
     const uint32_t* slot_ready;
     int n_slots;
@@ -195,7 +201,7 @@ __device__ __forceinline__ void gu_stage(uint32_t st, const Geom& g, int chunk, 
 #pragma unroll
         for (int nt = 0; nt < EX_NT; nt++) {
             bx[nt] = make_uint4(0, 0, 0, 0);
-            if (nt < NT && bval[nt]) bx[nt] = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + kk));
+            if (nt < NT && bval[nt]) bx[nt] = __ldca(reinterpret_cast<const uint4*>(xrow[nt] + kk));
         }
         uint32_t g0[4], g1[4], u0[4], u1[4];
         load_a<FMT>(gateC, g, 16, gq, gq + 8, q, i, g0, g1);
@@ -363,7 +369,7 @@ __device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunk
         for (int nt = 0; nt < NT; nt++) {
             bx[nt] = make_uint4(0, 0, 0, 0);
             if (bval[nt])
-                bx[nt] = __ldg(reinterpret_cast<const uint4*>(xrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i));
+                bx[nt] = __ldca(reinterpret_cast<const uint4*>(xrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i));
         }
         uint32_t g0[4], g1[4], u0[4], u1[4];
         load_a_fast<FMT>(st + aoff[t], g0, g1);
@@ -454,6 +460,86 @@ __device__ __forceinline__ int pair_row(const ExParams& p, const ItemCtx& c, int
     return c.shared ? col : __ldg(p.pair + c.u_off + col) / p.top_k;
 }
 
+// f16 copy of one bf16 row scaled by 2^-p, p from the row's largest magnitude (the
+// routing kernel's rule), by the EX_CT consumer threads: the row is held in
+// registers between its max and its conversion (16-byte loads, all issued first).
+constexpr int F16_ROW_PER = 4;  // 16-byte chunks per thread: rows of up to 8192 elements
+__device__ void row_to_f16(int d, const uint16_t* __restrict__ x, __half* x16, int* xexp, uint32_t* s_max) {
+    const int tid = threadIdx.x, nv = d / 8;
+    const uint4* xv = reinterpret_cast<const uint4*>(x);
+    uint4 v[F16_ROW_PER];
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const int c = j * EX_CT + tid;
+        v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) mx = max(mx, max((w[t] & 0x7FFFu) << 16, w[t] & 0x7FFF0000u));
+    }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if ((tid & 31) == 0) s_max[tid >> 5] = mx;
+    consumer_sync<EX_CT>();
+    uint32_t m = 0;
+#pragma unroll
+    for (int w = 0; w < EX_CW; w++) m = max(m, s_max[w]);
+    consumer_sync<EX_CT>();  // s_max is reused by the next row
+    const int pe = f16_scale_exponent(m);
+    const float sc = exp2i(-pe);
+    uint4* ov = reinterpret_cast<uint4*>(x16);
+#pragma unroll
+    for (int j = 0; j < F16_ROW_PER; j++) {
+        const int c = j * EX_CT + tid;
+        if (c >= nv) continue;
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * sc, __uint_as_float(w[t] & 0xFFFF0000u) * sc);
+            o[t] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        ov[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid == 0) *xexp = pe;
+}
+
+// The shared-expert launch makes its own f16 copy of the block's rows: each CTA
+// claims rows until none is left, then every CTA waits (bounded) until all rows
+// are written.  Rows are claimed only by running CTAs, so the wait always ends.
+__device__ void prepare_rows(const ExParams& p) {
+    __shared__ uint32_t s_max[EX_CW];
+    __shared__ int s_row;
+    const int tid = threadIdx.x;
+    __half* x16 = const_cast<__half*>(p.x16);
+    int* xexp = const_cast<int*>(p.xexp);
+    while (true) {
+        if (tid == 0) s_row = (int)atomicAdd(p.ctrl + CTRL_PREP_SH, 1u);
+        consumer_sync<EX_CT>();
+        const int n = s_row;
+        consumer_sync<EX_CT>();
+        if (n >= p.n_rows) break;
+        row_to_f16(p.k_gu, p.x_rows + (size_t)n * p.k_gu, x16 + (size_t)n * p.k_gu, xexp + n, s_max);
+        __threadfence();
+        consumer_sync<EX_CT>();
+        if (tid == 0) red_release_add(p.ctrl + CTRL_PREPD_SH, 1u);
+    }
+    if (tid == 0 && ld_acquire(p.ctrl + CTRL_PREPD_SH) < (uint32_t)p.n_rows) {
+        const uint64_t t0 = global_ns();
+        while (ld_acquire(p.ctrl + CTRL_PREPD_SH) < (uint32_t)p.n_rows) {
+            if (timed_out(p.ctrl)) break;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    consumer_sync<EX_CT>();  // the copy is read with coherent (L1-cached, not .nc) loads
+}
+
 // ---------------------------------------------------------------------------
 
 __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t* full, uint64_t* empty,
@@ -513,7 +599,17 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
             mt.slot = z;
             mbar_arrive_expect_tx(&full[stage], G.tx);
             unsigned char* st = ring + (size_t)stage * EX_STAGE;
-            if (type == IT_GU) {
+            if (G.merged) {
+                // 16 KB of codes in one box ([matrix][K chunk][row][128 B], the layout
+                // of the per-chunk boxes), the stage's scales in a second one
+                if (type == IT_GU) {
+                    tma_load_5d(st, mp, &full[stage], 0, row0, c * G.nbox, 0, z);
+                    tma_load_4d(st + EX_CODE_BYTES, mp + 1, &full[stage], c * G.sb, row0, 0, z);
+                } else {
+                    tma_load_4d(st, mp + 4, &full[stage], 0, row0, c * G.nbox, z);
+                    tma_load_3d(st + EX_CODE_BYTES, mp + 5, &full[stage], c * G.sb, row0, z);
+                }
+            } else if (type == IT_GU) {
                 for (int m = 0; m < 2; m++) {
                     for (int b = 0; b < G.nbox; b++)
                         tma_load_3d(st + m * G.nbox * G.bi * 16 + b * G.bi * 16, mp + 2 * m, &full[stage],
@@ -714,7 +810,7 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
                 uint32_t amax = 0;
                 if (col < c.r) {
                     const int row = pair_row(p, c, col);
-                    const float sc = exp2i(__ldg(p.xexp + row));
+                    const float sc = exp2i(__ldca(p.xexp + row));
                     gs *= sc;
                     us *= sc;
                     const float hv = gs / (1.f + expf(-gs)) * us;
@@ -788,6 +884,11 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         mbar_fence_init();
     }
     __syncthreads();
+    // launched after the previous kernel on the stream: wait for it here, unless this
+    // launch reads nothing that kernel writes (the shared experts beside the routing),
+    // in which case it waits before it completes
+    if (!p.dep_at_end) griddep_wait();
+    griddep_launch_dependents();
     const int S = p.n_shared;
     const int U = (p.job == J_LAYER && !p.routed_off) ? (int)p.ctrl[CTRL_UNIQUE] : 0;
     const int V = S + U;
@@ -796,6 +897,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         if (tid == EX_CT) producer(p, V, ring, full, empty, meta);
         return;
     }
+    if (p.x_rows != nullptr) prepare_rows(p);
     consumer<FR, FS, FAST>(p, V, ring, red, full, empty, meta);
 
     // the last CTA to finish leaves the workspace clean for the next call
@@ -812,8 +914,13 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         if (tid == 0) {
             p.ctrl[p.work_word] = 0;
             p.ctrl[p.exit_word] = 0;
+            if (p.x_rows != nullptr) {
+                p.ctrl[CTRL_PREP_SH] = 0;
+                p.ctrl[CTRL_PREPD_SH] = 0;
+            }
         }
     }
+    if (p.dep_at_end && tid == 0) griddep_wait();  // complete only after the previous kernel
 }
 
 // ---------------------------------------------------------------------------
@@ -856,6 +963,7 @@ static bool make_geom(Geom& g, int fmt, bool gu, int K, int rows_total) {
     if (rows_total % g.rows_item) return false;
     g.tx = (uint32_t)((gu ? 2 : 1) * (g.nbox * g.bi * g.rows_item + g.rows_item * g.sb));
     g.fast = (g.bi == 128 && g.cb == cap) ? 1 : 0;
+    g.merged = 0;  // set by pool_maps with the maps it builds for fast stages
     return true;
 }
 
@@ -893,6 +1001,23 @@ static bool make_maps(CUtensorMap* cm, CUtensorMap* sm, const Geom& g, int fmt, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// tiled uint8 map of rank 3 to 5: dims[0] contiguous, byte strides of dims 1..rank-1
+static bool map_u8(CUtensorMap* m, const void* addr, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, bool swizzle) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc || rank < 3 || rank > 5 || ((uintptr_t)addr & 15)) return false;
+    cuuint64_t gd[5], gs[4];
+    cuuint32_t bx[5], es[5] = {1, 1, 1, 1, 1};
+    for (int i = 0; i < rank; i++) {
+        gd[i] = dims[i];
+        bx[i] = box[i];
+    }
+    for (int i = 0; i + 1 < rank; i++) gs[i] = strides[i];
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(addr), gd, gs, bx, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // all six maps of a slab pool (gate, up, down)
 static bool pool_maps(CUtensorMap* maps, Geom* gg /*[2]: gate/up, down*/, const moe_pool* pool, int d, int f) {
     const int fmt = pool->format;
@@ -902,6 +1027,45 @@ static bool pool_maps(CUtensorMap* maps, Geom* gg /*[2]: gate/up, down*/, const 
     const int64_t codes_gu = fmt == MOE_FMT_MXFP4 ? (int64_t)f * d / 2 : (int64_t)f * d;
     const int64_t scales_gu = (int64_t)f * (d / 32) * cpb;
     const int64_t per = codes_gu + scales_gu;
+    if (gg[0].fast != gg[1].fast) gg[0].fast = gg[1].fast = 0;
+    if (gg[0].fast) {
+        // one box per stage and operand: gate and up codes [slot][matrix][row][K/128][128],
+        // their scales [slot][matrix][row][K/32 groups], down codes [slot][row][K/128][128]
+        const uint64_t sl = (uint64_t)pool->slot_bytes, ns = (uint64_t)pool->n_slots;
+        const Geom& a = gg[0];
+        const Geom& b = gg[1];
+        const uint64_t rsb_gu = (uint64_t)cpb * (d / 32), rsb_dn = (uint64_t)cpb * (f / 32);
+        {
+            const uint64_t dims[5] = {128, (uint64_t)f, (uint64_t)a.row_bytes / 128, 2, ns};
+            const uint64_t str[4] = {(uint64_t)a.row_bytes, 128, (uint64_t)per, sl};
+            const uint32_t box[5] = {128, (uint32_t)a.rows_item, (uint32_t)a.nbox, 2, 1};
+            if (!map_u8(&maps[0], base, 5, dims, str, box, true)) return false;
+        }
+        {
+            const uint64_t dims[4] = {rsb_gu, (uint64_t)f, 2, ns};
+            const uint64_t str[3] = {rsb_gu, (uint64_t)per, sl};
+            const uint32_t box[4] = {(uint32_t)a.sb, (uint32_t)a.rows_item, 2, 1};
+            if (!map_u8(&maps[1], base + codes_gu, 4, dims, str, box, false)) return false;
+        }
+        maps[2] = maps[0];
+        maps[3] = maps[1];
+        {
+            const uint64_t dims[4] = {128, (uint64_t)d, (uint64_t)b.row_bytes / 128, ns};
+            const uint64_t str[3] = {(uint64_t)b.row_bytes, 128, sl};
+            const uint32_t box[4] = {128, (uint32_t)b.rows_item, (uint32_t)b.nbox, 1};
+            if (!map_u8(&maps[4], base + 2 * per, 4, dims, str, box, true)) return false;
+        }
+        {
+            const uint64_t dims[3] = {rsb_dn, (uint64_t)d, ns};
+            const uint64_t str[2] = {rsb_dn, sl};
+            const uint32_t box[3] = {(uint32_t)b.sb, (uint32_t)b.rows_item, 1};
+            if (!map_u8(&maps[5], base + 2 * per + (fmt == MOE_FMT_MXFP4 ? (int64_t)d * f / 2 : (int64_t)d * f),
+                        3, dims, str, box, false))
+                return false;
+        }
+        gg[0].merged = gg[1].merged = 1;
+        return true;
+    }
     if (!make_maps(&maps[0], &maps[1], gg[0], fmt, base, base + codes_gu, f, d, pool->n_slots, pool->slot_bytes))
         return false;
     if (!make_maps(&maps[2], &maps[3], gg[0], fmt, base + per, base + per + codes_gu, f, d, pool->n_slots,
@@ -931,8 +1095,9 @@ static int launch_variant(const ExParams& p, cudaStream_t stream) {
     }
     const int grid = sm_count() * EX_CTAS_PER_SM;
     if (grid <= 0) return MOE_ERR_CUDA;
-    expert_kernel<FR, FS, FAST><<<grid, EX_THREADS, EX_SMEM, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (launch_chained(expert_kernel<FR, FS, FAST>, dim3(grid), dim3(EX_THREADS), EX_SMEM, stream, p) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 // The unrolled fast paths serve every matrix of the job when all their stages
@@ -1048,55 +1213,8 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
 }
 
-// f16 copy of bf16 rows scaled by 2^-p, p from each row's largest magnitude (the
-// same rule as the routing kernel's copy): one CTA per row, the row held in
-// registers between its max and its conversion (16-byte loads, all issued first).
-constexpr int F16_ROW_PER = 4;  // 16-byte chunks per thread: rows of up to 8192 elements at 256 threads
-__global__ void __launch_bounds__(256) rows_to_f16_kernel(int d, const uint16_t* __restrict__ x, __half* x16,
-                                                          int* xexp) {
-    const int n = blockIdx.x, tid = threadIdx.x, nv = d / 8;
-    const uint4* xv = reinterpret_cast<const uint4*>(x + (size_t)n * d);
-    uint4 v[F16_ROW_PER];
-#pragma unroll
-    for (int j = 0; j < F16_ROW_PER; j++) {
-        const int c = j * 256 + tid;
-        v[j] = c < nv ? __ldg(xv + c) : make_uint4(0, 0, 0, 0);
-    }
-    uint32_t mx = 0;
-#pragma unroll
-    for (int j = 0; j < F16_ROW_PER; j++) {
-        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-        for (int t = 0; t < 4; t++) mx = max(mx, max((w[t] & 0x7FFFu) << 16, w[t] & 0x7FFF0000u));
-    }
-    mx = __reduce_max_sync(0xffffffffu, mx);
-    __shared__ uint32_t s_max[8];
-    if ((tid & 31) == 0) s_max[tid >> 5] = mx;
-    __syncthreads();
-    uint32_t m = 0;
-#pragma unroll
-    for (int w = 0; w < 8; w++) m = max(m, s_max[w]);
-    const int p = f16_scale_exponent(m);
-    const float sc = exp2i(-p);
-    uint4* ov = reinterpret_cast<uint4*>(x16 + (size_t)n * d);
-#pragma unroll
-    for (int j = 0; j < F16_ROW_PER; j++) {
-        const int c = j * 256 + tid;
-        if (c >= nv) continue;
-        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        uint32_t o[4];
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            const __half2 h = __floats2half2_rn(__uint_as_float(w[t] << 16) * sc, __uint_as_float(w[t] & 0xFFFF0000u) * sc);
-            o[t] = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        ov[c] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-    if (tid == 0) xexp[n] = p;
-}
-
-extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const moe_pool* shared,
-                                  int32_t n_shared, void* ws, int32_t n_rows_max, void* stream) {
+static int shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const moe_pool* shared,
+                          int32_t n_shared, void* ws, int32_t n_rows_max, bool after_route, void* stream) {
     if (!desc || !ws || !x || !shared) return MOE_ERR_INVALID_ARG;
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
     if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
@@ -1105,7 +1223,7 @@ extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const ui
     if (n_shared < 1 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
     if (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared) return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)ws & 255) || ((uintptr_t)x & 15)) return MOE_ERR_INVALID_ARG;
-    if (d > F16_ROW_PER * 256 * 8) return MOE_ERR_UNSUPPORTED;
+    if (d > F16_ROW_PER * EX_CT * 8) return MOE_ERR_UNSUPPORTED;
 
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
@@ -1140,11 +1258,20 @@ extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const ui
     p.pairs_cap = (int64_t)n_shared * n_rows_max;
     p.work_word = CTRL_WORK_SH;
     p.exit_word = CTRL_EXIT_SH;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rows_to_f16_kernel<<<n_rows, 256, 0, s>>>(d, x, reinterpret_cast<__half*>(base + L.x16s),
-                                              reinterpret_cast<int*>(base + L.xexps));
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-    return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, s);
+    p.x_rows = x;
+    p.dep_at_end = after_route ? 1 : 0;
+    return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int moe_shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const moe_pool* shared,
+                                  int32_t n_shared, void* ws, int32_t n_rows_max, void* stream) {
+    return shared_experts(desc, n_rows, x, shared, n_shared, ws, n_rows_max, false, stream);
+}
+
+extern "C" int moe_shared_experts_after_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x,
+                                              const moe_pool* shared, int32_t n_shared, void* ws, int32_t n_rows_max,
+                                              void* stream) {
+    return shared_experts(desc, n_rows, x, shared, n_shared, ws, n_rows_max, true, stream);
 }
 
 // ---------------------------------------------------------------------------

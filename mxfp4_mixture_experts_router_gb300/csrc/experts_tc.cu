@@ -169,24 +169,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
-                                            int w) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
-                                            int c3, int c4) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
-        : "memory");
-}
-
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ int round16(int v) { return (v + 15) & ~15; }
@@ -756,7 +738,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int U = min((int)p.ctrl[CTRL_UNIQUE], C::MAX_U);
     if (tid == 0) {
         for (int s = 0; s < C::NST; s++) {
             mbar_init(&full[s], 1);
@@ -778,6 +759,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
                      "r"(C::TM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // the set-up above overlaps the previous kernel on the stream; everything below
+    // reads the routing's results
+    griddep_wait();
+    griddep_launch_dependents();
+    const int U = min((int)p.ctrl[CTRL_UNIQUE], C::MAX_U);
     // every expert's slot and pair range (all loads in flight at once), then the
     // prefix of its chunk counts (one warp: contiguous runs per lane, then a scan)
     for (int u = tid; u < U; u += NTHREADS) {
@@ -893,8 +879,9 @@ static int launch(const Params& p, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return MOE_ERR_CUDA;
-    tc_expert_kernel<NBM><<<sms, NTHREADS, C::SMEM, stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (launch_chained(tc_expert_kernel<NBM>, dim3(sms), dim3(NTHREADS), C::SMEM, stream, p) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
 }
 
 }  // namespace tc

@@ -509,6 +509,8 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     __shared__ int s_flag;
     const int tid = threadIdx.x;
     const int b = blockIdx.x;
+    // the shared experts of the block may start beside the routing (they need x only)
+    griddep_launch_dependents();
 
     if (p.x != nullptr && p.n_gemv_ctas == 0) {  // caller logits: one CTA per (row, chunk)
         const int nc = (p.d + RT_CHUNK - 1) / RT_CHUNK;

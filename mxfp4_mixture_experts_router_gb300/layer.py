@@ -105,10 +105,11 @@ class MoeLayer:
                            self.shared_pool_desc(), self.n_shared, self.ws, self.n_rows_max, self.y_part,
                            stream)
 
-    def shared_experts(self, n_rows: int, x, stream=None):
-        """The shared experts from x alone (independent of routing)."""
-        B.moe_shared_experts(self.desc, n_rows, x, self.shared_pool_desc(), self.n_shared, self.ws,
-                             self.n_rows_max, stream)
+    def shared_experts(self, n_rows: int, x, after_route: bool = False, stream=None):
+        """The shared experts from x alone (independent of routing); after_route: the
+        launch directly follows route() on the same stream and runs beside it."""
+        fn = B.moe_shared_experts_after_route if after_route else B.moe_shared_experts
+        fn(self.desc, n_rows, x, self.shared_pool_desc(), self.n_shared, self.ws, self.n_rows_max, stream)
 
     def combine(self, n_rows: int, residual, stream=None):
         shared_y = self.ws.data_ptr() + self.offsets.shared_y if self.n_shared else None
@@ -119,8 +120,9 @@ class MoeLayer:
                 stream=None):
         """Run one block: x, residual bf16 bits [N][d] on the device; returns out bits [N][d].
 
-        The shared experts run on a side stream while the block is routed (they need
-        x only); the routed experts follow the routing, and the combine waits for both."""
+        One stream: the routing, the shared experts (their kernel starts beside the
+        routing: they need x only), the routed experts, the combine; each launch after
+        the routing overlaps the tail of the one before it."""
         n = x.shape[0] if n_rows is None else n_rows
         self._block(n, x, residual, logits_in, mode, None)
         return self.out[:n]
@@ -131,42 +133,41 @@ class MoeLayer:
         return self._side_stream
 
     def _block(self, n, x, residual, logits_in, mode, evs):
-        """route (+ shared experts beside it) -> routed experts -> combine on the current
-        stream; evs, if given: 5 events recorded before the routing, after it, after
-        the join with the shared experts, after the routed experts, after the combine."""
+        """route -> shared experts -> routed experts -> combine on the current stream.
+        evs, if given: 5 events recorded at the start, once the routing has completed,
+        once the shared experts have (and the routing), once the routed experts have,
+        and at the end; the middle three on a side branch, so the chained launches of
+        the main stream keep overlapping."""
         main = torch.cuda.current_stream()
-        concurrent = self.n_shared > 0 and (mode & 0xFF) == B.MOE_MODE_DECODE and not (mode & B.MOE_MODE_DEBUG_GU)
-        if evs:
-            evs[0].record()
-        if concurrent:  # the shared experts branch off here, before the routing
-            fork = torch.cuda.Event()
-            fork.record(main)
-        # the routing is issued first so that its CTAs are placed before the
-        # persistent shared-expert kernel fills the SMs
-        self.route(n, x, logits_in=logits_in)
-        if concurrent:
+        chain = self.n_shared > 0 and (mode & 0xFF) == B.MOE_MODE_DECODE and not (mode & B.MOE_MODE_DEBUG_GU)
+
+        def mark(ev):
             side = self._side()
-            side.wait_event(fork)
-            with torch.cuda.stream(side):
-                self.shared_experts(n, x)
+            side.wait_stream(main)
+            ev.record(side)
+
         if evs:
-            evs[1].record()
-        if concurrent:
-            main.wait_stream(side)
+            evs[0].record(main)
+        self.route(n, x, logits_in=logits_in)
+        if evs:
+            mark(evs[1])
+        if chain:
+            self.shared_experts(n, x, after_route=True)
             if evs:
-                evs[2].record()
+                mark(evs[2])
             self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
         elif evs:
             self.experts(n, mode=mode | B.MOE_MODE_SHARED_ONLY)
-            evs[2].record()
+            mark(evs[2])
             self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
         else:
             self.experts(n, mode=mode)
         if evs:
-            evs[3].record()
+            mark(evs[3])
         self.combine(n, residual)
         if evs:
-            evs[4].record()
+            main.wait_stream(self._side())
+            evs[4].record(main)
 
     def capture(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
                 events: bool = False):
@@ -175,11 +176,11 @@ class MoeLayer:
         The graph reads the block from the given device buffers (x, residual and, if
         given, logits_in): refill them and call ``graph.replay()`` per block; the
         output lands in ``self.out``.  Kernel parameters, including the TMA tensor
-        maps, are fixed at capture time.  The graph runs the shared experts on a side
-        stream beside the routing, as forward() does.  With events=True five timing
-        events are recorded inside the graph (before the routing, after it, after the
-        join with the shared experts, after the routed experts, after the combine) and
-        returned; the events are None if the runtime refuses them."""
+        maps, are fixed at capture time.  The graph chains the kernels as forward()
+        does.  With events=True five timing events are recorded inside the graph (at
+        the start, after the routing, after the shared experts, after the routed
+        experts, at the end) and returned; the events are None if the runtime refuses
+        them."""
         import torch as _torch
         n = x.shape[0] if n_rows is None else n_rows
         side = _torch.cuda.Stream()

@@ -166,9 +166,11 @@ def test_shared_experts_tiny():
             assert err < 1e-4, (n, s, err)
 
 
-def test_shared_experts_beside_routing_match_the_sequential_layer():
-    """moe_shared_experts on a side stream beside moe_route (what forward() does)
-    gives the same bits as the shared experts run after the routing on one stream."""
+def test_shared_experts_after_routing_match_the_sequential_layer():
+    """moe_shared_experts_after_route chained behind moe_route (what forward() does:
+    its kernel starts beside the routing and makes its own f16 copy of the rows)
+    gives the same bits as one moe_expert_block call after the routing, and so does
+    a stand-alone moe_shared_experts call."""
     lay = SeededLayer(TINY_SHARED, seed=11, n_rows_max=16)
     L = lay.layer
     for n in (1, 7, 16):
@@ -184,7 +186,33 @@ def test_shared_experts_beside_routing_match_the_sequential_layer():
         torch.cuda.synchronize()
         assert torch.equal(L.shared_y(n), seq_shared), n
         assert torch.equal(conc_out, seq_out), n
+        L.shared_y(n).zero_()
+        L.shared_experts(n, x)
+        torch.cuda.synchronize()
+        assert torch.equal(L.shared_y(n), seq_shared), n
         assert L.error_bits() == 0
+
+
+def test_layer_graph_with_timing_events_matches_forward():
+    """The captured layer (chained launches, timing events on a side branch) gives the
+    bits of forward(), replay after replay."""
+    lay = SeededLayer(TINY_SHARED, seed=13, n_rows_max=16)
+    L = lay.layer
+    n = 3
+    x = to_dev_u16(syn.x_rows(13, range(n), TINY.d_model))
+    res = to_dev_u16(syn.x_rows(13, range(n), TINY.d_model, tag=syn.TAG_RESIDUAL))
+    want = L.forward(x, res).clone()
+    for events in (False, True):
+        g, evs = L.capture(x, res, events=events)
+        for _ in range(3):
+            L.out.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(L.out[:n], want)
+        if evs:
+            t = [evs[0].elapsed_time(evs[i]) for i in range(1, 5)]
+            assert all(v >= 0 for v in t) and t[3] >= max(t[:3])
+    assert L.error_bits() == 0
 
 
 def test_slot_ready_flag_never_set_times_out_cleanly():
