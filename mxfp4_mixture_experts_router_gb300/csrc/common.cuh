@@ -30,6 +30,7 @@ enum Ctrl : int {
     CTRL_EXIT_SH = 9,    // its finished CTAs
     CTRL_PREP_SH = 10,   // rows of the block claimed for the shared experts' f16 copy
     CTRL_PREPD_SH = 11,  // rows of that copy written
+    CTRL_RT_DONE = 12,   // routing finishers done with their rows' f16 copies
     CTRL_XMAX = 64,      // [64, 96): per-row max |x| bits published by the router GEMV CTAs
     CTRL_WORDS = 128
 };

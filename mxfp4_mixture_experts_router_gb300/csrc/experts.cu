@@ -41,7 +41,8 @@ constexpr int EX_STAGE = 17408;               // codes + scales
 constexpr int EX_NT = 2;                      // n-tiles of 8 rows: up to 16 rows per expert
 constexpr int EX_RED_FLOATS = EX_CW * 4 * EX_NT * 4 * 32;  // one down-item reduction
 constexpr int EX_RED_GU = EX_CW * 2 * EX_NT * 4 * 32;      // a gate/up item uses half of it
-constexpr size_t EX_SMEM = (size_t)EX_NST * EX_STAGE + EX_RED_FLOATS * 4 + 1024 + 1024;
+constexpr int EX_XS_BYTES = 57344;             // the block's f16 rows, kept in shared memory when they fit
+constexpr size_t EX_SMEM = (size_t)EX_NST * EX_STAGE + EX_RED_FLOATS * 4 + EX_XS_BYTES + 64 + 1024 + 1024;
 
 enum { IT_GU = 0, IT_DN = 1 };
 enum { J_LAYER = 0, J_Q8_SWIGLU = 1, J_Q8_PLAIN = 2 };
@@ -68,6 +69,7 @@ struct ExParams {
     // by the first CTAs to start; null when x16 was written by an earlier kernel
     const uint16_t* x_rows;
     int dep_at_end;  // wait for the previous kernel on the stream at the end, not the start
+    int x_smem;      // with x_rows: every CTA keeps its own f16 copy in shared memory (N d <= EX_XS_BYTES / 2)
     const int* expert_slot;
     const uint32_t* slot_ready;
     int n_slots;
@@ -201,7 +203,7 @@ __device__ __forceinline__ void gu_stage(uint32_t st, const Geom& g, int chunk, 
 #pragma unroll
         for (int nt = 0; nt < EX_NT; nt++) {
             bx[nt] = make_uint4(0, 0, 0, 0);
-            if (nt < NT && bval[nt]) bx[nt] = __ldca(reinterpret_cast<const uint4*>(xrow[nt] + kk));
+            if (nt < NT && bval[nt]) bx[nt] = *reinterpret_cast<const uint4*>(xrow[nt] + kk);
         }
         uint32_t g0[4], g1[4], u0[4], u1[4];
         load_a<FMT>(gateC, g, 16, gq, gq + 8, q, i, g0, g1);
@@ -243,8 +245,8 @@ __device__ __forceinline__ void dn_stage(uint32_t st, const Geom& g, int chunk, 
 #pragma unroll
             for (int t = 0; t < 4; t++) hi[nt][t] = lo[nt][t] = 0u;
             if (nt < NT && bval[nt]) {
-                const float4 va = __ldcg(reinterpret_cast<const float4*>(hrow[nt] + kk));
-                const float4 vb = __ldcg(reinterpret_cast<const float4*>(hrow[nt] + kk + 4));
+                const float4 va = __ldca(reinterpret_cast<const float4*>(hrow[nt] + kk));
+                const float4 vb = __ldca(reinterpret_cast<const float4*>(hrow[nt] + kk + 4));
                 const float v[8] = {va.x * hs[nt], va.y * hs[nt], va.z * hs[nt], va.w * hs[nt],
                                     vb.x * hs[nt], vb.y * hs[nt], vb.z * hs[nt], vb.w * hs[nt]};
 #pragma unroll
@@ -340,7 +342,7 @@ __device__ __forceinline__ float scale_t(uint32_t w, int t) {
 }
 
 template <int FMT, int T, int NT>
-__device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunks, int cw, int lane,
+__device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunks, int cw, int lane, bool xg,
                                               const __half* const (&xrow)[EX_NT],
                                               const bool (&bval)[EX_NT], float (&ag)[EX_NT][4],
                                               float (&au)[EX_NT][4]) {
@@ -351,9 +353,9 @@ __device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunk
     fast_offsets<FMT, T, 16>(cw, lane, aoff);
     const uint32_t upC = st + 512 * 16;
     const uint32_t gateS = st + EX_CODE_BYTES + gq * SB + 4 * cw, upS = gateS + 512;
-    if (chunk + 1 < nchunks) {
-        // the item's next stage reads the next K slice of the same rows: T*64 bytes
-        // per row and warp, fetched into L1 one 128-byte line per lane i
+    if (xg && chunk + 1 < nchunks) {
+        // the item's next stage reads the next K slice of the same rows (in global
+        // memory): T*64 bytes per row and warp, fetched into L1 one 128-byte line per lane i
         constexpr int LINES = (T * 64 + 127) / 128;
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
@@ -369,7 +371,7 @@ __device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunk
         for (int nt = 0; nt < NT; nt++) {
             bx[nt] = make_uint4(0, 0, 0, 0);
             if (bval[nt])
-                bx[nt] = __ldca(reinterpret_cast<const uint4*>(xrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i));
+                bx[nt] = *reinterpret_cast<const uint4*>(xrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i);
         }
         uint32_t g0[4], g1[4], u0[4], u1[4];
         load_a_fast<FMT>(st + aoff[t], g0, g1);
@@ -392,13 +394,21 @@ __device__ __forceinline__ void gu_stage_fast(uint32_t st, int chunk, int nchunk
 }
 
 template <int FMT, int T, int NT>
-__device__ __forceinline__ void dn_stage_fast(uint32_t st, int chunk, int cw, int lane,
+__device__ __forceinline__ void dn_stage_fast(uint32_t st, int chunk, int nchunks, int cw, int lane,
                                               const float* const (&hrow)[EX_NT],
                                               const float (&hs)[EX_NT], const bool (&bval)[EX_NT],
                                               float (&acc)[4][EX_NT][4]) {
     constexpr int GPS = 8 * T;
     constexpr int SB = FMT == MOE_FMT_MXFP4 ? GPS : 2 * GPS;
     const int gq = lane >> 2, i = lane & 3;
+    if (chunk + 1 < nchunks) {
+        // the next stage's h values of the same rows: T*128 bytes per row and warp,
+        // into L1 one line per lane i < T
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            if (bval[nt] && i < T)
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(hrow[nt] + ((chunk + 1) * GPS + cw * T + i) * 32));
+    }
     uint32_t aoff[T];
     fast_offsets<FMT, T, 64>(cw, lane, aoff);
     const uint32_t S = st + EX_CODE_BYTES + gq * SB + 2 * cw;
@@ -416,8 +426,8 @@ __device__ __forceinline__ void dn_stage_fast(uint32_t st, int chunk, int cw, in
             float4 va = make_float4(0.f, 0.f, 0.f, 0.f), vb = va;
             if (bval[nt]) {
                 const float* src = hrow[nt] + (chunk * GPS + cw * T + t) * 32 + 8 * i;
-                va = __ldcg(reinterpret_cast<const float4*>(src));
-                vb = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                va = __ldca(reinterpret_cast<const float4*>(src));
+                vb = __ldca(reinterpret_cast<const float4*>(src + 4));
             }
             const float v[8] = {va.x * hs[nt], va.y * hs[nt], va.z * hs[nt],
                                 va.w * hs[nt], vb.x * hs[nt], vb.y * hs[nt],
@@ -651,7 +661,8 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
 }
 
 template <int FR, int FS, bool FAST>
-__device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* red_base, uint64_t* full,
+__device__ void consumer(const ExParams& p, int V, const __half* x16, const int* xexp, bool x_global,
+                         unsigned char* ring, float* red_base, uint64_t* full,
                          uint64_t* empty, const Meta* meta) {
     const int tid = threadIdx.x, cw = tid >> 5, lane = tid & 31;
     const int S = p.n_shared, N = p.n_rows;
@@ -697,12 +708,12 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
             for (int nt = 0; nt < EX_NT; nt++) {
                 const int col = nt * 8 + (lane >> 2);
                 bval[nt] = col < c.r;
-                xrow[nt] = p.x16;
+                xrow[nt] = x16;
                 hrow[nt] = p.h;
                 hs[nt] = 1.f;
                 if (bval[nt]) {
                     if (type == IT_GU) {
-                        xrow[nt] = p.x16 + (size_t)pair_row(p, c, col) * p.k_gu;
+                        xrow[nt] = x16 + (size_t)pair_row(p, c, col) * p.k_gu;
                     } else {
                         hrow[nt] = p.h + (size_t)(c.pb + col) * p.k_dn;
                     }
@@ -732,6 +743,13 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
 #pragma unroll
                 for (int nt = 0; nt < EX_NT; nt++)
                     if (bval[nt]) hs[nt] = exp2i(-f16_scale_exponent(__ldcg(p.hmax + c.pb + nt * 8 + (lane >> 2))));
+                if constexpr (FAST) {  // the first stage's h lines (each stage prefetches the next)
+                    const int T = c.shared ? Tiles<FS>::T_DN : Tiles<FR>::T_DN;
+#pragma unroll
+                    for (int nt = 0; nt < EX_NT; nt++)
+                        if (bval[nt] && (lane & 3) < T)
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(hrow[nt] + (cw * T + (lane & 3)) * 32));
+                }
             }
         }
         const uint32_t st = smem_u32(ring + (size_t)stage * EX_STAGE);
@@ -739,26 +757,26 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
             if (type == IT_GU) {
                 if (c.shared) {
                     if (c.NT == 1)
-                        gu_stage_fast<FS, Tiles<FS>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                        gu_stage_fast<FS, Tiles<FS>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, x_global, xrow, bval, acc[0], acc[1]);
                     else
-                        gu_stage_fast<FS, Tiles<FS>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                        gu_stage_fast<FS, Tiles<FS>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, x_global, xrow, bval, acc[0], acc[1]);
                 } else {
                     if (c.NT == 1)
-                        gu_stage_fast<FR, Tiles<FR>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                        gu_stage_fast<FR, Tiles<FR>::T_GU, 1>(st, m.chunk, m.nchunks, cw, lane, x_global, xrow, bval, acc[0], acc[1]);
                     else
-                        gu_stage_fast<FR, Tiles<FR>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, xrow, bval, acc[0], acc[1]);
+                        gu_stage_fast<FR, Tiles<FR>::T_GU, 2>(st, m.chunk, m.nchunks, cw, lane, x_global, xrow, bval, acc[0], acc[1]);
                 }
             } else {
                 if (c.shared) {
                     if (c.NT == 1)
-                        dn_stage_fast<FS, Tiles<FS>::T_DN, 1>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                        dn_stage_fast<FS, Tiles<FS>::T_DN, 1>(st, m.chunk, m.nchunks, cw, lane, hrow, hs, bval, acc);
                     else
-                        dn_stage_fast<FS, Tiles<FS>::T_DN, 2>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                        dn_stage_fast<FS, Tiles<FS>::T_DN, 2>(st, m.chunk, m.nchunks, cw, lane, hrow, hs, bval, acc);
                 } else {
                     if (c.NT == 1)
-                        dn_stage_fast<FR, Tiles<FR>::T_DN, 1>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                        dn_stage_fast<FR, Tiles<FR>::T_DN, 1>(st, m.chunk, m.nchunks, cw, lane, hrow, hs, bval, acc);
                     else
-                        dn_stage_fast<FR, Tiles<FR>::T_DN, 2>(st, m.chunk, cw, lane, hrow, hs, bval, acc);
+                        dn_stage_fast<FR, Tiles<FR>::T_DN, 2>(st, m.chunk, m.nchunks, cw, lane, hrow, hs, bval, acc);
                 }
             }
         } else {
@@ -810,7 +828,7 @@ __device__ void consumer(const ExParams& p, int V, unsigned char* ring, float* r
                 uint32_t amax = 0;
                 if (col < c.r) {
                     const int row = pair_row(p, c, col);
-                    const float sc = exp2i(__ldca(p.xexp + row));
+                    const float sc = exp2i(xexp[row]);
                     gs *= sc;
                     us *= sc;
                     const float hv = gs / (1.f + expf(-gs)) * us;
@@ -870,7 +888,9 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* ring = smem;
     float* red = reinterpret_cast<float*>(ring + (size_t)EX_NST * EX_STAGE);
-    uint64_t* full = reinterpret_cast<uint64_t*>(red + EX_RED_FLOATS);
+    __half* xs = reinterpret_cast<__half*>(red + EX_RED_FLOATS);
+    int* xs_exp = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(xs) + EX_XS_BYTES);  // [16]
+    uint64_t* full = reinterpret_cast<uint64_t*>(xs_exp + 16);
     uint64_t* empty = full + EX_NST;
     Meta* meta = reinterpret_cast<Meta*>(empty + EX_NST);
     __shared__ int s_last;
@@ -897,8 +917,20 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         if (tid == EX_CT) producer(p, V, ring, full, empty, meta);
         return;
     }
-    if (p.x_rows != nullptr) prepare_rows(p);
-    consumer<FR, FS, FAST>(p, V, ring, red, full, empty, meta);
+    const __half* x16 = p.x16;
+    const int* xexp = p.xexp;
+    if (p.x_rows != nullptr && p.x_smem) {
+        // every CTA makes the f16 copy it reads (no hand-off between CTAs)
+        __shared__ uint32_t s_max[EX_CW];
+        for (int n = 0; n < p.n_rows; n++)
+            row_to_f16(p.k_gu, p.x_rows + (size_t)n * p.k_gu, xs + (size_t)n * p.k_gu, xs_exp + n, s_max);
+        consumer_sync<EX_CT>();
+        x16 = xs;
+        xexp = xs_exp;
+    } else if (p.x_rows != nullptr) {
+        prepare_rows(p);
+    }
+    consumer<FR, FS, FAST>(p, V, x16, xexp, !(p.x_rows != nullptr && p.x_smem), ring, red, full, empty, meta);
 
     // the last CTA to finish leaves the workspace clean for the next call
     consumer_sync<EX_CT>();
@@ -914,7 +946,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         if (tid == 0) {
             p.ctrl[p.work_word] = 0;
             p.ctrl[p.exit_word] = 0;
-            if (p.x_rows != nullptr) {
+            if (p.x_rows != nullptr && !p.x_smem) {
                 p.ctrl[CTRL_PREP_SH] = 0;
                 p.ctrl[CTRL_PREPD_SH] = 0;
             }
@@ -1259,6 +1291,7 @@ static int shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* 
     p.work_word = CTRL_WORK_SH;
     p.exit_word = CTRL_EXIT_SH;
     p.x_rows = x;
+    p.x_smem = (size_t)n_rows * d * 2 <= (size_t)EX_XS_BYTES ? 1 : 0;
     p.dep_at_end = after_route ? 1 : 0;
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream));
 }

@@ -74,7 +74,9 @@ struct Cfg {
     static constexpr uint32_t TM_COLS = TM_SFB + NST * 8 <= 256 ? 256 : 512;
     // per expert: (slot, first pair | pairs << 16) and the prefix of its chunk counts
     static constexpr int MAX_U = NBM == 16 ? 256 : 1024;
-    static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + 12;
+    // blocks of up to 5 rows: the block row of every (row, slot) pair (5 x k <= 160)
+    static constexpr int TOKS = NBM == 16 ? 160 : 0;
+    static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 12;
     static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -238,6 +240,24 @@ __device__ bool wait_bits(const Params& p, const uint32_t* flag, uint32_t bits) 
     return true;
 }
 
+// a claimed work item, decoded: its type, chunk, block, K split, slot and pairs
+struct Plan {
+    int item, type, cid, blk, split, z, p0, rc;
+};
+
+__device__ __forceinline__ void plan_item(const Params& p, int V, int U, const uint2* umeta, const int* cp, int item,
+                                          int total, Plan& q) {
+    q.item = item;
+    if (item >= total) return;
+    decode_item(p, V, item, q.type, q.cid, q.blk, q.split);
+    const int u = chunk_expert(cp, U, q.cid);
+    const uint2 mu = umeta[u];
+    const int o0 = (int)(mu.y & 0xFFFFu), r = (int)(mu.y >> 16);
+    q.z = (int)mu.x;
+    q.p0 = o0 + CHUNK * (q.cid - cp[u]);  // the chunk's first pair
+    q.rc = min(CHUNK, o0 + r - q.p0);     // and its pairs
+}
+
 // bounded wait until *flag >= target; false (with the timeout bit set) if it gave up
 __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t target) {
     if (ld_acquire(flag) >= target) return true;
@@ -269,22 +289,18 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
     uint32_t stage = 0, phase = 0, pending = 0, pending_par = 0;
     uint32_t sc_any = 0u, sc_cnt = 0u;  // per scale buffer: armed at all, and the parity of its arm count
     bool ok = true;
-    int item = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
-    for (int seq = 0; ok && item < total; seq++) {
-        int type, cid, blk, split;
-        decode_item(p, V, item, type, cid, blk, split);
-        const int u = chunk_expert(cp, U, cid);
-        const uint2 mu = umeta[u];
-        const int z = (int)mu.x, o0 = (int)(mu.y & 0xFFFFu), r = (int)(mu.y >> 16);
-        const int p0 = o0 + CHUNK * (cid - cp[u]);       // the chunk's first pair
-        const int rc = min(CHUNK, o0 + r - p0);          // and its pairs
+    Plan cur, nxt;
+    plan_item(p, V, U, umeta, cp, (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u), total, cur);
+    for (int seq = 0; ok && cur.item < total; seq++) {
+        const int item = cur.item, type = cur.type, cid = cur.cid, blk = cur.blk, split = cur.split;
+        const int z = cur.z, p0 = cur.p0, rc = cur.rc;
         const bool gu = type == IT_GU;
         // gate/up items need the slot's gate/up planes (bit 0), down items its down planes (bit 1)
         if (p.slot_ready != nullptr) ok = wait_bits(p, p.slot_ready + z, gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN);
         if (ok && !gu) {
-            // the chunk's SwiGLU activations must be complete before they are read
+            // the chunk's SwiGLU activations must be complete before the scale movers
+            // read them (they read this item's stages only after its claim below)
             ok = wait_at_least(p, p.gu_done + cid, (uint32_t)p.n_gu);
-            asm volatile("fence.proxy.async.global;" ::: "memory");
         }
         if (!ok) break;
         const int kr = gu ? p.d / S : p.f;     // K range of the item
@@ -300,6 +316,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
         const uint32_t tx = (uint32_t)(A_BYTES / 2);
         const uint32_t tx_sc = (uint32_t)(128 * sc);
         int next = total;
+        nxt.item = total;
         for (int c = 0; c < nch; c++) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                 set_error(p.ctrl, MOE_EBIT_TIMEOUT);
@@ -350,11 +367,13 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
                 stage = 0;
                 phase ^= 1u;
             }
-            // the next claim, issued now and read after the item: its latency hides
-            // behind this item's stages
+            // the next claim, issued now and decoded a few stages later: its latency
+            // and the decoding hide behind this item's stages (every item has at least
+            // NST >= 4 stages)
             if (c == 0) next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
+            if (c == 3) plan_item(p, V, U, umeta, cp, next, total, nxt);
         }
-        item = next;
+        cur = nxt;
     }
     // tell the consumers there is nothing more (after an error too, if a stage frees up)
     if (mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -385,10 +404,11 @@ struct BStage {
 // source row of activation row `row` of a stage: gate/up gathers the E4M3 terms of
 // the block rows of the chunk's pairs (3 x the pair's token + term), down reads the
 // chunk's rows of h (3 x pair + term) in place
-__device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row) {
+__device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row, const uint16_t* tok) {
     if (m.type != IT_GU) return m.brow + row;
     const int q = row / 3;
-    return 3 * (__ldg(p.pair + m.p0 + q) / p.k) + (row - 3 * q);
+    const int n = tok != nullptr ? (int)tok[m.p0 + q] : __ldg(p.pair + m.p0 + q) / p.k;
+    return 3 * n + (row - 3 * q);
 }
 
 // the source rows this thread reads for an item (data rows j / 16 of its chunks j,
@@ -401,25 +421,27 @@ struct BRows {
 };
 
 template <int NBM>
-__device__ __forceinline__ void b_rows(const Params& p, const Meta& m, int t, int lane, BRows<NBM>& r) {
+__device__ __forceinline__ void b_rows(const Params& p, const Meta& m, int t, int lane, BRows<NBM>& r,
+                                       const uint16_t* tok) {
     if (r.item == m.item) return;
     r.item = m.item;
 #pragma unroll
     for (int i = 0; i < NBM / 8; i++) {
         const int row = (t + 128 * i) >> 4;
-        r.d[i] = row < m.nrow ? b_src_row(p, m, row) : 0;
+        r.d[i] = row < m.nrow ? b_src_row(p, m, row, tok) : 0;
     }
 #pragma unroll
     for (int c = 0; c < 2; c++) {
         const int row = 32 * c + lane;
-        r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(p, m, row) : 0;
+        r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(p, m, row, tok) : 0;
     }
 }
 
+// the lines b_load will read for stage `chunk` of item m, into L1 (one prefetch per
+// 128-byte line of activation rows, one per scale row); rows from r
 template <int NBM>
-__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b,
-                                       BRows<NBM>& rows) {
-    b_rows<NBM>(p, m, t, lane, rows);
+__device__ __forceinline__ void b_prefetch(const Params& p, const Meta& m, int chunk, int t, int lane,
+                                           const BRows<NBM>& r) {
     const bool gu = m.type == IT_GU;
     const uint8_t* src = gu ? p.x_mx : p.h_mx;
     const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
@@ -428,14 +450,37 @@ __device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk
 #pragma unroll
     for (int i = 0; i < NBM / 8; i++) {
         const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
-        b.d[i] = row < m.nrow ? __ldcg(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * ld + k0 + c16 * 16))
+        if (row < m.nrow && (c16 & 7) == 0)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (size_t)r.d[i] * ld + k0 + c16 * 16));
+    }
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        const int row = 32 * c + lane;
+        if (row < m.nrow && row < NBM)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32));
+    }
+}
+
+template <int NBM>
+__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b,
+                                       BRows<NBM>& rows, const uint16_t* tok) {
+    b_rows<NBM>(p, m, t, lane, rows, tok);
+    const bool gu = m.type == IT_GU;
+    const uint8_t* src = gu ? p.x_mx : p.h_mx;
+    const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
+    const int ld = gu ? p.d : p.f;
+    const int k0 = m.kbase + chunk * KC;
+#pragma unroll
+    for (int i = 0; i < NBM / 8; i++) {
+        const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
+        b.d[i] = row < m.nrow ? __ldca(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * ld + k0 + c16 * 16))
                               : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int c = 0; c < 2; c++) {
         const int row = 32 * c + lane;
         b.s[c] = (row < m.nrow && row < NBM)
-                     ? __ldcg(reinterpret_cast<const uint2*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
+                     ? __ldca(reinterpret_cast<const uint2*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
                      : make_uint2(0, 0);
     }
 }
@@ -451,7 +496,7 @@ __device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk
 // when it belongs to the same item.
 template <int NBM>
 __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char* scbuf, uint32_t tbase,
-                            uint64_t* mready, uint64_t* scf, uint64_t* sfr, const Meta* meta) {
+                            uint64_t* mready, uint64_t* scf, uint64_t* sfr, const Meta* meta, const uint16_t* tok) {
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
     uint32_t stage = 0, phase = 0;
@@ -466,7 +511,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         }
         const Meta m = meta[stage];
         if (m.item < 0) break;
-        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b, rows);
+        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b, rows, tok);
         unsigned char* bst = smem + (size_t)stage * C::STAGE + A_BYTES;
 #pragma unroll
         for (int i = 0; i < NBM / 8; i++) {
@@ -498,18 +543,46 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfr[stage]);
-        // the next stage of the same item: its activations are known now
+        const uint32_t nstage = stage + 1 == (uint32_t)C::NST ? 0u : stage + 1;
+        const uint32_t nphase = nstage == 0u ? phase ^ 1u : phase;
         if (m.chunk + 1 < m.nchunks) {
-            b_load<NBM>(p, m, m.chunk + 1, t, lane, b, rows);
+            // the next stage of the same item: its activations are known now
+            b_load<NBM>(p, m, m.chunk + 1, t, lane, b, rows, tok);
             have_item = m.item;
             have_chunk = m.chunk + 1;
+        } else if (__all_sync(0xffffffffu, mbar_peek(&mready[nstage], nphase))) {
+            // the next stage is already claimed (the producer runs ahead while the
+            // ring is full): load the first activations of its item now
+            const Meta mn = meta[nstage];
+            have_item = -1;
+            if (mn.item >= 0) {
+                b_load<NBM>(p, mn, mn.chunk, t, lane, b, rows, tok);
+                have_item = mn.item;
+                have_chunk = mn.chunk;
+            }
         } else {
             have_item = -1;
         }
-        if (++stage == C::NST) {
-            stage = 0;
-            phase ^= 1u;
+        // two stages ahead, into L1: a later chunk of the same item, or the stage
+        // the producer has already claimed (its item's dependencies are met)
+        if (m.chunk + 2 < m.nchunks) {
+            BRows<NBM> r2 = rows;
+            if (r2.item != m.item) b_rows<NBM>(p, m, t, lane, r2, tok);
+            b_prefetch<NBM>(p, m, m.chunk + 2, t, lane, r2);
+        } else if (tok != nullptr) {
+            const uint32_t s2 = nstage + 1 == (uint32_t)C::NST ? 0u : nstage + 1;
+            const uint32_t ph2 = s2 == 0u ? nphase ^ 1u : nphase;
+            if (__all_sync(0xffffffffu, mbar_peek(&mready[s2], ph2))) {
+                const Meta m2 = meta[s2];
+                if (m2.item >= 0) {
+                    BRows<NBM> r2;
+                    b_rows<NBM>(p, m2, t, lane, r2, tok);
+                    b_prefetch<NBM>(p, m2, m2.chunk, t, lane, r2);
+                }
+            }
         }
+        stage = nstage;
+        phase = nphase;
     }
 }
 
@@ -721,6 +794,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     float* xch = reinterpret_cast<float*>(scbuf + 2 * C::SCB);
     uint2* umeta = reinterpret_cast<uint2*>(xch + XCH_FLOATS);
     int* cp = reinterpret_cast<int*>(umeta + C::MAX_U);  // [MAX_U + 1] chunk prefix
+    uint16_t* tok = C::TOKS > 0 ? reinterpret_cast<uint16_t*>(cp + C::MAX_U + 1) : nullptr;  // [TOKS]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)C::NST * C::STAGE + 2 * C::SCB + XCH_FLOATS * 4 +
                                                  ((C::META_BYTES + 15) & ~15));
     uint64_t* full = bars;
@@ -775,6 +849,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         }
         umeta[u] = make_uint2((uint32_t)z, (uint32_t)o0 | ((uint32_t)r << 16));
     }
+    if (tok != nullptr)  // the block row of every pair (small blocks only)
+        for (int i = tid; i < p.nk && i < C::TOKS; i += NTHREADS) tok[i] = (uint16_t)(__ldg(p.pair + i) / p.k);
     __syncthreads();
     if (warp == 1) {
         const int lane = tid & 31, per = (U + 31) / 32, b0 = lane * per, b1 = min(U, b0 + per);
@@ -802,7 +878,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
-        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sfr, meta);
+        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sfr, meta, tok);
     } else {
         epilogue<NBM>(p, tbase, xch, eflag, acc_full, acc_empty, am);
     }

@@ -19,6 +19,7 @@
 namespace moe {
 
 constexpr int RT_THREADS = 256;
+static_assert(RT_THREADS == 256, "topk_row_cta: one histogram bin and 4 experts per thread");
 constexpr int RT_KS = 512;      // K elements per slice
 constexpr int RT_EG = 64;       // experts per group (8 per warp)
 constexpr int RT_MAX_ROWS = 32;
@@ -281,7 +282,8 @@ __device__ __forceinline__ int key_expert(int t, int lane, bool vec) {
 // stopping as soon as exactly k keys qualify; keys above T are all taken and the
 // keys equal to T are taken in index order.  The k winners are then ranked
 // (larger key first, then lower index) through shared memory `sel` (2k words).
-__device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2, uint32_t* sel) {
+// If `sidx` is given, the selected experts also go there (shared memory, k words).
+__device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool from_l2, uint32_t* sel, int* sidx) {
     const int lane = threadIdx.x & 31, K = p.k;
     const bool vec = (p.E & 3) == 0 && ((uintptr_t)lrow & 15) == 0;
     uint32_t key[32];
@@ -426,10 +428,174 @@ __device__ void topk_row(const RouteParams& p, const float* lrow, int n, bool fr
     if (lane < K) {
         p.topk_idx[(size_t)n * K + lane] = my_idx;
         p.topk_w[(size_t)n * K + lane] = ex / sum;
+        if (sidx) sidx[lane] = my_idx;
     }
 }
 
-// Group the block's pairs by expert (N <= 32): smem counts and row bitmaps.
+// top-k of one row by the whole CTA (RT_THREADS threads; blocks of one or two
+// rows, where one warp per row would leave the CTA idle): thread t holds the
+// keys of experts 4t..4t+3.  The k-th largest key T is found by radix selection,
+// 8 bits per round from the most significant, with a shared-memory histogram per
+// round; keys above T are all taken and keys equal to T in index order (a block
+// scan of the tie counts); the k winners are ranked as in topk_row.  Same
+// selection and weight arithmetic as topk_row.  `s` is 2 KB of shared memory.
+__device__ void topk_row_cta(const RouteParams& p, const float* lrow, int n, bool from_l2, uint32_t* s, int* sidx) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, K = p.k, E = p.E;
+    uint32_t* hist = s;                         // [256]
+    uint32_t* wsum = s + 256;                   // [8] per-warp totals, [8] second scan
+    uint32_t* bc = s + 272;                     // [4] broadcast: prefix, remaining k, ...
+    uint32_t* sel = s + 288;                    // [2k]
+    uint32_t key[4];
+    const int e0 = 4 * tid;
+    bool nan = false;
+    if ((E & 3) == 0 && ((uintptr_t)lrow & 15) == 0) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e0 < E)
+            v = from_l2 ? __ldcg(reinterpret_cast<const float4*>(lrow + e0))
+                        : __ldg(reinterpret_cast<const float4*>(lrow + e0));
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            key[j] = e0 + j < E ? sel_key(f[j]) : 0u;
+            nan |= e0 + j < E && isnan(f[j]);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const float f = e0 + j < E ? (from_l2 ? __ldcg(lrow + e0 + j) : __ldg(lrow + e0 + j)) : 0.f;
+            key[j] = e0 + j < E ? sel_key(f) : 0u;
+            nan |= e0 + j < E && isnan(f);
+        }
+    }
+    if (__syncthreads_or(nan) && tid == 0) set_error(p.ctrl, MOE_EBIT_NAN);
+
+    // radix selection: after round r, prefix holds the top 8(r+1) bits of T and
+    // rem the number of keys equal to T on those bits still to take
+    uint32_t prefix = 0u, rem = (uint32_t)K;
+    for (int r = 0; r < 4; r++) {
+        const int shift = 24 - 8 * r;
+        hist[tid] = 0u;  // RT_THREADS == 256 bins
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const bool match = r == 0 || (key[j] >> (shift + 8)) == (prefix >> (shift + 8));
+            if (match && key[j] != 0u) atomicAdd(&hist[(key[j] >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds bins 255-8l .. 248-8l (descending); counts above each bin
+            uint32_t c[8], tot = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                c[j] = hist[255 - 8 * lane - j];
+                tot += c[j];
+            }
+            uint32_t incl = tot;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t up = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += up;
+            }
+            uint32_t above = incl - tot;  // keys in higher bins than this lane's first
+            int hit = -1;
+            uint32_t hit_above = 0;
+#pragma unroll
+            for (int j = 0; j < 8; j++) {
+                if (hit < 0 && above < rem && above + c[j] >= rem) {
+                    hit = j;
+                    hit_above = above;
+                }
+                above += c[j];
+            }
+            const uint32_t m = __ballot_sync(0xffffffffu, hit >= 0);
+            const int src = __ffs(m) - 1;  // exactly one lane holds the bin
+            const int hb = __shfl_sync(0xffffffffu, hit, src);
+            const uint32_t ha = __shfl_sync(0xffffffffu, hit_above, src);
+            if (lane == 0) {
+                bc[0] = prefix | ((uint32_t)(255 - 8 * src - hb) << shift);
+                bc[1] = rem - ha;
+            }
+        }
+        __syncthreads();
+        prefix = bc[0];
+        rem = bc[1];
+    }
+    const uint32_t T = prefix;
+    // rem keys equal to T are taken, in index order; every key above T is taken
+    uint32_t n_take = 0, n_tie = 0;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        n_take += key[j] > T ? 1u : 0u;
+        n_tie += key[j] == T ? 1u : 0u;
+    }
+    // exclusive block scans of the tie counts and of the takes (thread order = index order)
+    uint32_t it = n_tie, ik = n_take;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t a = __shfl_up_sync(0xffffffffu, it, o), b = __shfl_up_sync(0xffffffffu, ik, o);
+        if (lane >= o) {
+            it += a;
+            ik += b;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = it;
+        wsum[8 + warp] = ik;
+    }
+    __syncthreads();
+    uint32_t tie_before = it - n_tie, take_before = ik - n_take;
+    for (int w = 0; w < warp; w++) {
+        tie_before += wsum[w];
+        take_before += wsum[8 + w];
+    }
+    // ties taken by the threads before this one: min(tie_before, rem)
+    uint32_t at = take_before + min(tie_before, rem);
+    uint32_t ties_left = tie_before < rem ? rem - tie_before : 0u;
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const bool take = key[j] > T || (key[j] == T && ties_left > 0u);
+        if (key[j] == T && ties_left > 0u) ties_left--;
+        if (take) {
+            sel[at] = key[j];
+            sel[K + at] = (uint32_t)(e0 + j);
+            at++;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t wk = 0u, wi = 0u;
+        int rank = 0;
+        if (lane < K) {
+            wk = sel[lane];
+            wi = sel[K + lane];
+            for (int j = 0; j < K; j++) {
+                const uint32_t kj = sel[j], ij = sel[K + j];
+                rank += (kj > wk || (kj == wk && ij < wi)) ? 1 : 0;
+            }
+        }
+        __syncwarp();
+        if (lane < K) {
+            sel[rank] = wk;
+            sel[K + rank] = wi;
+        }
+        __syncwarp();
+        const uint32_t my_key = lane < K ? sel[lane] : 0u;
+        const int my_idx = lane < K ? (int)sel[K + lane] : 0;
+        const float my_val = (lane < K) ? key_value(my_key) : 0.f;
+        // weights: exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in slot order
+        const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
+        const float ex = (lane < K) ? expf(my_val - l0) : 0.f;
+        float sum = 0.f;
+        for (int j = 0; j < K; j++) sum += __shfl_sync(0xffffffffu, ex, j);
+        if (lane < K) {
+            p.topk_idx[(size_t)n * K + lane] = my_idx;
+            p.topk_w[(size_t)n * K + lane] = ex / sum;
+            if (sidx) sidx[lane] = my_idx;
+        }
+    }
+    __syncthreads();  // s is reused by the next row
+}
+
+// Group the block's pairs by expert (N <= 32): smem counts and row bitmaps; s_idx
+// holds the block's selections (N k words, written by topk_row).
 __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, int* s_off, int* s_idx) {
     const int tid = threadIdx.x;
     const int NK = p.N * p.k;
@@ -439,47 +605,63 @@ __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, 
     }
     __syncthreads();
     for (int i = tid; i < NK; i += RT_THREADS) {
-        const int e = __ldcg(p.topk_idx + i);
-        s_idx[i] = e;
+        const int e = s_idx[i];
         if (e >= 0 && e < p.E) {
             atomicAdd(&s_cnt[e], 1);
             atomicOr(&s_bits[e], 1u << (i / p.k));
         }
     }
     __syncthreads();
-    // exclusive scan of counts and of the "selected" flags (single warp; E <= 1024)
-    if (tid < 32) {
-        const int lane = tid;
-        const int per = (p.E + 31) / 32;
-        const int b = lane * per;
-        int c = 0, u = 0;
-        for (int e = b; e < min(b + per, p.E); e++) {
-            c += s_cnt[e];
-            u += s_cnt[e] > 0;
+    // exclusive scans over the experts of the counts and of the "selected" flags:
+    // thread t holds experts 4t..4t+3 (E <= 1024 = 4 RT_THREADS)
+    __shared__ int s_wc[RT_THREADS / 32], s_wu[RT_THREADS / 32];
+    {
+        const int lane = tid & 31, warp = tid >> 5;
+        int c[4], ct = 0, ut = 0;
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = 4 * tid + j;
+            c[j] = e < p.E ? s_cnt[e] : 0;
+            ct += c[j];
+            ut += c[j] > 0 ? 1 : 0;
         }
-        int cs = c, us = u;
+        int ic = ct, iu = ut;
         for (int o = 1; o < 32; o <<= 1) {
-            const int a = __shfl_up_sync(0xffffffffu, cs, o);
-            const int bb = __shfl_up_sync(0xffffffffu, us, o);
+            const int a = __shfl_up_sync(0xffffffffu, ic, o), bu = __shfl_up_sync(0xffffffffu, iu, o);
             if (lane >= o) {
-                cs += a;
-                us += bb;
+                ic += a;
+                iu += bu;
             }
         }
-        cs -= c;
-        us -= u;
-        for (int e = b; e < min(b + per, p.E); e++) {
+        if (lane == 31) {
+            s_wc[warp] = ic;
+            s_wu[warp] = iu;
+        }
+        __syncthreads();
+        int cs = ic - ct, us = iu - ut, c_all = 0, u_all = 0;
+        for (int w = 0; w < RT_THREADS / 32; w++) {
+            if (w < warp) {
+                cs += s_wc[w];
+                us += s_wu[w];
+            }
+            c_all += s_wc[w];
+            u_all += s_wu[w];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+            const int e = 4 * tid + j;
+            if (e >= p.E) break;
             s_off[e] = cs;
-            if (s_cnt[e] > 0) {
+            if (c[j] > 0) {
                 p.uexp[us] = e;
                 p.off[us] = cs;
                 us++;
             }
-            cs += s_cnt[e];
+            cs += c[j];
         }
-        if (lane == 31) {
-            p.off[us] = cs;
-            p.ctrl[CTRL_UNIQUE] = (uint32_t)us;
+        if (tid == 0) {
+            p.off[u_all] = c_all;
+            p.ctrl[CTRL_UNIQUE] = (uint32_t)u_all;
             p.ctrl[CTRL_ROWS] = (uint32_t)p.N;
         }
     }
@@ -565,11 +747,6 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
                     p.logits[(size_t)n * p.E + e] = a;
                 }
             }
-            // every slice of this group is done, and every CTA published every row's
-            // max: write the f16 copies of rows n = eg (mod n_eg)
-            for (int n = eg; n < p.N; n += p.n_eg)
-                prep_row_x16(p.x + (size_t)n * p.d, p.d, __ldcg(p.ctrl + CTRL_XMAX + n), p.x16 + (size_t)n * p.d,
-                             p.xexp + n);
             if (tid == 0) p.ctrl[RT_TICKET_EG + eg] = 0;
             group_finisher = true;
         }
@@ -577,29 +754,53 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
         group_finisher = true;  // x-preparation-only CTA (or caller logits)
     }
     if (!group_finisher) return;
+    const bool gemv_finisher = b < p.n_gemv_ctas;
     const int participants = (p.n_gemv_ctas > 0 ? p.n_eg : 0) + ((int)gridDim.x - p.n_gemv_ctas);
     __threadfence();
     __syncthreads();
     if (tid == 0) s_flag = (atomicAdd(p.ctrl + CTRL_TICKET, 1u) == (uint32_t)(participants - 1));
     __syncthreads();
-    if (!s_flag) return;
-    __threadfence();
-
-    // last CTA: selection, weights and grouping for every row
-    const int warp = tid >> 5;
-    const float* L = p.logits_in ? p.logits_in : p.logits;
-    uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw + 32768) + warp * 64;  // 2k words per warp
-    for (int n = warp; n < p.N; n += RT_THREADS / 32)
-        topk_row(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, sel);
-    __threadfence();
+    const bool last = s_flag != 0;
+    if (last) {
+        __threadfence();
+        // last CTA: selection, weights and grouping for every row (tables in shared
+        // memory: grouping [0, 16 KB), selections [32 KB, 34 KB))
+        const int warp = tid >> 5;
+        const float* L = p.logits_in ? p.logits_in : p.logits;
+        int* s_cnt = reinterpret_cast<int*>(smem_raw);
+        uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_cnt + 1024);
+        int* s_off = reinterpret_cast<int*>(s_bits + 1024);
+        int* s_idx = s_off + 1024;
+        if (p.N <= 2) {  // the whole CTA on each row
+            uint32_t* s_topk = reinterpret_cast<uint32_t*>(smem_raw + 32768);
+            for (int n = 0; n < p.N; n++)
+                topk_row_cta(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, s_topk, s_idx + n * p.k);
+        } else {  // a warp per row
+            uint32_t* sel = reinterpret_cast<uint32_t*>(smem_raw + 32768) + warp * 64;  // 2k words per warp
+            for (int n = warp; n < p.N; n += RT_THREADS / 32)
+                topk_row(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, sel, s_idx + n * p.k);
+        }
+        __syncthreads();
+        group_block(p, s_cnt, s_bits, s_off, s_idx);
+        if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
+        if (!gemv_finisher) {  // caller logits: every row's f16 copy is already written
+            for (int n = tid; n < RT_MAX_ROWS; n += RT_THREADS) p.ctrl[CTRL_XMAX + n] = 0;
+            return;
+        }
+    }
+    if (!gemv_finisher) return;
+    // every CTA has published every row's max: the finisher of group eg writes the
+    // f16 copies of rows n = eg (mod n_eg), after the selection (nothing in this
+    // launch waits for them); the last finisher to get here clears the maxima
+    const int eg = b / p.n_ks;
+    for (int n = eg; n < p.N; n += p.n_eg)
+        prep_row_x16(p.x + (size_t)n * p.d, p.d, __ldcg(p.ctrl + CTRL_XMAX + n), p.x16 + (size_t)n * p.d,
+                     p.xexp + n);
     __syncthreads();
-    int* s_cnt = reinterpret_cast<int*>(smem_raw);
-    uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_cnt + 1024);
-    int* s_off = reinterpret_cast<int*>(s_bits + 1024);
-    int* s_idx = s_off + 1024;
-    group_block(p, s_cnt, s_bits, s_off, s_idx);
-    for (int n = tid; n < RT_MAX_ROWS; n += RT_THREADS) p.ctrl[CTRL_XMAX + n] = 0;
-    if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
+    if (tid == 0 && atomicAdd(p.ctrl + CTRL_RT_DONE, 1u) == (uint32_t)(p.n_eg - 1)) {
+        for (int n = 0; n < RT_MAX_ROWS; n++) p.ctrl[CTRL_XMAX + n] = 0;
+        p.ctrl[CTRL_RT_DONE] = 0;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -615,7 +816,7 @@ __global__ void __launch_bounds__(RT_THREADS) route_rows_kernel(const RouteParam
     if (b < n_topk_ctas) {
         const int n = b * (RT_THREADS / 32) + warp;
         if (n >= p.N) return;
-        topk_row(p, p.logits_in + (size_t)n * p.E, n, false, sel[warp]);
+        topk_row(p, p.logits_in + (size_t)n * p.E, n, false, sel[warp], nullptr);
         __syncwarp();
         if (lane < p.k) {
             const int e = __ldcg(p.topk_idx + (size_t)n * p.k + lane);

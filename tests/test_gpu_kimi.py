@@ -109,9 +109,14 @@ def test_topk_ties_at_full_width(kimi):
     lg[5] = rng.normal(size=E).astype(np.float32)
     lg[5, [3, 400, 895]] = np.nan                              # NaN ranks last
     lg[6] = rng.normal(size=E).astype(np.float32)              # plain
-    idx, w = _route_only(lay, lg)
     want = orc.select_topk(lg.astype(np.float64), k)
-    assert np.array_equal(idx, want)
     ok = ~np.isnan(lg).any(axis=1)
-    np.testing.assert_allclose(w[ok], orc.routing_weights(lg.astype(np.float64), want)[ok], rtol=2e-6, atol=1e-7)
-    lay.layer.error_bits()  # the NaN row sets the NaN bit; read and clear it
+    # blocks of 7 rows (a warp per row), of 2 and of 1 (the whole CTA per row)
+    for rows in (7, 2, 1):
+        parts = [_route_only(lay, lg[r:r + rows]) for r in range(0, 7, rows)]
+        idx = np.concatenate([a for a, _ in parts])
+        w = np.concatenate([b for _, b in parts])
+        assert np.array_equal(idx, want), rows
+        np.testing.assert_allclose(w[ok], orc.routing_weights(lg.astype(np.float64), want)[ok], rtol=2e-6,
+                                   atol=1e-7)
+        lay.layer.error_bits()  # the NaN row sets the NaN bit; read and clear it

@@ -94,10 +94,16 @@ def test_topk_ties_signed_zero_and_nan(tiny):
     logits[4, 30] = 1.0
     logits[5, :] = 1.0
     x = syn.x_rows(4, range(n), TINY.d_model)
+    want = orc.select_topk(logits.astype(np.float64), TINY.top_k)
     g = tiny.run(x, x, logits=logits)
-    assert np.array_equal(g["idx"], orc.select_topk(logits.astype(np.float64), TINY.top_k))
+    assert np.array_equal(g["idx"], want)
     assert tiny.layer.error_bits() & B.MOE_EBIT_NAN
     assert tiny.layer.error_bits() == 0  # read-and-clear
+    for rows in (2, 1):  # small blocks: the whole CTA selects for each row
+        for r in range(0, n, rows):
+            g = tiny.run(x[r:r + rows], x[r:r + rows], logits=logits[r:r + rows])
+            assert np.array_equal(g["idx"], want[r:r + rows]), (rows, r)
+    assert tiny.layer.error_bits() & B.MOE_EBIT_NAN
 
 
 def test_expert_slot_placement_does_not_change_bits(tiny):
@@ -245,5 +251,9 @@ def test_topk_expert_count_not_a_multiple_of_four():
     want = orc.select_topk(lg.astype(np.float64), sh.top_k)
     assert np.array_equal(g["idx"], want)
     np.testing.assert_allclose(g["w"], orc.routing_weights(lg.astype(np.float64), want), rtol=2e-6, atol=1e-7)
+    for r in range(5):  # one row per block: the whole CTA selects
+        one = lay.run(x[r:r + 1], x[r:r + 1], logits=lg[r:r + 1])
+        assert np.array_equal(one["idx"][0], want[r]), r
+        assert np.array_equal(one["w"][0].view(np.uint32), g["w"][r].view(np.uint32)), r
     o = lay.oracle(x, x, logits=lg)
     assert_close_to_oracle(g["out"], o, "30 experts")
