@@ -675,6 +675,12 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
     float acc[4][EX_NT][4];
     int type = IT_GU, blk = 0;
     uint32_t items_done = 0;
+    // scale exponents of the h columns of the last expert whose down items ran here
+    // (final once its gate/up items are done; the same for all its down items)
+    __shared__ int s_hexp[EX_NT * 8];
+    __shared__ int s_hexp_v;
+    if (tid == 0) s_hexp_v = -1;
+    consumer_sync<EX_CT>();
 
     while (true) {
         if (!mbar_wait(&full[stage], phase)) {
@@ -740,9 +746,16 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
                     }
                     consumer_sync<EX_CT>();
                 }
+                const int cached = s_hexp_v;
+                consumer_sync<EX_CT>();
+                if (cached != c.v) {
+                    if (tid < c.r && tid < EX_NT * 8) s_hexp[tid] = f16_scale_exponent(__ldcg(p.hmax + c.pb + tid));
+                    if (tid == 0) s_hexp_v = c.v;
+                    consumer_sync<EX_CT>();
+                }
 #pragma unroll
                 for (int nt = 0; nt < EX_NT; nt++)
-                    if (bval[nt]) hs[nt] = exp2i(-f16_scale_exponent(__ldcg(p.hmax + c.pb + nt * 8 + (lane >> 2))));
+                    if (bval[nt]) hs[nt] = exp2i(-s_hexp[nt * 8 + (lane >> 2)]);
                 if constexpr (FAST) {  // the first stage's h lines (each stage prefetches the next)
                     const int T = c.shared ? Tiles<FS>::T_DN : Tiles<FR>::T_DN;
 #pragma unroll
@@ -868,7 +881,7 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
                 if (col >= c.r) continue;
                 float y = 0.f;
                 for (int w = 0; w < EX_CW; w++) y += red[((w * 4 + mt) * EX_NT + nt) * 128 + t * 32 + ln];
-                y *= exp2i(f16_scale_exponent(__ldcg(p.hmax + c.pb + col)));
+                y *= exp2i(s_hexp[col]);
                 const int mrow = blk * 64 + mt * 16 + (ln >> 2) + 8 * (t >> 1);
                 if (c.shared) {
                     float* dst = p.out_shared + (size_t)(c.pb + col) * p.m_dn + mrow;
