@@ -24,9 +24,10 @@
 //               E4M3 terms, or write the outputs.
 // Work items: gate/up items (64 rows of gate + the same 64 rows of up = one
 // M=128 tile, over one of TC_GU_SPLIT K ranges) and down items (128 rows, full
-// K), ordered gate/up of expert v then down of expert v-lag.  A down item's
-// activations are read only after every gate/up tile of its expert is finished
-// (bounded wait).
+// K): the gate/up items of every chunk first, then the down items in chunk
+// order, so a chunk's down items are claimed long after its gate/up tiles and
+// none waits at the end of the launch.  A down item's activations are read
+// only after every gate/up tile of its chunk is finished (bounded wait).
 //
 // The TMA engine moves about 18 bytes a cycle per SM and costs a roughly fixed
 // time per box, so it carries only the weights: a stage is one box of code rows
@@ -1021,7 +1022,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.nk = n_rows * k;
     p.n_gu = f / 64;
     p.n_dn = d / 128;
-    p.lag = 8;
+    p.lag = 1 << 30;  // every gate/up item before the first down item
     p.debug = (mode & MOE_MODE_DEBUG_GU) ? 1 : 0;
 
     p.expert_slot = expert_slot;
