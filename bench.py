@@ -593,6 +593,44 @@ def run_prefill_bench(args):
             "peak_gbs": peak, "peak_kind": peak_kind, "blocks": res, "data": "synthetic"}
 
 
+def run_prefill_profile_case(args):
+    """Small prefill case for ncu: 270 rows whose router logits favour 160 of the 896
+    experts (+8 on those), so each selected expert gets about 27 (row, slot) pairs, as in
+    the 1,533-row block with all experts; a pool of those 160 experts (2.8 GB).  Four
+    blocks, L2 flushed before each."""
+    import torch
+
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+
+    build_mod.build()
+    sh = syn.KIMI
+    E, k, d, n = sh.n_experts, sh.top_k, sh.d_model, 270
+    rng = np.random.default_rng(SEED + 7)
+    hot = np.sort(rng.choice(E, size=160, replace=False))
+    lg = rng.normal(size=(n, E)).astype(np.float32)
+    lg[:, hot] += 8.0
+    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=n, n_shared=0)
+    lay.alloc_pool(len(hot))
+    slots = np.zeros(E, dtype=np.int32)
+    threads = max(2, min(16, os.cpu_count() or 2))
+    for i, (e, slab) in enumerate(syn.mxfp4_slabs_parallel(SEED, hot.tolist(), sh, threads=threads)):
+        lay.put_slab(i, slab)
+        slots[e] = i
+    lay.set_expert_slots(slots)
+    x = torch.from_numpy(syn.x_rows(SEED, range(n), d).view(np.int16)).cuda().view(torch.uint16)
+    L = torch.from_numpy(lg).cuda()
+    flush = L2Flush(torch, torch.device("cuda"))
+    for _ in range(4):
+        flush.zero_()
+        lay.forward(x, x, logits_in=L, mode=B.MOE_MODE_PREFILL)
+    torch.cuda.synchronize()
+    assert lay.error_bits() == 0
+    u = int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item())
+    print(json.dumps({"prefill_profile_case": "ok", "rows": n, "unique_experts": u, "pairs": n * k}))
+
+
 def run_reference(args):
     """The CPU oracle timed on this host's cores: each step is the oracle's expert MLP
     of one (row, selected expert) pair of the workload (17,547,264 expert bytes)."""
@@ -635,7 +673,13 @@ def main():
     ap.add_argument("--prefill-rows", default="270,1533")
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--prefill-warmup", type=int, default=2)
+    ap.add_argument("--prefill-profile-case", action="store_true",
+                    help="run the small prefill ncu case (270 rows over 160 experts, 2.8 GB) and exit")
     args = ap.parse_args()
+
+    if args.prefill_profile_case:
+        run_prefill_profile_case(args)
+        return
 
     if args.prefill_bench:
         print(json.dumps(run_prefill_bench(args)))
