@@ -47,7 +47,7 @@ ROUTER_BYTES = 896 * 7168 * 2
 # dram__bytes_read.sum + dram__bytes_write.sum of an ncu capture of the profile case
 # (one row, the same 16 experts per launch as here), profiles/tc_expert_kernel_kimi_decode_1row.md.
 # Valid for the kernel as captured; reset to None when the kernel changes.
-TC_TRAFFIC = 284543744
+TC_TRAFFIC = 284755200
 METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
 UNIT = "GB/s"
 L2_FLUSH_BYTES = 256 << 20
