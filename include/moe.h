@@ -76,6 +76,14 @@ extern "C" {
                                       SHARED_ONLY call on the same workspace this does
                                       the work of one plain call, e.g. split over two
                                       streams that join before moe_combine */
+#define MOE_MODE_AFTER_SHARED 0x800 /* with MOE_MODE_ROUTED_ONLY, for the call made
+                                      right after moe_shared_experts_after_route on
+                                      the same stream (which itself directly follows
+                                      moe_route): the routed experts' kernel does not
+                                      wait for the shared experts to complete before
+                                      it starts (its CTAs get SMs only as the shared
+                                      experts' CTAs leave, each of which has seen the
+                                      routing complete), only before it completes */
 
 /* weight formats of a pool */
 /* bits of a slot's ready flag (moe_expert_block's slot_ready; the device expert cache

@@ -29,6 +29,7 @@ MOE_SLOT_DOWN = 2
 MOE_SLOT_READY = 3
 MOE_MODE_SHARED_ONLY = 0x200
 MOE_MODE_ROUTED_ONLY = 0x400
+MOE_MODE_AFTER_SHARED = 0x800
 MOE_FMT_MXFP4 = 0
 MOE_FMT_Q8_0 = 1
 MOE_EPI_NONE = 0

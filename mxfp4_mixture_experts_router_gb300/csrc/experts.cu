@@ -1184,6 +1184,7 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     if (base_mode != MOE_MODE_DECODE && base_mode != MOE_MODE_PREFILL) return MOE_ERR_UNSUPPORTED;
     const bool only_shared = (mode & MOE_MODE_SHARED_ONLY) != 0, only_routed = (mode & MOE_MODE_ROUTED_ONLY) != 0;
     if (only_shared && only_routed) return MOE_ERR_INVALID_ARG;
+    if ((mode & MOE_MODE_AFTER_SHARED) && !only_routed) return MOE_ERR_INVALID_ARG;
     if (n_rows < 1 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
     if (base_mode == MOE_MODE_DECODE && n_rows > 16) return MOE_ERR_UNSUPPORTED;
     // blocks of more than 16 rows: routed experts on the block-scaled path only (the

@@ -94,6 +94,7 @@ struct Params {
     CUtensorMap s_dn;       // down scales {f/32, d rows, slot}
     int d, f, k, n_rows, n_shared, nk;
     int n_gu, n_dn, lag, debug;
+    int after_shared;  // launched right behind the shared experts that ran beside the routing
     const int* expert_slot;
     const uint32_t* slot_ready;
     int n_slots;
@@ -408,7 +409,7 @@ struct BStage {
 __device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row, const uint16_t* tok) {
     if (m.type != IT_GU) return m.brow + row;
     const int q = row / 3;
-    const int n = tok != nullptr ? (int)tok[m.p0 + q] : __ldg(p.pair + m.p0 + q) / p.k;
+    const int n = tok != nullptr ? (int)tok[m.p0 + q] : __ldcg(p.pair + m.p0 + q) / p.k;
     return 3 * n + (row - 3 * q);
 }
 
@@ -777,7 +778,7 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
                 if (col < r) {
                     const float y = __uint_as_float(v[3 * col]) + __uint_as_float(v[3 * col + 1]) +
                                     __uint_as_float(v[3 * col + 2]);
-                    const int pid = __ldg(p.pair + o0 + col);
+                    const int pid = __ldcg(p.pair + o0 + col);
                     p.y_part[(size_t)pid * p.d + m0 + m] = y;
                 }
             }
@@ -835,15 +836,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     // the set-up above overlaps the previous kernel on the stream; everything below
-    // reads the routing's results
-    griddep_wait();
+    // reads the routing's results.  Directly after the shared experts that ran beside
+    // the routing, this CTA only starts once a CTA of theirs has left its SM, and each
+    // of those leaves only after the routing has completed: no wait here (the acquire
+    // below drops stale L1 lines), and the wait for the shared experts is at the end.
+    if (!p.after_shared) griddep_wait();
     griddep_launch_dependents();
-    const int U = min((int)p.ctrl[CTRL_UNIQUE], C::MAX_U);
+    __shared__ int s_u;
+    if (tid == 0) s_u = (int)ld_acquire(p.ctrl + CTRL_UNIQUE);
+    __syncthreads();
+    const int U = min(s_u, C::MAX_U);
     // every expert's slot and pair range (all loads in flight at once), then the
     // prefix of its chunk counts (one warp: contiguous runs per lane, then a scan)
     for (int u = tid; u < U; u += NTHREADS) {
-        int z = __ldg(p.expert_slot + __ldg(p.uexp + u));
-        const int o0 = __ldg(p.off + u), r = __ldg(p.off + u + 1) - o0;
+        int z = __ldg(p.expert_slot + __ldcg(p.uexp + u));
+        const int o0 = __ldcg(p.off + u), r = __ldcg(p.off + u + 1) - o0;
         if (z < 0 || z >= p.n_slots) {
             set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
             z = 0;
@@ -851,7 +858,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         umeta[u] = make_uint2((uint32_t)z, (uint32_t)o0 | ((uint32_t)r << 16));
     }
     if (tok != nullptr)  // the block row of every pair (small blocks only)
-        for (int i = tid; i < p.nk && i < C::TOKS; i += NTHREADS) tok[i] = (uint16_t)(__ldg(p.pair + i) / p.k);
+        for (int i = tid; i < p.nk && i < C::TOKS; i += NTHREADS) tok[i] = (uint16_t)(__ldcg(p.pair + i) / p.k);
     __syncthreads();
     if (warp == 1) {
         const int lane = tid & 31, per = (U + 31) / 32, b0 = lane * per, b1 = min(U, b0 + per);
@@ -904,6 +911,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
             p.ctrl[CTRL_EXIT_TC] = 0;
         }
     }
+    if (p.after_shared && tid == 0) griddep_wait();  // complete only after the shared experts
 }
 
 // ---------------------------------------------------------------------------
@@ -1024,6 +1032,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.n_dn = d / 128;
     p.lag = 1 << 30;  // every gate/up item before the first down item
     p.debug = (mode & MOE_MODE_DEBUG_GU) ? 1 : 0;
+    p.after_shared = (mode & MOE_MODE_AFTER_SHARED) ? 1 : 0;
 
     p.expert_slot = expert_slot;
     p.slot_ready = slot_ready;

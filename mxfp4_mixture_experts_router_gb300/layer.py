@@ -155,7 +155,7 @@ class MoeLayer:
             self.shared_experts(n, x, after_route=True)
             if evs:
                 mark(evs[2])
-            self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY)
+            self.experts(n, mode=mode | B.MOE_MODE_ROUTED_ONLY | B.MOE_MODE_AFTER_SHARED)
         elif evs:
             self.experts(n, mode=mode | B.MOE_MODE_SHARED_ONLY)
             mark(evs[2])

@@ -69,6 +69,9 @@ def test_argument_errors_are_reported_before_any_launch(lib):
     pool = B.pool(256, 17547264 + 256 - 17547264 % 256, 1, B.MOE_FMT_MXFP4)
     assert L.moe_expert_block(ctypes.byref(kimi), 17, 0, ctypes.byref(pool), 256, None, None, 0, 256, 32, 256,
                               None) == B.MOE_ERR_UNSUPPORTED
+    # MOE_MODE_AFTER_SHARED only with MOE_MODE_ROUTED_ONLY
+    assert L.moe_expert_block(ctypes.byref(kimi), 1, B.MOE_MODE_AFTER_SHARED, ctypes.byref(pool), 256, None, None, 0,
+                              256, 16, 256, None) == B.MOE_ERR_INVALID_ARG
     # q8_0: SwiGLU needs the up matrix; K must be a multiple of 256
     assert L.q8_0_block_matmul(1, 7168, 64, 256, 0, 256, 256, None, None, B.MOE_EPI_SWIGLU, 256, 256, None) == \
         B.MOE_ERR_INVALID_ARG
