@@ -50,6 +50,8 @@ ROUTER_BYTES = 896 * 7168 * 2
 TC_TRAFFIC = 284755200
 METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
 UNIT = "GB/s"
+WORKLOAD = ("Kimi K3.1 MoE layer decode, 1 row/step: d=7168 f=1536 E=896 top-16 + 2 Q8_0 shared, "
+            "all experts resident, 100 seeded rows")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -328,8 +330,7 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "mxfp4 weights x f16 activations, fp32 accumulate, bf16 out", "data": "synthetic",
-        "config": {"workload": "Kimi K3.1 MoE layer decode, 1 row/step: d=7168 f=1536 E=896 top-16 + 2 Q8_0 "
-                               "shared, all experts resident, 100 seeded rows",
+        "config": {"workload": WORKLOAD,
                    "rows_per_step": 1,
                    "l2": "flushed before every step (256 MB write, then 256 MB read), outside the events",
                    "parallelism": f"replicas x{world}", "blocks_sigma0.5": blocks},
@@ -643,9 +644,10 @@ def run_reference(args):
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
             "steps": K, "warmup": W, "ms_per_step": total / K * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Kimi K3.1 MoE layer decode, 1 row/step (oracle sample)", "rows_per_step": 1},
+            "config": {"workload": WORKLOAD, "rows_per_step": 1},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "one (row, selected expert) fp64 expert MLP per step"},
+                             "sample": "each step one (row, selected expert) fp64 expert MLP of the workload "
+                                       "(17,547,264 expert bytes); the metric's unit scaled from it"},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
