@@ -280,7 +280,7 @@ __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t ta
 template <int NBM>
 __device__ void producer(const Params& p, int U, const uint2* umeta, const int* cp, unsigned char* smem,
                          unsigned char* scbuf, uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf,
-                         Meta* meta) {
+                         Meta* meta, int first) {
     using C = Cfg<NBM>;
     tma_prefetch_desc(&p.a_gu);
     tma_prefetch_desc(&p.a_dn);
@@ -292,7 +292,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
     uint32_t sc_any = 0u, sc_cnt = 0u;  // per scale buffer: armed at all, and the parity of its arm count
     bool ok = true;
     Plan cur, nxt;
-    plan_item(p, V, U, umeta, cp, (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u), total, cur);
+    plan_item(p, V, U, umeta, cp, first, total, cur);
     for (int seq = 0; ok && cur.item < total; seq++) {
         const int item = cur.item, type = cur.type, cid = cur.cid, blk = cur.blk, split = cur.split;
         const int z = cur.z, p0 = cur.p0, rc = cur.rc;
@@ -843,7 +843,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     if (!p.after_shared) griddep_wait();
     griddep_launch_dependents();
     __shared__ int s_u;
-    if (tid == 0) s_u = (int)ld_acquire(p.ctrl + CTRL_UNIQUE);
+    // the producer's first claim goes out now: its latency overlaps the loads below
+    int first = 0;
+    if (tid == 0) {
+        s_u = (int)ld_acquire(p.ctrl + CTRL_UNIQUE);
+        first = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
+    }
     __syncthreads();
     const int U = min(s_u, C::MAX_U);
     // every expert's slot and pair range (all loads in flight at once), then the
@@ -882,7 +887,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const uint32_t tbase = *tslot;
 
     if (warp == 0) {
-        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, meta);
+        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, meta, first);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
