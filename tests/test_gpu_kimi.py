@@ -120,3 +120,29 @@ def test_topk_ties_at_full_width(kimi):
         np.testing.assert_allclose(w[ok], orc.routing_weights(lg.astype(np.float64), want)[ok], rtol=2e-6,
                                    atol=1e-7)
         lay.layer.error_bits()  # the NaN row sets the NaN bit; read and clear it
+
+
+@pytest.mark.parametrize("n", [1, 4])
+def test_chained_layer_equals_sequential_calls(kimi, n):
+    """forward() chains route -> shared experts (beside the routing) -> routed experts
+    (MOE_MODE_AFTER_SHARED: started as the shared experts' CTAs leave) -> combine; the
+    same calls made one after another with plain waits give the same bits."""
+    lay, _, blocks = kimi
+    L = lay.layer
+    logits = blocks[2.0][:n]
+    x = syn.x_rows(SEED + 5, range(n), KIMI.d_model)
+    res = syn.x_rows(SEED + 5, range(n), KIMI.d_model, tag=syn.TAG_RESIDUAL)
+    chained = lay.run(x, res, logits=logits)
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.uint16)
+    rd = torch.from_numpy(np.ascontiguousarray(res).view(np.int16)).cuda().view(torch.uint16)
+    ld = torch.from_numpy(np.ascontiguousarray(logits, np.float32)).cuda()
+    L.out.zero_()
+    L.route(n, xd, logits_in=ld)
+    torch.cuda.synchronize()
+    L.experts(n)
+    torch.cuda.synchronize()
+    L.combine(n, rd)
+    torch.cuda.synchronize()
+    seq = L.out[:n].view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(chained["out"], seq)
+    assert L.error_bits() == 0
