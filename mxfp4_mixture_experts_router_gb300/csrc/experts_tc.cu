@@ -1,5 +1,5 @@
 // Block-scaled tensor-core path (tcgen05, kind::mxf8f6f4) for the routed MXFP4
-// experts of a decode block.
+// experts of a block (decode blocks and prefill).
 //
 // Pages: "Run Kimi 3.1 locally on one GPU": MXFP4 experts (section "One GPU,
 // three storage tiers"); a block reads each expert once for all its rows
@@ -35,9 +35,10 @@
 // tensor map) and the scales of a whole item arrive in one box into a per-item
 // buffer.  The small activation operand (rows of the block or of the expert's
 // pairs, from L2) and its scales are loaded by the scale-mover warps one stage
-// ahead into registers and written in the swizzled layout the MMA reads.  Every
-// expert's slot and pair range sit in shared memory (read by all threads at the
-// start), and the next item's claim is issued while the current item streams.
+// ahead into registers (two stages ahead into L1) and written in the swizzled
+// layout the MMA reads.  Every expert's slot and pair range sit in shared memory
+// (read by all threads at the start), and the next item's claim is issued and
+// decoded while the current item streams.
 #include "common.cuh"
 
 namespace moe {
