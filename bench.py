@@ -193,6 +193,23 @@ def cpu_baseline(n_pairs: int = 16):
 # GPU layer
 # ---------------------------------------------------------------------------
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (the slowest rank's time); the value itself on one
+    rank.  device: where the collective's tensor lives (the GPU for NCCL, CPU for gloo)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world: int, steps: int, bytes_per_step: float, max_total_ms: float) -> float:
+    """Whole-job throughput: every rank processed steps x bytes_per_step, timed by the
+    slowest rank (replicas: the units of all ranks over the max time)."""
+    return world * steps * bytes_per_step / (max_total_ms * 1e-3) / 1e9
+
+
 def build_layer(torch, dev):
     from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
     sh = syn.KIMI
@@ -278,14 +295,10 @@ def run_ours(args, rank, world):
             b_.record()
             torch.cuda.synchronize()
             kern_ms.append(a_.elapsed_time(b_))
-    total_ms = sum(layer_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(layer_ms), world, dev)
     U = syn.KIMI.top_k  # a single row selects 16 distinct experts
     unique_bytes = U * SLAB
-    value = world * K * unique_bytes / (total_ms * 1e-3) / 1e9
+    value = job_gbs(world, K, unique_bytes, total_ms)
     all_bytes = unique_bytes + 2 * Q8_SLAB + ROUTER_BYTES + 3 * syn.KIMI.d_model * 2
     # routed-expert kernel, algorithmic bytes of one launch: the unique experts' slabs,
     # the row's three E4M3 activation terms with their scales, the fp32 y_part rows
@@ -310,12 +323,8 @@ def run_ours(args, rank, world):
         if i >= W:
             e2e[i - W][1].record()
         torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * K * unique_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e), world, dev)
+    e2e_value = job_gbs(world, K, unique_bytes, e2e_ms)
 
     blocks = {}
     if not args.no_blocks:
