@@ -977,15 +977,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe initialisation of a function-local static)
+    static const EncodeTiledFn fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -1121,23 +1122,20 @@ static bool pool_maps(CUtensorMap* maps, Geom* gg /*[2]: gate/up, down*/, const 
 }
 
 static int sm_count() {
-    static int n = -1;
-    if (n < 0) {
-        int dev = 0;
+    static const int n = [] {
+        int dev = 0, v = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n = 0;
-    }
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            v = 0;
+        return v;
+    }();
     return n;
 }
 
 template <int FR, int FS, bool FAST>
 static int launch_variant(const ExParams& p, cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        if (kernel_smem_attrs(expert_kernel<FR, FS, FAST>, (int)EX_SMEM) != cudaSuccess) return MOE_ERR_CUDA;
-        attr = true;
-    }
+    static const cudaError_t attr = kernel_smem_attrs(expert_kernel<FR, FS, FAST>, (int)EX_SMEM);
+    if (attr != cudaSuccess) return MOE_ERR_CUDA;
     const int grid = sm_count() * EX_CTAS_PER_SM;
     if (grid <= 0) return MOE_ERR_CUDA;
     if (launch_chained(expert_kernel<FR, FS, FAST>, dim3(grid), dim3(EX_THREADS), EX_SMEM, stream, p) != cudaSuccess)
@@ -1198,7 +1196,7 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
 
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
-    static ExParams p;  // large (tensor maps); filled per call, copied into the launch
+    thread_local ExParams p;  // large (tensor maps); filled per call, copied into the launch
     memset(&p, 0, sizeof(p));
     if (!pool_maps(&p.map[0], &p.geom[0], routed, d, f)) return MOE_ERR_UNSUPPORTED;
     if (n_shared > 0 && !pool_maps(&p.map[6], &p.geom[2], shared, d, f)) return MOE_ERR_UNSUPPORTED;
@@ -1273,7 +1271,7 @@ static int shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* 
 
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
-    static ExParams p;
+    thread_local ExParams p;  // filled per call, copied into the launch
     memset(&p, 0, sizeof(p));
     if (!pool_maps(&p.map[6], &p.geom[2], shared, d, f)) return MOE_ERR_UNSUPPORTED;
     for (int i = 0; i < 6; i++) p.map[i] = p.map[6 + i];  // no routed experts in this launch
@@ -1400,7 +1398,7 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
 
     const Q8Ws L = q8_layout(n_rows, k_in);
     char* base = static_cast<char*>(ws);
-    static ExParams p;
+    thread_local ExParams p;  // filled per call, copied into the launch
     memset(&p, 0, sizeof(p));
     Geom g;
     if (!make_geom(g, MOE_FMT_Q8_0, swiglu, k_in, n_out)) return MOE_ERR_UNSUPPORTED;

@@ -929,15 +929,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe initialisation of a function-local static)
+    static const EncodeTiledFn fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult qr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
                 cudaSuccess &&
             qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
+            return reinterpret_cast<EncodeTiledFn>(ptr);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -961,11 +962,8 @@ static bool map_nd(CUtensorMap* m, CUtensorMapDataType type, const void* addr, i
 template <int NBM>
 static int launch(const Params& p, cudaStream_t stream) {
     using C = Cfg<NBM>;
-    static bool attr = false;
-    if (!attr) {
-        if (kernel_smem_attrs(tc_expert_kernel<NBM>, (int)C::SMEM) != cudaSuccess) return MOE_ERR_CUDA;
-        attr = true;
-    }
+    static const cudaError_t attr = kernel_smem_attrs(tc_expert_kernel<NBM>, (int)C::SMEM);
+    if (attr != cudaSuccess) return MOE_ERR_CUDA;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
@@ -998,7 +996,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
         return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
-    static Params p;
+    thread_local Params p;  // filled per call, copied into the launch
     memset(&p, 0, sizeof(p));
     // slab planes: [gate codes | gate scales | up codes | up scales | down codes | down scales]
     const char* pool = static_cast<const char*>(routed->base);

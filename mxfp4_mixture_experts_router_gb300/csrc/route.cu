@@ -982,11 +982,8 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     const int prep_ctas = (logits_in && x) ? n_rows * ((d + RT_CHUNK - 1) / RT_CHUNK) : n_rows;
     int grid = p.n_gemv_ctas > prep_ctas ? p.n_gemv_ctas : prep_ctas;
     const size_t smem = (size_t)RT_MAX_ROWS * 32 * 17 * 4;  // padded x slice (also covers the grouping tables)
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (kernel_smem_attrs(route_kernel, (int)smem) != cudaSuccess) return MOE_ERR_CUDA;
-        attr_set = true;
-    }
+    static const cudaError_t attr = kernel_smem_attrs(route_kernel, (int)smem);
+    if (attr != cudaSuccess) return MOE_ERR_CUDA;
     route_kernel<<<grid, RT_THREADS, smem, cs>>>(p);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
