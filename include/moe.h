@@ -200,30 +200,6 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
               void* ws, int32_t n_rows_max, int32_t n_shared, void* stream);
 
 /*
- * Every selected expert's SwiGLU MLP on the rows routed to it, plus the shared
- * experts on every row.  Pages: MXFP4 experts ("Run Kimi 3.1 locally on one
- * GPU", "One GPU, three storage tiers"), a block reads each expert once for
- * all its rows ("A drafter that leaves the answer unchanged"):
- *   g = x Wg^T, u = x Wu^T, h = silu(g) * u, y = h Wd^T   per (row, slot)
- * Each expert's slab is streamed from HBM once per call.  Must follow
- * moe_route on the same workspace and stream.
- *
- *  mode         MOE_MODE_DECODE (n_rows <= 16) or MOE_MODE_PREFILL, optionally
- *               | MOE_MODE_DEBUG_GU, and at most one of MOE_MODE_SHARED_ONLY /
- *               MOE_MODE_ROUTED_ONLY (both: MOE_ERR_INVALID_ARG)
- *  routed       pool holding the routed experts (host struct, MXFP4)
- *  expert_slot  int32 [E] slot of each expert in `routed` (device)
- *  slot_ready   uint32 [routed->n_slots] flags, or NULL when every slot is
- *               resident: an expert's gate/up planes are read only after its
- *               flag has MOE_SLOT_GATE_UP, its down planes only after it has
- *               MOE_SLOT_DOWN (bounded waits; MOE_EBIT_TIMEOUT when one runs
- *               out); a resident slot holds MOE_SLOT_READY
- *  shared       pool of n_shared Q8_0 shared experts in slots 0..n_shared-1,
- *               or NULL with n_shared == 0
- *  y_part       fp32 [n_rows][k][d] output of each (row, slot)
- *  The shared experts' outputs go to the workspace (moe_ws_offsets.shared_y).
- */
-/*
  * The shared experts alone, straight from the block's rows: they depend on x
  * only, not on the routing ("Run Kimi K3 and K3.1 Pro Locally": every token
  * also runs the 2 shared experts; their matmuls load each weight once for all
@@ -254,6 +230,33 @@ MOE_API int moe_shared_experts_after_route(const moe_desc* desc, int32_t n_rows,
                        const moe_pool* shared, int32_t n_shared,
                        void* ws, int32_t n_rows_max, void* stream);
 
+/*
+ * Every selected expert's SwiGLU MLP on the rows routed to it, plus the shared
+ * experts on every row.  Pages: MXFP4 experts ("Run Kimi 3.1 locally on one
+ * GPU", "One GPU, three storage tiers"), a block reads each expert once for
+ * all its rows ("A drafter that leaves the answer unchanged"):
+ *   g = x Wg^T, u = x Wu^T, h = silu(g) * u, y = h Wd^T   per (row, slot)
+ * Each expert's slab is streamed from HBM once per call.  Must follow
+ * moe_route on the same workspace and stream.
+ *
+ *  mode         MOE_MODE_DECODE (n_rows <= 16) or MOE_MODE_PREFILL, optionally
+ *               | MOE_MODE_DEBUG_GU, and at most one of MOE_MODE_SHARED_ONLY /
+ *               MOE_MODE_ROUTED_ONLY (both: MOE_ERR_INVALID_ARG); with
+ *               MOE_MODE_ROUTED_ONLY, | MOE_MODE_AFTER_SHARED for the call right
+ *               after moe_shared_experts_after_route (without ROUTED_ONLY:
+ *               MOE_ERR_INVALID_ARG)
+ *  routed       pool holding the routed experts (host struct, MXFP4)
+ *  expert_slot  int32 [E] slot of each expert in `routed` (device)
+ *  slot_ready   uint32 [routed->n_slots] flags, or NULL when every slot is
+ *               resident: an expert's gate/up planes are read only after its
+ *               flag has MOE_SLOT_GATE_UP, its down planes only after it has
+ *               MOE_SLOT_DOWN (bounded waits; MOE_EBIT_TIMEOUT when one runs
+ *               out); a resident slot holds MOE_SLOT_READY
+ *  shared       pool of n_shared Q8_0 shared experts in slots 0..n_shared-1,
+ *               or NULL with n_shared == 0
+ *  y_part       fp32 [n_rows][k][d] output of each (row, slot)
+ *  The shared experts' outputs go to the workspace (moe_ws_offsets.shared_y).
+ */
 MOE_API int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mode,
                      const moe_pool* routed, const int32_t* expert_slot,
                      const uint32_t* slot_ready,
