@@ -310,16 +310,29 @@ MOE_API int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out,
  * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress); make that first call before any stream
- * capture.  Every call shares the one array: the call clears the parts that
- * must start at zero, but calls that overlap on the GPU (different streams,
- * or different host threads on one device) race on it and must be serialised
- * by the caller.
+ * capture.  The address is kept per device together with the context it
+ * belongs to: after a device reset (or any new primary context) the next call
+ * looks it up again, so make that call outside a capture too.  Every call
+ * shares the one array: the call clears the parts that must start at zero, but
+ * calls that overlap on the GPU (different streams, or different host threads
+ * on one device) race on it and must be serialised by the caller.  Device-side
+ * errors (a bounded wait that ran out) accumulate in the array's error word
+ * across calls; read and clear them with q8_0_noalloc_get_error.
  */
 MOE_API int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n_out,
                                       const void* x, int32_t x_dtype,
                                       const int8_t* q, const uint16_t* d,
                                       const int8_t* q2, const uint16_t* d2,
                                       int32_t epilogue, float* y, void* stream);
+
+/*
+ * The device error word (MOE_EBIT_* bits) of q8_0_block_matmul_noalloc's static
+ * array on the current device: every bit its calls set since the last read.
+ * Synchronises `stream`, returns the word through *bits (host) and clears it.
+ * Allocates nothing.  Returns MOE_OK, MOE_ERR_INVALID_ARG (bits NULL) or
+ * MOE_ERR_CUDA.  Like the matmul call, it has no counterpart on the pages.
+ */
+MOE_API int q8_0_noalloc_get_error(void* stream, uint32_t* bits);
 
 /*
  * Reads the workspace's device error word (synchronising `stream`), clears it,

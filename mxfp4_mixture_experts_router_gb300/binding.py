@@ -43,7 +43,7 @@ MOE_CACHE_KEEP_MULTI_ROW = 1
 EXPORTED = [
     "moe_slab_bytes", "moe_workspace_size", "moe_workspace_offsets", "moe_route", "moe_expert_block",
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
-    "q8_0_block_matmul_noalloc", "moe_shared_experts", "moe_shared_experts_after_route",
+    "q8_0_block_matmul_noalloc", "q8_0_noalloc_get_error", "moe_shared_experts", "moe_shared_experts_after_route",
     "moe_cache_create", "moe_cache_request", "moe_cache_stats_get", "moe_cache_sync", "moe_cache_destroy",
 ]
 
@@ -108,6 +108,7 @@ def lib() -> ctypes.CDLL:
         L.q8_0_workspace_size.restype = SZ
         L.q8_0_block_matmul.argtypes = [I32, I32, I32, P, I32, P, P, P, P, I32, P, P, P]
         L.q8_0_block_matmul_noalloc.argtypes = [I32, I32, I32, P, I32, P, P, P, P, I32, P, P]
+        L.q8_0_noalloc_get_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_get_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_device_sm_count.restype = I32
         _LIB = L
@@ -211,6 +212,14 @@ def q8_0_block_matmul_noalloc(n_rows: int, k_in: int, n_out: int, x, x_dtype: in
     _check(lib().q8_0_block_matmul_noalloc(n_rows, k_in, n_out, _ptr(x), x_dtype, _ptr(q), _ptr(dq), _ptr(q2),
                                            _ptr(d2), epilogue, _ptr(y), _stream(stream)),
            "q8_0_block_matmul_noalloc")
+
+
+def q8_0_noalloc_get_error(stream=None) -> int:
+    """Device error bits collected by q8_0_block_matmul_noalloc calls on the current
+    device since the last read (read and cleared)."""
+    bits = ctypes.c_uint32(0)
+    _check(lib().q8_0_noalloc_get_error(_stream(stream), ctypes.byref(bits)), "q8_0_noalloc_get_error")
+    return bits.value
 
 
 def moe_get_error(ws, stream=None) -> int:

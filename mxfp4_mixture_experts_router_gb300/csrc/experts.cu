@@ -27,6 +27,8 @@
 // * A row's arithmetic never depends on the other rows of the block: K is
 //   always reduced in the same order, the row's tensor-core column does not
 //   change its result, and scale exponents are per row.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -1475,9 +1477,56 @@ constexpr int Q8_NOALLOC_MAX_DEVICES = 64;
 
 static __device__ __align__(256) unsigned char q8_noalloc_scratch[Q8_NOALLOC_BYTES];
 
-// Device address of the scratch array on each device (looked up once per
-// device, with that device current; the symbol name is only a host stand-in).
-static void* q8_noalloc_addr[Q8_NOALLOC_MAX_DEVICES];
+// Device address of the scratch array on each device, looked up with that device
+// current (in host code the symbol's name is only a stand-in, not a device
+// address).  The address belongs to the context it was looked up in: a device
+// reset or a new primary context makes it stale, so the context is kept beside it
+// and a change of context repeats the lookup.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+static CtxGetCurrentFn ctx_get_current_fn() {
+    static const CtxGetCurrentFn fn = [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            return reinterpret_cast<CtxGetCurrentFn>(ptr);
+        return static_cast<CtxGetCurrentFn>(nullptr);
+    }();
+    return fn;
+}
+
+struct NoallocSlot {
+    std::mutex m;
+    CUcontext ctx = nullptr;
+    void* addr = nullptr;
+};
+static NoallocSlot q8_noalloc_slot[Q8_NOALLOC_MAX_DEVICES];
+
+// The scratch array's device address on the current device (nullptr on failure).
+static unsigned char* q8_noalloc_scratch_addr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= Q8_NOALLOC_MAX_DEVICES) return nullptr;
+    CtxGetCurrentFn get_ctx = ctx_get_current_fn();
+    CUcontext ctx = nullptr;
+    if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS) return nullptr;
+    if (ctx == nullptr) {
+        // no context current on this thread yet: the symbol lookup makes the
+        // device's primary context current
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, q8_noalloc_scratch) != cudaSuccess) return nullptr;
+        if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr) return nullptr;
+    }
+    NoallocSlot& slot = q8_noalloc_slot[dev];
+    std::lock_guard<std::mutex> lock(slot.m);
+    if (slot.ctx != ctx || slot.addr == nullptr) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, q8_noalloc_scratch) != cudaSuccess || addr == nullptr) return nullptr;
+        slot.ctx = ctx;
+        slot.addr = addr;
+    }
+    return static_cast<unsigned char*>(slot.addr);
+}
 
 extern "C" int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n_out, const void* x,
                                          int32_t x_dtype, const int8_t* q, const uint16_t* dq, const int8_t* q2,
@@ -1486,19 +1535,27 @@ extern "C" int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n
         return MOE_ERR_UNSUPPORTED;
     const Q8Ws L = q8_layout(n_rows, k_in);
     if (L.total > Q8_NOALLOC_BYTES) return MOE_ERR_UNSUPPORTED;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= Q8_NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED;
-    if (q8_noalloc_addr[dev] == nullptr) {
-        void* addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, q8_noalloc_scratch) != cudaSuccess || addr == nullptr) return MOE_ERR_CUDA;
-        q8_noalloc_addr[dev] = addr;
-    }
-    unsigned char* ws = static_cast<unsigned char*>(q8_noalloc_addr[dev]);
+    unsigned char* ws = q8_noalloc_scratch_addr();
+    if (ws == nullptr) return MOE_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // the array keeps the previous call's contents: clear the control words and
-    // the gate/up completion counter, which the kernel expects to start at zero
-    if (cudaMemsetAsync(ws + L.ctrl, 0, CTRL_WORDS * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the array keeps the previous call's contents: clear the control words after the
+    // error word (which collects the device errors of every call until
+    // q8_0_noalloc_get_error reads and clears it) and the gate/up completion counter,
+    // which the kernel expects to start at zero
+    if (cudaMemsetAsync(ws + L.ctrl + 4 * (CTRL_ERROR + 1), 0, (CTRL_WORDS - CTRL_ERROR - 1) * 4, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     if (cudaMemsetAsync(ws + L.gu_done, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     return q8_0_block_matmul(n_rows, k_in, n_out, x, x_dtype, q, dq, q2, d2, epilogue, y, ws, stream);
+}
+
+extern "C" int q8_0_noalloc_get_error(void* stream, uint32_t* bits) {
+    if (!bits) return MOE_ERR_INVALID_ARG;
+    unsigned char* ws = q8_noalloc_scratch_addr();
+    if (ws == nullptr) return MOE_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* word = reinterpret_cast<uint32_t*>(ws) + CTRL_ERROR;  // the control block starts the array
+    if (cudaMemcpyAsync(bits, word, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(word, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -21,7 +21,7 @@ Everything here is plain numpy in float64, written step by step from the pages:
   checkpoint, here carried as a BF16 router and Q8_0 shared experts, since the
   first page quantises the whole non-expert spine to Q8_0).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the pages give the formats and counts, not these steps):
 
 * Router function: softmax over the router logits, the k largest kept, their
   probabilities renormalised to sum to 1 (routed scaling 1).  Selection is done

@@ -1,14 +1,15 @@
 """Device expert cache on the GPU: blocks of several layers run with their routed
 experts served from a small cache (fewer slots than the experts they touch, so
 slots are evicted and re-uploaded while the kernels run) give bit-for-bit the
-outputs of the same layers with every slab resident."""
+outputs of the same layers with every slab resident, and the first and last
+blocks also match the CPU oracle on the same expert bodies."""
 
 import numpy as np
 import pytest
 import torch
 
 import moe_synth as syn
-from gpu_util import ensure_built, to_dev_u16
+from gpu_util import assert_close_to_oracle, ensure_built, to_dev_u16
 from mxfp4_mixture_experts_router_gb300 import binding as B
 from mxfp4_mixture_experts_router_gb300.cache import DeviceExpertCache
 from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
@@ -65,6 +66,10 @@ def run_case(shape, n_bodies, n_slots, n_rows, n_layers, n_blocks, policy, seed)
             assert lay.error_bits() == 0
             assert torch.equal(got, ref), blk
             assert torch.equal(lay.y_part[:n_rows], ref_y), blk
+            if blk in (0, n_blocks - 1):
+                # the cached layer against the oracle on the same bodies and logits
+                o = orc.moe_layer(x, x, shape, lambda e, l=layer: slabs[body_of(l, e, n_bodies)], logits=logits)
+                assert_close_to_oracle(got.view(torch.int16).cpu().numpy().view(np.uint16), o, f"cached block {blk}")
         cache.sync()
         st = cache.stats()
         assert st["misses"] == uploads and st["evictions"] > 0 and st["hits"] > 0

@@ -66,17 +66,23 @@ def test_verification_block_rows_equal_single_rows(kimi, sigma):
             assert np.array_equal(one["y"][0].view(np.uint32), blk["y"][r].view(np.uint32)), (n, r)
 
 
-def test_verification_block_matches_oracle(kimi):
+@pytest.mark.parametrize("sigma,rows", [(0.5, [0, 15]), (0.1, list(range(16))), (2.0, list(range(16)))])
+def test_verification_block_matches_oracle(kimi, sigma, rows):
+    """16-row verification blocks (the 48-column configuration) against the oracle:
+    every row at sigma 0.1 (about 24 experts, up to 16 rows each) and 2.0 (about 188
+    experts, mostly one row each), two rows at 0.5."""
     lay, _, blocks = kimi
-    logits = blocks[0.5]
+    logits = blocks[sigma]
     x = syn.x_rows(SEED + 2, range(16), KIMI.d_model)
     res = syn.x_rows(SEED + 2, range(16), KIMI.d_model, tag=syn.TAG_RESIDUAL)
     g = lay.run(x, res, logits=logits)
-    rows = [0, 15]
     o = lay.oracle(x[rows], res[rows], logits=logits[rows])
+    assert np.array_equal(g["idx"][rows], o["idx"])
     for i, r in enumerate(rows):
         one = {"out": o["out"][i:i + 1], "out_bf16": o["out_bf16"][i:i + 1]}
-        assert_close_to_oracle(g["out"][r:r + 1], one, f"kimi block row {r}")
+        assert_close_to_oracle(g["out"][r:r + 1], one, f"kimi block sigma {sigma} row {r}")
+        rel_y = np.linalg.norm(g["y"][r] - o["y"][i]) / np.linalg.norm(o["y"][i])
+        assert rel_y < 1e-3, (sigma, r, rel_y)
 
 
 def _route_only(lay, logits):

@@ -59,6 +59,8 @@ def test_noalloc_matches_allocating_entry_point_on_consecutive_calls():
     h = torch.from_numpy(np.random.default_rng(32).standard_normal((16, f)).astype(np.float32) * 1e4).cuda()
     got, want = _both(16, f, d, h, B.MOE_DTYPE_F32, *w["down"], None, None, B.MOE_EPI_NONE)
     _close(got, want)
+    # no device-side error in either call (the error word collects them until read)
+    assert B.q8_0_noalloc_get_error() == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
