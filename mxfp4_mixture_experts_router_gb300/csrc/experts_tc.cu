@@ -292,15 +292,26 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
     uint32_t stage = 0, phase = 0, pending = 0, pending_par = 0;
     uint32_t sc_any = 0u, sc_cnt = 0u;  // per scale buffer: armed at all, and the parity of its arm count
     bool ok = true;
+    // Claims run two items ahead: the claim of the item after next goes out at the
+    // first stage of the current item and is decoded one item later, so neither the
+    // atomic's round trip nor the next item's dependency load (issued right after its
+    // decoding) waits in line with the stages.
     Plan cur, nxt;
     plan_item(p, V, U, umeta, cp, first, total, cur);
+    int claim_next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
+    uint32_t dep_cur = 0u;  // the current item's dependency word as last read
+    if (cur.item < total) {
+        if (p.slot_ready != nullptr) dep_cur = ld_acquire(p.slot_ready + cur.z);
+        else if (cur.type != IT_GU) dep_cur = ld_acquire(p.gu_done + cur.cid);
+    }
     for (int seq = 0; ok && cur.item < total; seq++) {
         const int item = cur.item, type = cur.type, cid = cur.cid, blk = cur.blk, split = cur.split;
         const int z = cur.z, p0 = cur.p0, rc = cur.rc;
         const bool gu = type == IT_GU;
         // gate/up items need the slot's gate/up planes (bit 0), down items its down planes (bit 1)
-        if (p.slot_ready != nullptr) ok = wait_bits(p, p.slot_ready + z, gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN);
-        if (ok && !gu) {
+        if (p.slot_ready != nullptr && (dep_cur & (gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN)) == 0u)
+            ok = wait_bits(p, p.slot_ready + z, gu ? MOE_SLOT_GATE_UP : MOE_SLOT_DOWN);
+        if (ok && !gu && (p.slot_ready != nullptr || dep_cur < (uint32_t)p.n_gu)) {
             // the chunk's SwiGLU activations must be complete before the scale movers
             // read them (they read this item's stages only after its claim below)
             ok = wait_at_least(p, p.gu_done + cid, (uint32_t)p.n_gu);
@@ -318,7 +329,8 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
         // an unpacked 4-bit code box counts its packed (global) bytes: half its shared-memory size
         const uint32_t tx = (uint32_t)(A_BYTES / 2);
         const uint32_t tx_sc = (uint32_t)(128 * sc);
-        int next = total;
+        int claim_after = total;
+        uint32_t dep_nxt = 0u;
         nxt.item = total;
         for (int c = 0; c < nch; c++) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -370,13 +382,20 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
                 stage = 0;
                 phase ^= 1u;
             }
-            // the next claim, issued now and decoded a few stages later: its latency
-            // and the decoding hide behind this item's stages (every item has at least
-            // NST >= 4 stages)
-            if (c == 0) next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
-            if (c == 3) plan_item(p, V, U, umeta, cp, next, total, nxt);
+            if (c == 0) {
+                // the claim two items ahead, and the decoding of the next item (claimed
+                // one item ago) with its dependency load, which lands during this item
+                claim_after = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
+                plan_item(p, V, U, umeta, cp, claim_next, total, nxt);
+                if (nxt.item < total) {
+                    if (p.slot_ready != nullptr) dep_nxt = ld_acquire(p.slot_ready + nxt.z);
+                    else if (nxt.type != IT_GU) dep_nxt = ld_acquire(p.gu_done + nxt.cid);
+                }
+            }
         }
         cur = nxt;
+        claim_next = claim_after;
+        dep_cur = dep_nxt;
     }
     // tell the consumers there is nothing more (after an error too, if a stage frees up)
     if (mbar_wait(&empty[stage], phase ^ 1u)) {
