@@ -31,6 +31,12 @@ import sys
 import threading
 import time
 
+if "reference" in sys.argv[sys.argv.index("--impl") + 1:sys.argv.index("--impl") + 2] if "--impl" in sys.argv else False:
+    # the reference arm (the CPU oracle) runs on one core: single-threaded BLAS, set
+    # before numpy loads it
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = "1"
+
 import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -43,15 +49,12 @@ N_ROWS_SEEDED = 100
 SLAB = 17547264
 Q8_SLAB = 35094528
 ROUTER_BYTES = 896 * 7168 * 2
-# DRAM bytes (read + write) of one routed-expert kernel launch on this workload:
-# dram__bytes_read.sum + dram__bytes_write.sum of an ncu capture of the profile case
-# (one row, the same 16 experts per launch as here), profiles/tc_expert_kernel_kimi_decode_1row.md.
-# Valid for the kernel as captured; reset to None when the kernel changes.
-TC_TRAFFIC = 284755200
 METRIC = "MoE-layer HBM GB/s on unique MXFP4 expert bytes; layer µs at 1/8/16 rows"
 UNIT = "GB/s"
 WORKLOAD = ("Kimi K3.1 MoE layer decode, 1 row/step: d=7168 f=1536 E=896 top-16 + 2 Q8_0 shared, "
-            "all experts resident, 100 seeded rows")
+            "all experts resident, rows drawn in turn from 100 seeded rows")
+DTYPE = ("mxfp4 weights x 5-term E2M1 (MX) activations on tcgen05 (routed experts), int8 x f16 activations "
+         "on mma.sync (shared experts), fp32 accumulate, bf16 out")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -142,8 +145,63 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle sample (the baseline), run in a single-threaded subprocess
+# CPU oracle sample (the baseline): whole layer rows through the oracle, in
+# spawned worker processes with single-threaded BLAS
 # ---------------------------------------------------------------------------
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu or /proc/cpuinfo), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _oracle_row_worker(row, barrier, queue):
+    """One seeded row of the 1-row Kimi decode workload through the whole oracle layer
+    (router GEMV, top-16, 16 MXFP4 experts, 2 Q8_0 shared experts, combine).  Input
+    creation (the row's expert slabs) happens before the barrier and is not timed."""
+    from oracle import moe_oracle as orc
+    sh = syn.KIMI
+    router = syn.router_weight(SEED, sh)
+    x = syn.x_rows(SEED, [row], sh.d_model)
+    lo = orc.router_logits(x, router)
+    sel = orc.select_topk(lo.astype(np.float32).astype(np.float64), sh.top_k)[0]
+    slabs = {int(e): syn.mxfp4_expert_slab(SEED, int(e), sh) for e in sel}
+    shared = [syn.q8_0_shared_slab(SEED, s, sh) for s in range(2)]
+    barrier.wait()
+    t0 = time.perf_counter()
+    orc.moe_layer(x, x, sh, lambda e: slabs[e], router_w_bits=router, shared_slabs=shared)
+    queue.put((row, time.perf_counter() - t0))
+
+
+def oracle_layer_rows(rows):
+    """Times the oracle on the given rows, one spawned process per row, all started
+    together after their inputs exist.  Returns (unique expert bytes / s, wall s)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(len(rows))
+    queue = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_row_worker, args=(r, barrier, queue)) for r in rows]
+    for pr in procs:
+        pr.start()
+    times = [queue.get(timeout=900)[1] for _ in rows]
+    for pr in procs:
+        pr.join()
+    wall = max(times)
+    return len(rows) * syn.KIMI.top_k * SLAB / wall / 1e9, wall
+
 
 def oracle_pairs(n_pairs: int, start: int = 0):
     """(row, expert) pairs of the workload in order: the experts each seeded row's
@@ -176,17 +234,27 @@ def oracle_step_seconds(pairs):
     return times
 
 
-def cpu_baseline(n_pairs: int = 16):
+def cpu_baseline(all_cores: int):
+    """The oracle on this host's cores: 1 core (two rows one after the other) and all
+    cores (one row per core, concurrently), single-threaded BLAS in every process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-sample", str(n_pairs)],
-                       capture_output=True, text=True, env=env, timeout=900)
-    if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-300:]}
-    secs = json.loads(r.stdout.strip().splitlines()[-1])["seconds"]
-    return {"value": n_pairs * SLAB / sum(secs) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n_pairs} (row, expert) pairs of the 1-row Kimi decode workload: fp64 slab decode + "
-                      f"SwiGLU expert MLP per pair, {sum(secs):.1f} s; router, shared experts and combine "
-                      f"(<25% of the bytes) not in the sample"}
+    res = {}
+    for cores, rows in ((1, "0"), (all_cores, ",".join(str(r) for r in range(all_cores)))):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-rows", rows],
+                           capture_output=True, text=True, env=env, timeout=1800)
+        if r.returncode != 0:
+            res[cores] = {"error": r.stderr[-300:]}
+            continue
+        res[cores] = json.loads(r.stdout.strip().splitlines()[-1])
+    one = res.get(1, {})
+    allc = res.get(all_cores, {})
+    return {"value": allc.get("gbs"), "unit": UNIT, "cores": all_cores, "kind": "oracle",
+            "cpu": cpu_model(),
+            "one_core": {"value": one.get("gbs"), "cores": 1, "seconds": one.get("seconds")},
+            "sample": f"whole 1-row layers of the Kimi decode workload (router GEMV, top-16, 16 MXFP4 experts, "
+                      f"2 Q8_0 shared experts, combine) in float64: {all_cores} rows at once on {all_cores} cores "
+                      f"({allc.get('seconds')} s), and 1 row on 1 core; value = unique expert bytes "
+                      f"(16 x 17,547,264 per row) / time"}
 
 
 # ---------------------------------------------------------------------------
@@ -225,10 +293,31 @@ def build_layer(torch, dev):
     return lay
 
 
+class Timeline:
+    """The layer's kernel timeline in its workspace (first CTA start and last CTA end of
+    the routing, shared-expert and routed-expert kernels, written by the kernels
+    themselves): zeroed before a step, read after it."""
+
+    def __init__(self, torch, lay):
+        self.words = lay.ws[lay.offsets.timeline: lay.offsets.timeline + 64]
+
+    def zero_(self):
+        self.words.zero_()
+
+    def spans_us(self):
+        w = self.words.cpu().numpy().view(np.uint64)
+        out = {}
+        for k, name in enumerate(("route", "shared_experts", "routed_experts")):
+            start_inv, end = int(w[2 * k]), int(w[2 * k + 1])
+            if start_inv and end:
+                start = (~start_inv) & ((1 << 64) - 1)
+                out[name] = ((start, end), (end - start) / 1e3)
+        return out
+
+
 def run_ours(args, rank, world):
     import torch
 
-    from mxfp4_mixture_experts_router_gb300 import binding as B
     from mxfp4_mixture_experts_router_gb300 import build as build_mod
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -236,30 +325,28 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", local)
     build_mod.build()
     lay = build_layer(torch, dev)
-    stream = torch.cuda.current_stream()
     xs = syn.x_rows(SEED, range(N_ROWS_SEEDED), syn.KIMI.d_model)
     X = torch.from_numpy(xs.view(np.int16)).to(dev).view(torch.uint16)
-    flusher = L2Flush(torch, dev)
-    flush = flusher
+    flush = L2Flush(torch, dev)
+    tl = Timeline(torch, lay)
     K, W = args.steps, args.warmup
 
-    # one captured graph per step: route -> experts -> combine, timing events inside
+    # one captured graph per step: route -> shared experts -> routed experts -> combine
     Xs = torch.empty((1, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
     Xs.copy_(X[:1])
-    graph, gev = lay.capture(Xs, Xs, events=True)
+    graph, _ = lay.capture(Xs, Xs)
     for i in range(W):
         flush.zero_()
         Xs.copy_(X[i % N_ROWS_SEEDED: i % N_ROWS_SEEDED + 1])
         graph.replay()
     torch.cuda.synchronize()
     assert lay.error_bits() == 0
-    gev = timeable(gev)
 
     props = torch.cuda.get_device_properties(dev)
     bus = getattr(props, "pci_bus_id", None)
     sampler = ClockSampler(bus if isinstance(bus, str) else None)
-    layer_ms, kern_ms, seg_ms = [], [], []
-    outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    layer_ms, spans = [], []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -268,45 +355,44 @@ def run_ours(args, rank, world):
     for i in range(K):
         r = (W + i) % N_ROWS_SEEDED
         flush.zero_()
+        tl.zero_()
         Xs.copy_(X[r: r + 1])
-        outer[i][0].record()
+        ev[i][0].record()
         graph.replay()
-        outer[i][1].record()
+        ev[i][1].record()
         torch.cuda.synchronize()
-        if gev is not None:
-            layer_ms.append(gev[0].elapsed_time(gev[4]))
-            kern_ms.append(gev[2].elapsed_time(gev[3]))
-            seg_ms.append([gev[i].elapsed_time(gev[i + 1]) for i in range(4)])
-        else:
-            layer_ms.append(outer[i][0].elapsed_time(outer[i][1]))
+        layer_ms.append(ev[i][0].elapsed_time(ev[i][1]))
+        spans.append(tl.spans_us())
     wall = time.perf_counter() - t_wall
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
     assert lay.error_bits() == 0
-    if not kern_ms:  # no events inside the graph: time the routed-expert kernel on its own
-        for i in range(K):
-            flush.zero_()
-            lay.route(1, Xs)
-            lay.experts(1, mode=B.MOE_MODE_SHARED_ONLY)
-            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_.record()
-            lay.experts(1, mode=B.MOE_MODE_ROUTED_ONLY)
-            b_.record()
-            torch.cuda.synchronize()
-            kern_ms.append(a_.elapsed_time(b_))
     total_ms = max_over_ranks(sum(layer_ms), world, dev)
     U = syn.KIMI.top_k  # a single row selects 16 distinct experts
     unique_bytes = U * SLAB
     value = job_gbs(world, K, unique_bytes, total_ms)
     all_bytes = unique_bytes + 2 * Q8_SLAB + ROUTER_BYTES + 3 * syn.KIMI.d_model * 2
     # routed-expert kernel, algorithmic bytes of one launch: the unique experts' slabs,
-    # the row's three E4M3 activation terms with their scales, the fp32 y_part rows
+    # the row's MX_TERMS packed E2M1 activation terms with their scales, the fp32 y_part rows
     d_ = syn.KIMI.d_model
-    kern_bytes = unique_bytes + 3 * (d_ + d_ // 32) + U * d_ * 4
-    kern_avg_s = statistics.mean(kern_ms) * 1e-3
+    kern_bytes = unique_bytes + 5 * (d_ // 2 + d_ // 32) + U * d_ * 4
+    kern_us = [sp["routed_experts"][1] for sp in spans if "routed_experts" in sp]
+    kern_avg_s = statistics.mean(kern_us) * 1e-6
     peak, peak_kind = load_peaks()
     achieved = kern_bytes / kern_avg_s / 1e9
+
+    def seg(name):
+        v = [sp[name][1] for sp in spans if name in sp]
+        return round(statistics.median(v), 2) if v else None
+
+    t0s = [min(v[0][0] for v in sp.values()) for sp in spans if sp]
+    offsets = {}
+    for name in ("route", "shared_experts", "routed_experts"):
+        st = [sp[name][0][0] - t for sp, t in zip(spans, t0s) if name in sp]
+        en = [sp[name][0][1] - t for sp, t in zip(spans, t0s) if name in sp]
+        if st:
+            offsets[name] = [round(statistics.median(st) / 1e3, 2), round(statistics.median(en) / 1e3, 2)]
 
     # end to end through the public API: pinned host row -> graph replay -> pinned host output
     xh = torch.from_numpy(xs.view(np.int16)).view(torch.uint16).pin_memory()
@@ -326,69 +412,90 @@ def run_ours(args, rank, world):
     e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e), world, dev)
     e2e_value = job_gbs(world, K, unique_bytes, e2e_ms)
 
-    blocks = {}
-    if not args.no_blocks:
-        blocks["1"] = {"us_median": statistics.median(layer_ms) * 1e3, "unique_experts": U,
-                       "gbs_unique": unique_bytes / statistics.median(layer_ms) / 1e6,
-                       "gbs_all_bytes": all_bytes / statistics.median(layer_ms) / 1e6,
-                       "routing": "router GEMV"}
-        for n in (8, 16):
-            blocks[str(n)] = time_blocks(torch, lay, X, flush, n, reps=max(5, min(K, 20)))
+    # warm L2 (no flush between steps), labelled as such
+    warm = []
+    for i in range(max(K, 10)):
+        r = i % N_ROWS_SEEDED
+        Xs.copy_(X[r: r + 1])
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record()
+        graph.replay()
+        b_.record()
+        torch.cuda.synchronize()
+        warm.append(a_.elapsed_time(b_))
 
+    med = statistics.median(layer_ms)
+    blocks = {"1": {"us_median": med * 1e3, "unique_experts": U, "gbs_unique": unique_bytes / med / 1e6,
+                    "frac_unique": round(unique_bytes / med / 1e6 / peak, 4),
+                    "gbs_all_bytes": all_bytes / med / 1e6, "routing": "router GEMV"}}
+    if not args.no_blocks:
+        for sigma in (0.1, 0.5, 2.0):
+            for n in (2, 4, 8, 16):
+                blocks[f"{n}@{sigma}"] = time_blocks(torch, lay, X, flush, n, sigma, reps=args.block_reps, peak=peak)
+
+    traffic, traffic_note = measured_traffic()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 weights x f16 activations, fp32 accumulate, bf16 out", "data": "synthetic",
-        "config": {"workload": WORKLOAD,
+        "dtype": DTYPE, "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows_timed": K,
                    "rows_per_step": 1,
                    "l2": "flushed before every step (256 MB write, then 256 MB read), outside the events",
-                   "parallelism": f"replicas x{world}", "blocks_sigma0.5": blocks},
+                   "parallelism": f"replicas x{world}"},
         "layer_us_p10_p50_p90": [float(np.percentile(layer_ms, q)) * 1e3 for q in (10, 50, 90)],
+        "layer_us_warm_l2_median": round(statistics.median(warm) * 1e3, 2),
         "all_bytes_gbs": world * K * all_bytes / (total_ms * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": TC_TRAFFIC,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "moe::tc::tc_expert_kernel", "peak_kind": peak_kind,
-                     "bytes_per_launch": kern_bytes, "avg_launch_us": kern_avg_s * 1e6},
-        "segments_us_median": ({name: statistics.median(s_[i] for s_ in seg_ms) * 1e3
-                                for i, name in enumerate(("route", "shared_experts_past_route", "routed_experts", "combine"))}
-                               if seg_ms else None),
+                     "bytes_per_launch": kern_bytes, "avg_launch_us": round(kern_avg_s * 1e6, 2),
+                     "timing": "the kernel's own timeline: first CTA start to last CTA end (%globaltimer), "
+                               "in the layer", "traffic_source": traffic_note},
+        "kernel_spans_us_median": {"route": seg("route"), "shared_experts": seg("shared_experts"),
+                                   "routed_experts": seg("routed_experts")},
+        "kernel_start_end_us_median": offsets,
+        "blocks": blocks,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
                 "d2h_bytes_per_step": syn.KIMI.d_model * 2},
         "gpu_launches": K * 4,
-        "timing": "one CUDA graph per step: route, shared experts, routed experts, combine chained on one "
-                  "stream; timing events at its start and end and, for the segments, on a side branch"
-                  if gev is not None else "one CUDA graph per step, events around the replay",
+        "timing": "one CUDA graph per step (route, shared experts, routed experts, combine chained on one "
+                  "stream), CUDA events around the replay; kernel spans from the kernels' own timeline",
         "clocks": clocks,
         "wall_s_timed_region": wall,
     }
     return line
 
 
-def timeable(evs):
-    """The graph's timing events if the runtime lets them be timed, else None."""
-    if evs is None:
-        return None
+def measured_traffic():
+    """DRAM bytes (read + write) of one routed-expert launch on this workload from an ncu
+    capture, if one was recorded for the kernel source as it is now: profiles/ holds the
+    capture's figure with the SHA-256 of csrc/experts_tc.cu it was taken on."""
+    import hashlib
     try:
-        evs[0].elapsed_time(evs[4])
-        return evs
-    except Exception:
-        return None
+        with open(os.path.join(ROOT, "profiles", "routed_kernel_traffic.json")) as fh:
+            rec = json.load(fh)
+        with open(os.path.join(ROOT, "mxfp4_mixture_experts_router_gb300", "csrc", "experts_tc.cu"), "rb") as fh:
+            sha = hashlib.sha256(fh.read()).hexdigest()
+    except (OSError, ValueError):
+        return None, "no ncu capture recorded"
+    if rec.get("source_sha256") != sha:
+        return None, "the recorded ncu capture is of an earlier version of the kernel"
+    return int(rec["dram_bytes_per_launch"]), rec.get("command", "ncu")
 
 
-def time_blocks(torch, lay, X, flush, n, reps):
-    """Verification blocks of n rows: shared N(0,1) base logits + N(0, 0.5) per-row noise,
-    one captured graph replayed per block."""
+def time_blocks(torch, lay, X, flush, n, sigma, reps, peak):
+    """Verification blocks of n rows: shared N(0,1) base logits + N(0, sigma) per-row
+    noise (caller logits), one captured graph replayed per block, L2 flushed before each."""
     dev = X.device
     Xs = torch.empty((n, syn.KIMI.d_model), dtype=torch.uint16, device=dev)
     Ls = torch.empty((n, syn.KIMI.n_experts), dtype=torch.float32, device=dev)
-    lgs = [torch.from_numpy(syn.block_logits(SEED, n, syn.KIMI.n_experts, 0.5, block=b)).to(dev)
+    lgs = [torch.from_numpy(syn.block_logits(SEED, n, syn.KIMI.n_experts, sigma, block=b)).to(dev)
            for b in range(reps + 3)]
     Xs.copy_(X[:n])
     Ls.copy_(lgs[0])
-    graph, gev = lay.capture(Xs, Xs, logits_in=Ls, events=True)
+    graph, _ = lay.capture(Xs, Xs, logits_in=Ls)
     graph.replay()
     torch.cuda.synchronize()
-    gev = timeable(gev)
     ts, us = [], []
     for b in range(reps + 3):
         x0 = (b * n) % (N_ROWS_SEEDED - n)
@@ -401,13 +508,14 @@ def time_blocks(torch, lay, X, flush, n, reps):
         e1.record()
         torch.cuda.synchronize()
         if b >= 3:
-            ts.append(gev[0].elapsed_time(gev[4]) if gev is not None else e0.elapsed_time(e1))
+            ts.append(e0.elapsed_time(e1))
             us.append(int(lay.ws_view(lay.offsets.n_unique, 1, torch.int32).item()))
     t = statistics.median(ts)
     u = statistics.mean(us)
     allb = u * SLAB + 2 * Q8_SLAB + 3 * n * syn.KIMI.d_model * 2
-    return {"us_median": t * 1e3, "unique_experts": u, "gbs_unique": u * SLAB / t / 1e6,
-            "gbs_all_bytes": allb / t / 1e6, "routing": "caller logits"}
+    return {"us_median": round(t * 1e3, 2), "unique_experts": u, "gbs_unique": round(u * SLAB / t / 1e6, 1),
+            "frac_unique": round(u * SLAB / t / 1e6 / peak, 4), "gbs_all_bytes": round(allb / t / 1e6, 1),
+            "routing": "caller logits", "blocks_timed": reps}
 
 
 def run_profile_case(args):
@@ -649,12 +757,13 @@ def run_reference(args):
     secs = oracle_step_seconds(pairs)[W:]
     total = sum(secs)
     value = K * SLAB / total / 1e9
-    cores = 1 if os.environ.get("OPENBLAS_NUM_THREADS") == "1" else (os.cpu_count() or 1)
+    cores = 1  # BLAS pinned to one thread before numpy was imported
     return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": 1,
             "steps": K, "warmup": W, "ms_per_step": total / K * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD, "rows_per_step": 1},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "cpu": cpu_model(),
                              "sample": "each step one (row, selected expert) fp64 expert MLP of the workload "
                                        "(17,547,264 expert bytes); the metric's unit scaled from it"},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -668,7 +777,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-blocks", action="store_true")
-    ap.add_argument("--_oracle-sample", type=int, default=0, dest="oracle_sample")
+    ap.add_argument("--block-reps", type=int, default=10)
+    ap.add_argument("--_oracle-rows", default="", dest="oracle_rows")
     ap.add_argument("--profile-case", action="store_true",
                     help="run the small ncu case (a few layers, <1 GB on the device) and exit")
     ap.add_argument("--profile-rows", type=int, default=1)
@@ -704,8 +814,9 @@ def main():
         run_profile_case(args)
         return
 
-    if args.oracle_sample:
-        print(json.dumps({"seconds": oracle_step_seconds(oracle_pairs(args.oracle_sample))}))
+    if args.oracle_rows:
+        gbs, secs = oracle_layer_rows([int(v) for v in args.oracle_rows.split(",")])
+        print(json.dumps({"gbs": round(gbs, 5), "seconds": round(secs, 2)}))
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -721,7 +832,7 @@ def main():
     line = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(max(1, min(16, os.cpu_count() or 1)))
         print(json.dumps(line))
     if world > 1:
         import torch

@@ -163,6 +163,14 @@ typedef struct moe_ws_offsets {
     int64_t dbg_u;        /* float [pairs][f] up projection   (MOE_MODE_DEBUG_GU) */
     int64_t h;            /* float [pairs][f] SwiGLU activations */
     int64_t shared_y;     /* float [n_shared][N][d] shared-expert outputs */
+    int64_t timeline;     /* uint64 [4][2] kernel timeline: for the routing kernel
+                             (moe_route with the router GEMV), the shared-expert kernel and
+                             the routed-expert kernel (in that order; the fourth pair is
+                             unused) the bitwise complement of the earliest CTA start and
+                             the latest CTA end (%globaltimer ns) since the caller last
+                             zeroed these 64 bytes; zero = no launch yet.  Zeroing them is
+                             optional (they only serve timing) and must not overlap a
+                             running layer. */
 } moe_ws_offsets;
 
 MOE_API int moe_workspace_offsets(const moe_desc* desc, int32_t n_rows_max, int32_t n_shared,

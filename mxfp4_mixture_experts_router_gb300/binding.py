@@ -60,7 +60,7 @@ class MoePool(ctypes.Structure):
 
 class MoeWsOffsets(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
-                ("error_word", "n_unique", "uexp", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y")]
+                ("error_word", "n_unique", "uexp", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y", "timeline")]
 
 
 class MoeCacheStats(ctypes.Structure):

@@ -105,6 +105,7 @@ extern "C" int moe_workspace_offsets(const moe_desc* desc, int32_t n_rows_max, i
     o->dbg_u = (int64_t)L.dbg_u;
     o->h = (int64_t)L.h;
     o->shared_y = (int64_t)L.shared_y;
+    o->timeline = (int64_t)L.ctrl + 4 * CTRL_TL;
     return MOE_OK;
 }
 

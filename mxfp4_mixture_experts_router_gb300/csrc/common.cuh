@@ -32,11 +32,18 @@ enum Ctrl : int {
     CTRL_PREPD_SH = 11,  // rows of that copy written
     CTRL_RT_DONE = 12,   // routing finishers done with their rows' f16 copies
     CTRL_XMAX = 64,      // [64, 96): per-row max |x| bits published by the router GEMV CTAs
+    CTRL_TL = 96,        // [96, 128): kernel timeline, 4 kernels x (~first start, last end) as u64 pairs
     CTRL_WORDS = 128
 };
 
+// kernels of the timeline (CTRL_TL)
+enum TlKernel : int { TL_ROUTE = 0, TL_SHARED = 1, TL_ROUTED = 2 };
+
 // K splits of a gate/up tile in the block-scaled tensor-core expert kernel
 constexpr int TC_GU_SPLIT = 2;
+// E2M1 terms an activation value is split into for that kernel (each term with
+// its own E8M0 scale per 32 elements): about 16 significant bits survive
+constexpr int MX_TERMS = 5;
 
 struct WsLayout {
     size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
@@ -67,13 +74,14 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.dbg_u = take((size_t)L.pairs * f * 4);
     L.shared_y = take((size_t)n_shared * N * d * 4);
     L.logits = take((size_t)N * E * 4);
-    // MX activations for the block-scaled expert kernel: 3 E4M3 rows per row of x
-    // and per routed pair of h, plus 64 rows of padding that a 64-row tile may read
-    L.mx_rows_x = 3 * N + 64;
-    L.mx_rows_h = 3 * N * k + 64;
-    L.x_mx = take((size_t)L.mx_rows_x * d);
+    // MX activations for the block-scaled expert kernel: MX_TERMS rows of packed
+    // E2M1 codes (two per byte, even element in the low nibble) per row of x and
+    // per routed pair of h, plus 80 rows of padding
+    L.mx_rows_x = (int64_t)MX_TERMS * N + 80;
+    L.mx_rows_h = (int64_t)MX_TERMS * N * k + 80;
+    L.x_mx = take((size_t)L.mx_rows_x * (d / 2));
     L.x_sc = take((size_t)L.mx_rows_x * (d / 32));
-    L.h_mx = take((size_t)L.mx_rows_h * f);
+    L.h_mx = take((size_t)L.mx_rows_h * (f / 2));
     L.h_sc = take((size_t)L.mx_rows_h * (f / 32));
     // the block-scaled kernel works on chunks of at most 16 pairs of one expert:
     // at most E + N*k/16 of them; one finished-tile counter per chunk
@@ -153,6 +161,16 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Kernel timeline: every CTA of kernel `k` records its start and end time
+// (%globaltimer, ns); the workspace keeps the bitwise complement of the earliest
+// start and the latest end since the words were last zeroed (zero = none yet).
+__device__ __forceinline__ void tl_begin(uint32_t* ctrl, int k) {
+    atomicMax(reinterpret_cast<unsigned long long*>(ctrl + CTRL_TL) + 2 * k, (unsigned long long)~global_ns());
+}
+__device__ __forceinline__ void tl_end(uint32_t* ctrl, int k) {
+    atomicMax(reinterpret_cast<unsigned long long*>(ctrl + CTRL_TL) + 2 * k + 1, (unsigned long long)global_ns());
 }
 
 __device__ __forceinline__ void set_error(uint32_t* ctrl, uint32_t bits) {
@@ -341,6 +359,52 @@ __device__ __forceinline__ void mx3_split(float v, uint32_t (&q)[3], uint32_t (&
         r -= back * exp2i(e);
         sbyte[t] = (uint32_t)(e + 127);
     }
+}
+
+// E2M1 code of v (round to nearest even, saturating at +-6) and its exact value.
+__device__ __forceinline__ uint32_t e2m1_code(float v, float& back) {
+    uint32_t bytes, h2;
+    asm("{ .reg .b8 t;\n"
+        "  cvt.rn.satfinite.e2m1x2.f32 t, %2, %2;\n"
+        "  cvt.rn.f16x2.e2m1x2 %1, t;\n"
+        "  mov.b32 %0, {t, t, t, t}; }"
+        : "=r"(bytes), "=r"(h2)
+        : "f"(v));
+    back = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    return bytes & 0xFu;
+}
+
+// Splits the 32 values of a block (one per lane) into MX_TERMS E2M1 terms with
+// their own power-of-two block scales, v ~ sum_t q_t * 2^(s_t - 127): each term
+// codes the residual of the previous ones (the block's largest residual lands in
+// (3, 6]).  Writes the lane's codes and, in every lane, the E8M0 scale bytes.
+__device__ __forceinline__ void mx_split(float v, uint32_t (&q)[MX_TERMS], uint32_t (&sbyte)[MX_TERMS]) {
+    float r = v;
+#pragma unroll
+    for (int t = 0; t < MX_TERMS; t++) {
+        const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(r) & 0x7FFFFFFFu);
+        // m = 1.f * 2^E: scale 2^(E-2) when f <= 1.5 (m / scale in [4, 6]), else 2^(E-1)
+        int e = (int)(m >> 23) - 127 - 1 - ((m & 0x7FFFFFu) <= 0x400000u ? 1 : 0);
+        e = m == 0u ? 0 : e;
+        e = e < -126 ? -126 : (e > 127 ? 127 : e);
+        float back;
+        q[t] = e2m1_code(r * exp2i(-e), back);
+        r -= back * exp2i(e);
+        sbyte[t] = (uint32_t)(e + 127);
+    }
+}
+
+// Stores the 32 four-bit codes of a warp (lane i: element i) as 16 packed bytes
+// (even element in the low nibble) at dst, 4-byte aligned.
+__device__ __forceinline__ void store_e2m1_block(uint8_t* dst, uint32_t code) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t b = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);  // even lanes: one byte
+    const uint32_t b1 = __shfl_down_sync(0xffffffffu, b, 2);
+    const uint32_t b2 = __shfl_down_sync(0xffffffffu, b, 4);
+    const uint32_t b3 = __shfl_down_sync(0xffffffffu, b, 6);
+    if ((lane & 7) == 0)
+        *reinterpret_cast<uint32_t*>(dst + (lane >> 1)) = (b & 0xFFu) | ((b1 & 0xFFu) << 8) | ((b2 & 0xFFu) << 16) |
+                                                           ((b3 & 0xFFu) << 24);
 }
 
 // D[16x8] += A[16x16] * B[16x8], f16 inputs, fp32 accumulate.

@@ -911,6 +911,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
     __shared__ int s_last;
 
     const int tid = threadIdx.x;
+    const int tl_kernel = p.job == J_LAYER ? (p.routed_off ? TL_SHARED : TL_ROUTED) : -1;
+    if (tid == 0 && tl_kernel >= 0) tl_begin(p.ctrl, tl_kernel);
     if (tid == 0) {
         for (int s = 0; s < EX_NST; s++) {
             mbar_init(&full[s], 1);
@@ -967,6 +969,7 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
             }
         }
     }
+    if (tid == 0 && tl_kernel >= 0) tl_end(p.ctrl, tl_kernel);
     if (p.dep_at_end && tid == 0) griddep_wait();  // complete only after the previous kernel
 }
 

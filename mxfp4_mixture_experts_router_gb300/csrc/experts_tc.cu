@@ -1,4 +1,4 @@
-// Block-scaled tensor-core path (tcgen05, kind::mxf8f6f4) for the routed MXFP4
+// Block-scaled tensor-core path (tcgen05, kind::mxf4) for the routed MXFP4
 // experts of a block (decode blocks and prefill).
 //
 // Pages: "Run Kimi 3.1 locally on one GPU": MXFP4 experts (section "One GPU,
@@ -6,12 +6,12 @@
 // (section "A drafter that leaves the answer unchanged").
 //
 // Each expert's E2M1 codes and E8M0 scales go to the tensor cores exactly as
-// they are stored: TMA unpacks the 4-bit codes into the byte-per-element
-// shared-memory form that kind::mxf8f6f4 reads (16U4_ALIGN16B), the scales are
-// moved into tensor memory, and tcgen05.mma applies them per 32-element block.
-// The activations are the other operand, each row split into three E4M3 terms
-// with their own E8M0 block scales (v ~ sum of terms, about 12 bits), so a
-// token is three B columns whose results are summed in a fixed order.
+// they are stored: TMA copies the packed 4-bit codes into shared memory (two
+// per byte, the layout kind::mxf4 reads), the scales are moved into tensor
+// memory, and tcgen05.mma applies them per 32-element block (scale_vec::2X).
+// The activations are the other operand, each row split into MX_TERMS E2M1
+// terms with their own E8M0 block scales (v ~ sum of terms), so a token is
+// MX_TERMS B columns whose results are summed in a fixed order.
 //
 // One CTA per SM, persistent, warp-specialised:
 //   warp 0      producer: claims work items in order and TMA-loads them into a
@@ -21,7 +21,7 @@
 //               scales to tensor memory
 //   warps 6..9  epilogue: read the TMEM accumulators (double-buffered), reduce
 //               the K splits of a gate/up tile, finish SwiGLU and re-split h into
-//               E4M3 terms, or write the outputs.
+//               E2M1 terms, or write the outputs.
 // Work items: gate/up items (64 rows of gate + the same 64 rows of up = one
 // M=128 tile, over one of TC_GU_SPLIT K ranges) and down items (128 rows, full
 // K): the gate/up items of every chunk first, then the down items in chunk
@@ -29,11 +29,12 @@
 // none waits at the end of the launch.  A down item's activations are read
 // only after every gate/up tile of its chunk is finished (bounded wait).
 //
-// The TMA engine moves about 18 bytes a cycle per SM and costs a roughly fixed
-// time per box, so it carries only the weights: a stage is one box of code rows
-// (128 rows x 256 K: gate and up rows and both 128-K halves arrive through a 5-D
-// tensor map) and the scales of a whole item arrive in one box into a per-item
-// buffer.  The small activation operand (rows of the block or of the expert's
+// TMA costs a roughly fixed time per box, so it carries only the weights: a
+// stage is one 16 KB box of code rows (128 rows x 256 K; gate and up rows arrive
+// through a 5-D tensor map) and the scales of a whole item arrive in one box into
+// a per-item buffer.  Packed codes take half the shared memory (and half the
+// tensor core's shared-memory reads) of the byte-per-element form, so the ring
+// holds twice the stages.  The small activation operand (rows of the block or of the expert's
 // pairs, from L2) and its scales are loaded by the scale-mover warps one stage
 // ahead into registers (two stages ahead into L1) and written in the swizzled
 // layout the MMA reads.  Every expert's slot and pair range sit in shared memory
@@ -44,23 +45,25 @@
 namespace moe {
 namespace tc {
 
-constexpr int KC = 256;                     // K elements per stage
-constexpr int A_BYTES = 128 * KC;           // 128 rows x 256 codes, one byte each after unpacking
+constexpr int KC = 512;                     // K elements per stage
+constexpr int KCH = KC / 256;               // 128-byte pieces (256 packed K) of a row per stage
+constexpr int A_BYTES = 128 * KC / 2;       // 128 rows x KC packed E2M1 codes: KCH regions of 128 x 128 B
+constexpr int SF_COLS = KC / 32;            // tensor-memory scale columns per stage (4 per 128 K)
+constexpr int T = MX_TERMS;                 // B columns (activation terms) per token
 constexpr int SC_MAX = 112;                 // scale bytes per row of one item (its K range / 32)
 constexpr int SA_BYTES = 128 * SC_MAX;      // A scales of an item
 constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens (xor-swizzled)
-constexpr int CHUNK = 16;                   // pairs of one expert per work item (48 MMA columns)
+constexpr int CHUNK = 16;                   // pairs of one expert per work item (80 MMA columns)
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
-constexpr int MAX_NST = 5;
 
-// Two configurations: blocks of up to 5 rows (16 activation rows, 5-stage ring)
-// and of up to 16 rows (48 activation rows, 4-stage ring).
+// Two configurations: blocks of up to 5 rows (32 activation rows, 4-stage ring)
+// and of up to 16 rows or prefill chunks (80 activation rows, 3-stage ring).
 template <int NBM>
 struct Cfg {
-    static constexpr int NST = NBM == 16 ? 5 : 4;      // ring stages
-    static constexpr int B_BYTES = 2 * NBM * 128;      // B of a stage: two K halves of up to NBM rows x 128 B
+    static constexpr int NST = NBM == 32 ? 4 : 3;      // ring stages
+    static constexpr int B_BYTES = KCH * NBM * 128;    // B of a stage: KCH regions of NBM rows x 128 B
     static constexpr int STAGE = A_BYTES + B_BYTES;    // a multiple of 1024
     static constexpr int SCB = SA_BYTES;               // one per-item A-scale buffer (two, by item parity)
     // tensor memory: two accumulator sets (double-buffered across items), each of
@@ -68,29 +71,29 @@ struct Cfg {
     // overlap in the tensor pipe; the epilogue sums them in order; the same NACC
     // in both configurations keeps a row's arithmetic independent of the block),
     // then the A and B scale columns of every stage
-    static constexpr int ACC_COLS = NBM == 16 ? 16 : 64;
+    static constexpr int ACC_COLS = NBM;
     static constexpr int NACC = 2;
     static constexpr uint32_t ACC_SET = NACC * ACC_COLS;
-    static constexpr uint32_t TM_SFA = 2 * ACC_SET;    // A scales: + stage*8 + set*4 (four 32-row columns)
-    static constexpr uint32_t TM_SFB = TM_SFA + NST * 8;
-    static constexpr uint32_t TM_COLS = TM_SFB + NST * 8 <= 256 ? 256 : 512;
+    static constexpr uint32_t TM_SFA = 2 * ACC_SET;    // A scales: + stage*SF_COLS + set*4 (four 32-row columns)
+    static constexpr uint32_t TM_SFB = TM_SFA + NST * SF_COLS;
+    static constexpr uint32_t TM_COLS = TM_SFB + NST * SF_COLS <= 256 ? 256 : 512;
     // per expert: (slot, first pair | pairs << 16) and the prefix of its chunk counts
-    static constexpr int MAX_U = NBM == 16 ? 256 : 1024;
+    static constexpr int MAX_U = NBM == 32 ? 128 : 1024;
     // blocks of up to 5 rows: the block row of every (row, slot) pair (5 x k <= 160)
-    static constexpr int TOKS = NBM == 16 ? 160 : 0;
+    static constexpr int TOKS = NBM == 32 ? 160 : 0;
     static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 12;
     static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
-    static_assert(TM_SFB + NST * 8 <= TM_COLS && NBM <= ACC_COLS, "tensor memory columns");
-    static_assert(NST <= MAX_NST, "ring");
+    static_assert(TM_SFB + NST * SF_COLS <= TM_COLS && NBM <= ACC_COLS && NBM <= 128, "tensor memory columns");
+    static_assert(NBM % 16 == 0 && CHUNK * T <= 80, "MMA N");
 };
 
 enum { IT_GU = 0, IT_DN = 1 };
 
 struct Params {
-    CUtensorMap a_gu;       // gate and up codes {128 K, f rows, 2 matrices, d/128, slot}, 4-bit unpacked to bytes
-    CUtensorMap a_dn;       // down codes {128 K, d rows, f/128, slot}
+    CUtensorMap a_gu;       // gate and up codes {128 B = 256 K, f rows, 2 matrices, d/256, slot}, packed
+    CUtensorMap a_dn;       // down codes {128 B, d rows, f/256, slot}
     CUtensorMap s_gu;       // gate and up E8M0 scales {d/32, f rows, 2, slot}
     CUtensorMap s_dn;       // down scales {f/32, d rows, slot}
     int d, f, k, n_rows, n_shared, nk;
@@ -106,9 +109,9 @@ struct Params {
     uint32_t* gu_done;
     uint32_t* gu_cnt;
     float* gu_part;
-    const uint8_t* x_mx;   // E4M3 terms of the block's rows (row 3n+t) [rows][d] and scales [rows][d/32]
+    const uint8_t* x_mx;   // packed E2M1 terms of the block's rows (row T n + t) [rows][d/2], scales [rows][d/32]
     const uint8_t* x_sc;
-    uint8_t* h_mx;         // E4M3 terms of the pairs' SwiGLU activations (row 3P+t) [rows][f], scales [rows][f/32]
+    uint8_t* h_mx;         // packed E2M1 terms of the pairs' SwiGLU activations (row T P + t) [rows][f/2], scales
     uint8_t* h_sc;
     float* y_part;
     float* dbg_g;
@@ -152,10 +155,11 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
-// instruction descriptor: E2M1 A, E4M3 B, fp32 D, K-major, M = 128, N = nb,
-// E8M0 scales, scale byte `sf` of the 32-bit scale words for both operands
+// instruction descriptor of kind::mxf4: E2M1 A and B (format code 1), fp32 D,
+// K-major, M = 128, N = nb, E8M0 scales; with scale_vec::2X an MMA (K = 64) uses
+// two scale bytes of each 32-bit scale word, starting at byte `sf` (0 or 2)
 __device__ __forceinline__ uint32_t idesc(int nb, int sf) {
-    return ((uint32_t)sf << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(nb >> 3) << 17) | (1u << 23) | (8u << 24) |
+    return ((uint32_t)sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nb >> 3) << 17) | (1u << 23) | (8u << 24) |
            ((uint32_t)sf << 29);
 }
 
@@ -163,7 +167,7 @@ __device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a, uint64_t b, 
                                        bool acc) {
     asm volatile(
         "{ .reg .pred p; setp.ne.u32 p, %6, 0;\n"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(
             d_tmem),
         "l"(a), "l"(b), "r"(id), "r"(sfa), "r"(sfb), "r"(acc ? 1u : 0u)
         : "memory");
@@ -281,7 +285,7 @@ __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t ta
 template <int NBM>
 __device__ void producer(const Params& p, int U, const uint2* umeta, const int* cp, unsigned char* smem,
                          unsigned char* scbuf, uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf,
-                         Meta* meta, int first) {
+                         uint64_t* sce, Meta* meta, int first) {
     using C = Cfg<NBM>;
     tma_prefetch_desc(&p.a_gu);
     tma_prefetch_desc(&p.a_dn);
@@ -321,13 +325,12 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
         const int kbase = gu ? split * kr : 0;
         const int nch = kr / KC;
         const int sc = kr / 32;                // scale bytes per row of the item
-        const int nb = round16(3 * rc);       // activation rows loaded = MMA N
-        const int brow = 3 * p0;               // down: the chunk's rows of h
+        const int nb = round16(T * rc);       // activation rows loaded = MMA N
+        const int brow = T * p0;               // down: the chunk's rows of h
         const int row0 = gu ? blk * 64 : blk * 128;
         const int sbuf = seq & 1;
         unsigned char* sa = scbuf + sbuf * C::SCB;
-        // an unpacked 4-bit code box counts its packed (global) bytes: half its shared-memory size
-        const uint32_t tx = (uint32_t)(A_BYTES / 2);
+        const uint32_t tx = (uint32_t)A_BYTES;
         const uint32_t tx_sc = (uint32_t)(128 * sc);
         int claim_after = total;
         uint32_t dep_nxt = 0u;
@@ -351,13 +354,17 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
             mt.sbuf = sbuf;
             mt.sc = sc;
             mt.kbase = kbase;
-            mt.nrow = 3 * rc;
+            mt.nrow = T * rc;
             mt.brow = brow;
             mt.p0 = p0;
             if (c == 0) {
-                // the item's scales into its buffer, which item seq-2 used last: every
-                // item has at least NST stages, so that item's scales have all been
-                // moved to tensor memory before this stage was released
+                // the item's scales into its buffer, once the scale movers are done
+                // with item seq-2, which used it last
+                if (seq >= 2 && !mbar_wait(&sce[sbuf], (uint32_t)((seq >> 1) - 1) & 1u)) {
+                    set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
                 mbar_arrive_expect_tx(&scf[sbuf], tx_sc);
                 if (gu)
                     tma_load_4d(sa, &p.s_gu, &scf[sbuf], kbase / 32, row0, 0, z);
@@ -371,7 +378,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
             mbar_arrive(&mready[stage]);
             mbar_arrive_expect_tx(&full[stage], tx);
             unsigned char* st = smem + (size_t)stage * C::STAGE;
-            const int kc = (kbase + c * KC) / 128;   // first 128-K chunk of the stage
+            const int kc = (kbase + c * KC) / 256;   // the stage's first 256-K piece
             if (gu)
                 tma_load_5d(st, &p.a_gu, &full[stage], 0, row0, 0, kc, z);
             else
@@ -414,32 +421,34 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
 }
 
 // One stage's activation operand, held in registers between its loads and its
-// stores: chunk j = t + 128 i (row j / 16, 16-byte piece j % 16 of the row's
-// 256 K) of this thread t, and the stage's 8 scale bytes of rows lane and
-// 32 + lane (every warp loads the scales its own lane quadrant needs).
+// stores: 16-byte piece j = t + 128 i (row j / (8 KCH), piece j % (8 KCH) of the
+// row's KC/2 packed bytes) of this thread t, and the stage's KC/32 scale bytes of
+// rows lane, 32 + lane and 64 + lane (every warp loads the scales its own lane
+// quadrant needs).
+constexpr int BP = 8 * KCH;  // 16-byte pieces of a B row per stage
 template <int NBM>
 struct BStage {
-    uint4 d[NBM / 8];
-    uint2 s[2];
+    uint4 d[NBM * BP / 128];
+    uint4 s[3];
 };
 
-// source row of activation row `row` of a stage: gate/up gathers the E4M3 terms of
-// the block rows of the chunk's pairs (3 x the pair's token + term), down reads the
-// chunk's rows of h (3 x pair + term) in place
+// source row of activation row `row` of a stage: gate/up gathers the E2M1 terms of
+// the block rows of the chunk's pairs (T x the pair's token + term), down reads the
+// chunk's rows of h (T x pair + term) in place
 __device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row, const uint16_t* tok) {
     if (m.type != IT_GU) return m.brow + row;
-    const int q = row / 3;
+    const int q = row / T;
     const int n = tok != nullptr ? (int)tok[m.p0 + q] : __ldcg(p.pair + m.p0 + q) / p.k;
-    return 3 * n + (row - 3 * q);
+    return T * n + (row - T * q);
 }
 
-// the source rows this thread reads for an item (data rows j / 16 of its chunks j,
-// scale rows lane and 32 + lane), resolved once per item
+// the source rows this thread reads for an item (data rows j / BP of its pieces j,
+// scale rows lane, 32 + lane and 64 + lane), resolved once per item
 template <int NBM>
 struct BRows {
     int item = -1;
-    int d[NBM / 8];
-    int s[2];
+    int d[NBM * BP / 128];
+    int s[3];
 };
 
 template <int NBM>
@@ -448,19 +457,19 @@ __device__ __forceinline__ void b_rows(const Params& p, const Meta& m, int t, in
     if (r.item == m.item) return;
     r.item = m.item;
 #pragma unroll
-    for (int i = 0; i < NBM / 8; i++) {
-        const int row = (t + 128 * i) >> 4;
+    for (int i = 0; i < NBM * BP / 128; i++) {
+        const int row = (t + 128 * i) / BP;
         r.d[i] = row < m.nrow ? b_src_row(p, m, row, tok) : 0;
     }
 #pragma unroll
-    for (int c = 0; c < 2; c++) {
+    for (int c = 0; c < 3; c++) {
         const int row = 32 * c + lane;
         r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(p, m, row, tok) : 0;
     }
 }
 
 // the lines b_load will read for stage `chunk` of item m, into L1 (one prefetch per
-// 128-byte line of activation rows, one per scale row); rows from r
+// 128-byte row of packed activation codes, one per scale row); rows from r
 template <int NBM>
 __device__ __forceinline__ void b_prefetch(const Params& p, const Meta& m, int chunk, int t, int lane,
                                            const BRows<NBM>& r) {
@@ -470,13 +479,13 @@ __device__ __forceinline__ void b_prefetch(const Params& p, const Meta& m, int c
     const int ld = gu ? p.d : p.f;
     const int k0 = m.kbase + chunk * KC;
 #pragma unroll
-    for (int i = 0; i < NBM / 8; i++) {
-        const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
+    for (int i = 0; i < NBM * BP / 128; i++) {
+        const int j = t + 128 * i, row = j / BP, c16 = j % BP;
         if (row < m.nrow && (c16 & 7) == 0)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (size_t)r.d[i] * ld + k0 + c16 * 16));
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (size_t)r.d[i] * (ld / 2) + k0 / 2 + c16 * 16));
     }
 #pragma unroll
-    for (int c = 0; c < 2; c++) {
+    for (int c = 0; c < 3; c++) {
         const int row = 32 * c + lane;
         if (row < m.nrow && row < NBM)
             asm volatile("prefetch.global.L1 [%0];" ::"l"(ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32));
@@ -493,32 +502,36 @@ __device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk
     const int ld = gu ? p.d : p.f;
     const int k0 = m.kbase + chunk * KC;
 #pragma unroll
-    for (int i = 0; i < NBM / 8; i++) {
-        const int j = t + 128 * i, row = j >> 4, c16 = j & 15;
-        b.d[i] = row < m.nrow ? __ldca(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * ld + k0 + c16 * 16))
-                              : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < NBM * BP / 128; i++) {
+        const int j = t + 128 * i, row = j / BP, c16 = j % BP;
+        b.d[i] = row < m.nrow
+                     ? __ldca(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * (ld / 2) + k0 / 2 + c16 * 16))
+                     : make_uint4(0, 0, 0, 0);
     }
+    static_assert(KC / 32 == 16, "one 16-byte scale load per row and stage");
 #pragma unroll
-    for (int c = 0; c < 2; c++) {
+    for (int c = 0; c < 3; c++) {
         const int row = 32 * c + lane;
         b.s[c] = (row < m.nrow && row < NBM)
-                     ? __ldca(reinterpret_cast<const uint2*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
-                     : make_uint2(0, 0);
+                     ? __ldca(reinterpret_cast<const uint4*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
+                     : make_uint4(0, 0, 0, 0);
     }
 }
 
 // warps 2..5: per stage, the activation rows into the stage's B area (the
-// 128-byte-swizzled K-major layout the MMA reads: two 128-K halves of nb rows,
-// piece cc of row r at 16 * (cc ^ (r % 8))) and every E8M0 scale into tensor
-// memory.  Scale of row m (A: weight row, B: activation row) for the stage's K
+// 128-byte-swizzled K-major layout the MMA reads: KCH regions of NBM rows of 128
+// packed bytes, piece cc of row r at 16 * (cc ^ (r % 8))) and every E8M0 scale
+// into tensor memory.  Scale of row m (A: weight row, B: activation row) for the stage's K
 // blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word at lane m % 32,
 // column base + set*4 + m / 32; each warp writes the copy in its own lane
 // quadrant.  A stage is prepared as soon as the producer has claimed it (its
 // codes may still be in flight); the next stage's activations are loaded ahead
-// when it belongs to the same item.
+// when it belongs to the same item.  After an item's last stage the warps release
+// its scale buffer (sce).
 template <int NBM>
 __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char* scbuf, uint32_t tbase,
-                            uint64_t* mready, uint64_t* scf, uint64_t* sfr, const Meta* meta, const uint16_t* tok) {
+                            uint64_t* mready, uint64_t* scf, uint64_t* sce, uint64_t* sfr, const Meta* meta,
+                            const uint16_t* tok) {
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
     uint32_t stage = 0, phase = 0;
@@ -536,10 +549,10 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b, rows, tok);
         unsigned char* bst = smem + (size_t)stage * C::STAGE + A_BYTES;
 #pragma unroll
-        for (int i = 0; i < NBM / 8; i++) {
-            const int j = t + 128 * i, row = j >> 4, c16 = j & 15, kh = c16 >> 3, cc = c16 & 7;
+        for (int i = 0; i < NBM * BP / 128; i++) {
+            const int j = t + 128 * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
             if (row < m.nrow)
-                *reinterpret_cast<uint4*>(bst + kh * (m.nb * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = b.d[i];
+                *reinterpret_cast<uint4*>(bst + kh * (NBM * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = b.d[i];
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (m.chunk == 0) {  // the item's A scales have landed
@@ -553,18 +566,23 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         const int kb_off = m.chunk * (KC / 32);
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 #pragma unroll
-        for (int set = 0; set < 2; set++) {
+        for (int set = 0; set < KC / 128; set++) {
             uint32_t wa[4];
 #pragma unroll
             for (int c = 0; c < 4; c++) wa[c] = lds32(sa + (32 * c + lane) * m.sc + kb_off + 4 * set);
-            const uint32_t w0 = set ? b.s[0].y : b.s[0].x, w1 = set ? b.s[1].y : b.s[1].x;
-            tm_st4(tbase + C::TM_SFA + stage * 8 + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
-            tm_st4(tbase + C::TM_SFB + stage * 8 + set * 4 + lane_base, w0, w1, 0u, 0u);
+            const uint32_t w0 = set == 0 ? b.s[0].x : set == 1 ? b.s[0].y : set == 2 ? b.s[0].z : b.s[0].w;
+            const uint32_t w1 = set == 0 ? b.s[1].x : set == 1 ? b.s[1].y : set == 2 ? b.s[1].z : b.s[1].w;
+            const uint32_t w2 = set == 0 ? b.s[2].x : set == 1 ? b.s[2].y : set == 2 ? b.s[2].z : b.s[2].w;
+            tm_st4(tbase + C::TM_SFA + stage * SF_COLS + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
+            tm_st4(tbase + C::TM_SFB + stage * SF_COLS + set * 4 + lane_base, w0, w1, w2, 0u);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sfr[stage]);
+        if (lane == 0) {
+            mbar_arrive(&sfr[stage]);
+            if (m.chunk == m.nchunks - 1) mbar_arrive(&sce[m.sbuf]);  // done reading the item's scales
+        }
         const uint32_t nstage = stage + 1 == (uint32_t)C::NST ? 0u : stage + 1;
         const uint32_t nphase = nstage == 0u ? phase ^ 1u : phase;
         if (m.chunk + 1 < m.nchunks) {
@@ -608,7 +626,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
     }
 }
 
-// warp 1, one thread: eight MMAs (K = 32 each) per stage into the item's accumulator
+// warp 1, one thread: four MMAs (K = 64 each) per stage into the item's accumulator
 template <int NBM>
 __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase, uint64_t* full, uint64_t* empty,
                            uint64_t* sfr, uint64_t* acc_full, uint64_t* acc_empty, uint64_t* done, const Meta* meta,
@@ -646,17 +664,18 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
             a.split = m.split;
             a.nb = m.nb;
             a.p0 = m.p0;
-            a.rc = m.nrow / 3;
+            a.rc = m.nrow / T;
         }
         const uint32_t st = smem_u32(smem + (size_t)stage * C::STAGE);
-        const uint32_t b_half = (uint32_t)m.nb * 128;   // the B box's second 128-K half
 #pragma unroll
-        for (int ks = 0; ks < KC / 32; ks++) {
-            const uint64_t ad = sdesc(st + (ks >> 2) * 16384 + (ks & 3) * 32);
-            const uint64_t bd = sdesc(st + A_BYTES + (ks >> 2) * b_half + (ks & 3) * 32);
-            mma_mx(tbase + b * C::ACC_SET + (ks % C::NACC) * C::ACC_COLS, ad, bd, idesc(m.nb, ks & 3),
-                   tbase + C::TM_SFA + stage * 8 + (ks >> 2) * 4, tbase + C::TM_SFB + stage * 8 + (ks >> 2) * 4,
-                   m.chunk != 0 || ks >= C::NACC);
+        for (int ks = 0; ks < KC / 64; ks++) {
+            // K = 64 packed codes = 32 bytes of a 128-byte row piece; four MMAs per piece
+            const int kh = ks >> 2;
+            const uint64_t ad = sdesc(st + kh * 16384 + (ks & 3) * 32);
+            const uint64_t bd = sdesc(st + A_BYTES + kh * (NBM * 128) + (ks & 3) * 32);
+            mma_mx(tbase + b * C::ACC_SET + (ks % C::NACC) * C::ACC_COLS, ad, bd, idesc(m.nb, (ks & 1) * 2),
+                   tbase + C::TM_SFA + stage * SF_COLS + (ks >> 1) * 4,
+                   tbase + C::TM_SFB + stage * SF_COLS + (ks >> 1) * 4, m.chunk != 0 || ks >= C::NACC);
         }
         mma_commit(&empty[stage]);
         if (m.chunk == m.nchunks - 1) {
@@ -732,14 +751,17 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
         const int m = 32 * q + lane;
-        const int o0 = a.p0, r = a.rc;  // the chunk's pairs: o0 .. o0 + r - 1, MMA columns 3 per pair
+        const int o0 = a.p0, r = a.rc;  // the chunk's pairs: o0 .. o0 + r - 1, MMA columns T per pair
         if (a.type == IT_GU) {
-            // the 3 term columns of each pair summed in order; rows 0..63 gate, 64..127 up
+            // the T term columns of each pair summed in order; rows 0..63 gate, 64..127 up
 #pragma unroll
-            for (int n = 0; n < NBM / 3; n++)
-                if (n < r)
-                    xch[xch_at(m, n)] = __uint_as_float(v[3 * n]) + __uint_as_float(v[3 * n + 1]) +
-                                        __uint_as_float(v[3 * n + 2]);
+            for (int n = 0; n < NBM / T; n++)
+                if (n < r) {
+                    float sum = __uint_as_float(v[T * n]);
+#pragma unroll
+                    for (int tt = 1; tt < T; tt++) sum += __uint_as_float(v[T * n + tt]);
+                    xch[xch_at(m, n)] = sum;
+                }
             epi_sync();
             // this split's sums for the expert's pairs: part[tile][split][pair][128]
             const size_t tile_base = (size_t)a.blk * S * p.nk;
@@ -778,12 +800,12 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
                         p.dbg_g[o] = g;
                         p.dbg_u[o] = u;
                     }
-                    uint32_t qv[3], sbits[3];
-                    mx3_split(hv, qv, sbits);
+                    uint32_t qv[T], sbits[T];
+                    mx_split(hv, qv, sbits);
 #pragma unroll
-                    for (int t = 0; t < 3; t++) {
-                        p.h_mx[(size_t)(3 * P + t) * p.f + j0 + j] = (uint8_t)qv[t];
-                        if (lane == 0) p.h_sc[(size_t)(3 * P + t) * (p.f / 32) + (j0 >> 5) + jb] = (uint8_t)sbits[t];
+                    for (int t = 0; t < T; t++) {
+                        store_e2m1_block(p.h_mx + (size_t)(T * P + t) * (p.f / 2) + (j0 + 32 * jb) / 2, qv[t]);
+                        if (lane == 0) p.h_sc[(size_t)(T * P + t) * (p.f / 32) + (j0 >> 5) + jb] = (uint8_t)sbits[t];
                     }
                     wrote = true;
                 }
@@ -794,10 +816,11 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
         } else {
             const int m0 = a.blk * 128;
 #pragma unroll
-            for (int col = 0; col < NBM / 3; col++) {
+            for (int col = 0; col < NBM / T; col++) {
                 if (col < r) {
-                    const float y = __uint_as_float(v[3 * col]) + __uint_as_float(v[3 * col + 1]) +
-                                    __uint_as_float(v[3 * col + 2]);
+                    float y = __uint_as_float(v[T * col]);
+#pragma unroll
+                    for (int tt = 1; tt < T; tt++) y += __uint_as_float(v[T * col + tt]);
                     const int pid = __ldcg(p.pair + o0 + col);
                     p.y_part[(size_t)pid * p.d + m0 + m] = y;
                 }
@@ -824,16 +847,19 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     uint64_t* sfr = empty + C::NST;
     uint64_t* mready = sfr + C::NST;
     uint64_t* scf = mready + C::NST;
-    uint64_t* acc_full = scf + 2;
+    uint64_t* sce = scf + 2;
+    uint64_t* acc_full = sce + 2;
     uint64_t* acc_empty = acc_full + 2;
     uint64_t* done = acc_empty + 2;
     Meta* meta = reinterpret_cast<Meta*>(done + 1);
     AccMeta* am = reinterpret_cast<AccMeta*>(meta + C::NST);
+    static_assert((4 * C::NST + 9) * 8 + C::NST * sizeof(Meta) + 2 * sizeof(AccMeta) + 8 <= 1024, "barrier area");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(am + 2);
     int* eflag = reinterpret_cast<int*>(tslot + 1);
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    if (tid == 0) tl_begin(p.ctrl, TL_ROUTED);
     if (tid == 0) {
         for (int s = 0; s < C::NST; s++) {
             mbar_init(&full[s], 1);
@@ -843,6 +869,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         }
         mbar_init(&scf[0], 1);
         mbar_init(&scf[1], 1);
+        mbar_init(&sce[0], 4);
+        mbar_init(&sce[1], 4);
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 2);
             mbar_init(&acc_empty[b], 4);
@@ -907,11 +935,11 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const uint32_t tbase = *tslot;
 
     if (warp == 0) {
-        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, meta, first);
+        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, sce, meta, first);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
-        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sfr, meta, tok);
+        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sce, sfr, meta, tok);
     } else {
         epilogue<NBM>(p, tbase, xch, eflag, acc_full, acc_empty, am);
     }
@@ -936,6 +964,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
             p.ctrl[CTRL_EXIT_TC] = 0;
         }
     }
+    if (tid == 0) tl_end(p.ctrl, TL_ROUTED);
     if (p.after_shared && tid == 0) griddep_wait();  // complete only after the shared experts
 }
 
@@ -994,14 +1023,14 @@ static int launch(const Params& p, cudaStream_t stream) {
 
 }  // namespace tc
 
-// Shapes the block-scaled path serves: gate/up K splits that are multiples of 512
-// elements with a scale row that fits the per-item buffer, a down K range that is
-// a multiple of 512 (scale row likewise), at least as many stages per item as the
-// ring holds, and blocks of at most 16 rows (48 activation columns).
+// Shapes the block-scaled path serves: gate/up K splits that are whole stages
+// (multiples of 256 elements) with a scale row that fits the per-item buffer, a
+// down K range of whole stages (scale row likewise), 64-row gate/up and 128-row
+// down tiles.
 bool tc_expert_supported(int d, int f, int n_rows) {
     using namespace tc;
-    return d % (512 * S) == 0 && d / S / 32 <= SC_MAX && d / S / KC >= MAX_NST && f % 512 == 0 &&
-           f / 32 <= SC_MAX && f / KC >= MAX_NST && n_rows >= 1;
+    return d % (KC * S) == 0 && d % 128 == 0 && d / S / 32 <= SC_MAX && f % KC == 0 && f % 64 == 0 &&
+           f / 32 <= SC_MAX && n_rows >= 1;
 }
 
 int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool* routed, const int32_t* expert_slot,
@@ -1011,7 +1040,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
     // first pair and pair count share one 32-bit word per expert; a block of up to 5
     // rows runs the 16-column configuration (at most 5 * k experts)
-    if (n_rows * k >= 65536 || E > Cfg<48>::MAX_U || (n_rows <= 5 && n_rows * k > Cfg<16>::MAX_U))
+    if (n_rows * k >= 65536 || E > Cfg<80>::MAX_U || (n_rows <= 5 && n_rows * k > Cfg<32>::MAX_U))
         return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
@@ -1023,12 +1052,12 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     const uint64_t slot = (uint64_t)routed->slot_bytes, ns = (uint64_t)routed->n_slots;
     const char* down_c = pool + 2 * per;
     const char* down_s = down_c + (uint64_t)d * f / 2;
-    const CUtensorMapDataType U4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    {   // 128-K chunks of a code row are 64 bytes apart
-        const uint64_t dims[5] = {128, (uint64_t)f, 2, (uint64_t)d / 128, ns};
-        const uint64_t str[4] = {(uint64_t)d / 2, per, 64, slot};
-        const uint32_t box[5] = {128, 64, 2, KC / 128, 1};
-        if (!map_nd(&p.a_gu, U4, pool, 5, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
+    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    {   // 256-K pieces of a code row are 128 bytes apart; a box is 64 gate + 64 up rows x KCH pieces
+        const uint64_t dims[5] = {128, (uint64_t)f, 2, (uint64_t)d / 256, ns};
+        const uint64_t str[4] = {(uint64_t)d / 2, per, 128, slot};
+        const uint32_t box[5] = {128, 64, 2, KCH, 1};
+        if (!map_nd(&p.a_gu, U8, pool, 5, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
     }
     {
         const uint64_t dims[4] = {(uint64_t)d / 32, (uint64_t)f, 2, ns}, str[3] = {(uint64_t)d / 32, per, slot};
@@ -1036,9 +1065,9 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
         if (!map_nd(&p.s_gu, U8, pool + (uint64_t)f * d / 2, 4, dims, str, box, false)) return MOE_ERR_UNSUPPORTED;
     }
     {
-        const uint64_t dims[4] = {128, (uint64_t)d, (uint64_t)f / 128, ns}, str[3] = {(uint64_t)f / 2, 64, slot};
-        const uint32_t box[4] = {128, 128, KC / 128, 1};
-        if (!map_nd(&p.a_dn, U4, down_c, 4, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
+        const uint64_t dims[4] = {128, (uint64_t)d, (uint64_t)f / 256, ns}, str[3] = {(uint64_t)f / 2, 128, slot};
+        const uint32_t box[4] = {128, 128, KCH, 1};
+        if (!map_nd(&p.a_dn, U8, down_c, 4, dims, str, box, true)) return MOE_ERR_UNSUPPORTED;
     }
     {
         const uint64_t dims[3] = {(uint64_t)f / 32, (uint64_t)d, ns}, str[2] = {(uint64_t)f / 32, slot};
@@ -1074,8 +1103,8 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.y_part = y_part;
     p.dbg_g = reinterpret_cast<float*>(base + L.dbg_g);
     p.dbg_u = reinterpret_cast<float*>(base + L.dbg_u);
-    // a chunk holds at most min(n_rows, 16) pairs: 3 of them per MMA column triple
-    return n_rows <= 5 ? launch<16>(p, stream) : launch<48>(p, stream);
+    // a chunk holds at most min(n_rows, 16) pairs, T MMA columns each
+    return n_rows <= 5 ? launch<32>(p, stream) : launch<80>(p, stream);
 }
 
 }  // namespace moe

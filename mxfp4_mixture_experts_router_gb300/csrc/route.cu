@@ -44,8 +44,8 @@ struct RouteParams {
     int* xexp;
     uint32_t* gu_done;
     uint32_t* hmax;
-    uint8_t* x_mx;        // [3N][d] E4M3 terms of x for the block-scaled expert kernel
-    uint8_t* x_sc;        // [3N][d/32] their E8M0 scales
+    uint8_t* x_mx;        // [MX_TERMS N][d/2] packed E2M1 terms of x for the block-scaled expert kernel
+    uint8_t* x_sc;        // [MX_TERMS N][d/32] their E8M0 scales
     uint32_t* gu_done_tc;
     uint32_t* rbits;      // blocks of more than 32 rows: [groups][E] row bitmaps
     uint32_t* rbits2;
@@ -57,7 +57,7 @@ struct RouteParams {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// E4M3 split of one 1024-element chunk of row n (four blocks per warp, loads
+// E2M1 split of one 1024-element chunk of row n (four blocks per warp, loads
 // first), and the chunk's max |x| published for the row's f16 copy
 constexpr int RT_CHUNK = 1024;
 __device__ void prep_chunk_mx(const RouteParams& p, int n, int c) {
@@ -76,12 +76,12 @@ __device__ void prep_chunk_mx(const RouteParams& p, int n, int c) {
         const int blk = c * (RT_CHUNK / 32) + warp * 4 + i;
         if (blk >= nblk) continue;
         mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-        uint32_t q[3], sb[3];
-        mx3_split(v[i], q, sb);
+        uint32_t q[MX_TERMS], sb[MX_TERMS];
+        mx_split(v[i], q, sb);
 #pragma unroll
-        for (int t = 0; t < 3; t++) {
-            p.x_mx[(size_t)(3 * n + t) * p.d + blk * 32 + lane] = (uint8_t)q[t];
-            if (lane == 0) p.x_sc[(size_t)(3 * n + t) * nblk + blk] = (uint8_t)sb[t];
+        for (int t = 0; t < MX_TERMS; t++) {
+            store_e2m1_block(p.x_mx + (size_t)(MX_TERMS * n + t) * (p.d / 2) + blk * 16, q[t]);
+            if (lane == 0) p.x_sc[(size_t)(MX_TERMS * n + t) * nblk + blk] = (uint8_t)sb[t];
         }
     }
     mx = __reduce_max_sync(0xffffffffu, mx);
@@ -177,7 +177,7 @@ __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N]
     }
     __syncthreads();
     // publish each row's max |x| over this slice, and split the slice's 32-element
-    // blocks of rows n = eg (mod n_eg) into E4M3 terms (all from the staged copy)
+    // blocks of rows n = eg (mod n_eg) into E2M1 terms (all from the staged copy)
     for (int n = warp; n < p.N; n += RT_THREADS / 32) {
         uint32_t mx = 0;
         for (int c = 0; c < per_lane; c++) mx = max(mx, __float_as_uint(xs[(n * 32 + lane) * 17 + c]) & 0x7FFFFFFFu);
@@ -191,13 +191,13 @@ __device__ void gemv_slice(const RouteParams& p, int ks, int eg, float* xs /*[N]
             for (; task < nblk; task += RT_THREADS / 32) {
                 const int el = task * 32 + lane;  // element of the slice
                 const float v = xs[(n * 32 + el / per_lane) * 17 + el % per_lane];
-                uint32_t q[3], sb[3];
-                mx3_split(v, q, sb);
+                uint32_t q[MX_TERMS], sb[MX_TERMS];
+                mx_split(v, q, sb);
                 const int blk = (k0 >> 5) + task;
 #pragma unroll
-                for (int t = 0; t < 3; t++) {
-                    p.x_mx[(size_t)(3 * n + t) * p.d + k0 + el] = (uint8_t)q[t];
-                    if (lane == 0) p.x_sc[(size_t)(3 * n + t) * (p.d / 32) + blk] = (uint8_t)sb[t];
+                for (int t = 0; t < MX_TERMS; t++) {
+                    store_e2m1_block(p.x_mx + (size_t)(MX_TERMS * n + t) * (p.d / 2) + (k0 + task * 32) / 2, q[t]);
+                    if (lane == 0) p.x_sc[(size_t)(MX_TERMS * n + t) * (p.d / 32) + blk] = (uint8_t)sb[t];
                 }
             }
             task -= nblk;
@@ -693,6 +693,8 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     const int b = blockIdx.x;
     // the shared experts of the block may start beside the routing (they need x only)
     griddep_launch_dependents();
+    const bool stamp = tid == 0 && p.n_gemv_ctas > 0;  // timeline of the router-GEMV launch
+    if (stamp) tl_begin(p.ctrl, TL_ROUTE);
 
     if (p.x != nullptr && p.n_gemv_ctas == 0) {  // caller logits: one CTA per (row, chunk)
         const int nc = (p.d + RT_CHUNK - 1) / RT_CHUNK;
@@ -753,7 +755,10 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
     } else {
         group_finisher = true;  // x-preparation-only CTA (or caller logits)
     }
-    if (!group_finisher) return;
+    if (!group_finisher) {
+        if (stamp) tl_end(p.ctrl, TL_ROUTE);
+        return;
+    }
     const bool gemv_finisher = b < p.n_gemv_ctas;
     const int participants = (p.n_gemv_ctas > 0 ? p.n_eg : 0) + ((int)gridDim.x - p.n_gemv_ctas);
     __threadfence();
@@ -783,6 +788,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
         __syncthreads();
         group_block(p, s_cnt, s_bits, s_off, s_idx);
         if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
+        if (stamp) tl_end(p.ctrl, TL_ROUTE);  // the routing is complete
         if (!gemv_finisher) {  // caller logits: every row's f16 copy is already written
             for (int n = tid; n < RT_MAX_ROWS; n += RT_THREADS) p.ctrl[CTRL_XMAX + n] = 0;
             return;
@@ -801,6 +807,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
         for (int n = 0; n < RT_MAX_ROWS; n++) p.ctrl[CTRL_XMAX + n] = 0;
         p.ctrl[CTRL_RT_DONE] = 0;
     }
+    if (stamp) tl_end(p.ctrl, TL_ROUTE);
 }
 
 // ---------------------------------------------------------------------------
@@ -809,7 +816,7 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
 
 // per row (one warp each): the top-k and its weights, and the row's bit in the
 // bitmap of every expert it selected (its 32-row group); the other CTAs split the
-// rows into E4M3 terms for the expert kernel
+// rows into E2M1 terms for the expert kernel
 __global__ void __launch_bounds__(RT_THREADS) route_rows_kernel(const RouteParams p, int n_topk_ctas) {
     __shared__ uint32_t sel[RT_THREADS / 32][64];
     const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
