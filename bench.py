@@ -433,6 +433,15 @@ def run_ours(args, rank, world):
             for n in (2, 4, 8, 16):
                 blocks[f"{n}@{sigma}"] = time_blocks(torch, lay, X, flush, n, sigma, reps=args.block_reps, peak=peak)
 
+    spine = time_spine(torch, flush, peak) if not args.no_blocks else None
+    stacked = None
+    if not args.no_stacked:
+        stacked = run_stacked_legs(torch, args)
+    prefill = None
+    if not args.no_prefill:
+        del flush  # the prefill leg makes its own flush buffer
+        pf = run_prefill_bench(args, pool=(lay.pool, lay.slot_bytes, lay.n_slots))
+        prefill = {"blocks": pf["blocks"], "workload": pf["config"]["workload"], "steps": args.prefill_steps}
     traffic, traffic_note = measured_traffic()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -455,6 +464,9 @@ def run_ours(args, rank, world):
                                    "routed_experts": seg("routed_experts")},
         "kernel_start_end_us_median": offsets,
         "blocks": blocks,
+        "spine_q8_0_matmul": spine,
+        "prefill": prefill,
+        "stacked": stacked,
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": syn.KIMI.d_model * 2,
                 "d2h_bytes_per_step": syn.KIMI.d_model * 2},
         "gpu_launches": K * 4,
@@ -464,6 +476,41 @@ def run_ours(args, rank, world):
         "wall_s_timed_region": wall,
     }
     return line
+
+
+SPINE_SHAPES = [(7168, 1536), (1536, 12288), (8192, 7168)]
+
+
+def time_spine(torch, flush, peak, reps=10):
+    """Q8_0 spine matmuls (q8_0_block_matmul) at attention-projection shapes for blocks
+    of 1, 8 and 16 rows: weight bytes (int8 codes + fp16 scales, each read once per
+    block) / kernel time, L2 flushed before each call, CUDA events around the call."""
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    out = {}
+    for k_in, n_out in SPINE_SHAPES:
+        key = int(syn.stream_key(SEED, 77, k_in, n_out))
+        q = torch.from_numpy((syn.u64(key, 0, n_out * k_in // 8).view(np.int8))).cuda()
+        dq = torch.from_numpy(((1e-3 + 9e-3 * syn.uniform01(key + 1, 0, n_out * k_in // 32)).astype(np.float16))
+                              .view(np.int16)).cuda()
+        wbytes = n_out * k_in + 2 * n_out * (k_in // 32)
+        for n in (1, 8, 16):
+            x = torch.from_numpy(syn.x_rows(SEED, range(n), k_in).view(np.int16)).cuda().view(torch.uint16)
+            ws = torch.zeros(B.q8_0_workspace_size(n, k_in, n_out), dtype=torch.uint8, device="cuda")
+            y = torch.empty((n, n_out), dtype=torch.float32, device="cuda")
+            ts = []
+            for r in range(reps + 3):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                B.q8_0_block_matmul(n, k_in, n_out, x, B.MOE_DTYPE_BF16, q, dq, None, None, B.MOE_EPI_NONE, y, ws)
+                b.record()
+                torch.cuda.synchronize()
+                if r >= 3:
+                    ts.append(a.elapsed_time(b))
+            t = statistics.median(ts)
+            out[f"{k_in}x{n_out}@{n}"] = {"us_median": round(t * 1e3, 2), "gbs": round(wbytes / t / 1e6, 1),
+                                          "frac": round(wbytes / t / 1e6 / peak, 4)}
+    return out
 
 
 def measured_traffic():
@@ -554,112 +601,152 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": "ok", "rows": len(rows), "pool_experts": len(experts)}))
 
 
-def host_topk(logits: np.ndarray, k: int) -> np.ndarray:
-    """The experts each row selects, as the routing kernel selects them (larger logit
-    first, ties to the lower index): what the cache client needs before the layer runs."""
-    order = np.lexsort((np.broadcast_to(np.arange(logits.shape[1]), logits.shape), -logits), axis=1)
-    return order[:, :k]
-
-
-def run_cache_bench(args):
-    """Stacked decode through the device expert cache: `layers` Kimi-shaped MoE layers,
-    8-row blocks, (layer, expert) -> one of `bodies` seeded bodies in a pinned host pool,
-    a device cache of `slots` slots filled on 8 upload streams; logits per layer = a fixed
-    per-layer popularity N(0,1) + a block base that drifts as AR(1) (rho 0.9) + row noise
-    N(0, 0.5).  Both eviction policies run on the same sequence of blocks."""
-    import torch
-    from concurrent.futures import ThreadPoolExecutor
-
-    from mxfp4_mixture_experts_router_gb300 import binding as B
-    from mxfp4_mixture_experts_router_gb300 import build as build_mod
-    from mxfp4_mixture_experts_router_gb300.cache import DeviceExpertCache
-    from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
-
-    build_mod.build()
+def gpu_body_pool(torch, n_bodies: int, seed: int):
+    """n_bodies synthetic MXFP4 expert slabs in a pinned host pool, drawn on the GPU
+    from a seeded generator: uniform code bytes, E8M0 scale bytes 120 + (byte mod 8)
+    (the exponent range of the seeded slabs), then copied to pinned host memory."""
     sh = syn.KIMI
-    E, k, d = sh.n_experts, sh.top_k, sh.d_model
-    L, NB, N, slots = args.cache_layers, args.cache_bodies, 8, args.cache_slots
-    t0 = time.perf_counter()
-    host = torch.empty((NB, SLAB), dtype=torch.uint8).pin_memory()
+    d, f = sh.d_model, sh.d_ff
+    per = f * d // 2 + f * d // 32
+    planes = [(f * d // 2, f * d // 32), (per + f * d // 2, f * d // 32), (2 * per + d * f // 2, d * f // 32)]
+    host = torch.empty((n_bodies, SLAB), dtype=torch.uint8).pin_memory()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    for b0 in range(0, n_bodies, 16):
+        m = min(16, n_bodies - b0)
+        buf = torch.randint(0, 256, (m, SLAB), dtype=torch.uint8, device="cuda", generator=gen)
+        for off, cnt in planes:
+            buf[:, off:off + cnt] = 120 + (buf[:, off:off + cnt] & 7)
+        host[b0:b0 + m].copy_(buf)
+    torch.cuda.synchronize()
+    return host
 
-    def fill(b):
-        host[b].copy_(torch.from_numpy(syn.mxfp4_body_slab(SEED, b, sh)))
 
-    with ThreadPoolExecutor(max_workers=max(2, min(16, os.cpu_count() or 2))) as ex:
-        list(ex.map(fill, range(NB)))
-    setup_s = time.perf_counter() - t0
-    base = host.data_ptr()
-    body = np.array([[syn.body_of(l, e, NB) for e in range(E)] for l in range(L)], dtype=np.uint64)
-    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=N, n_shared=0)
-    x = torch.from_numpy(syn.x_rows(SEED, range(N), d).view(np.int16)).cuda().view(torch.uint16)
-    stage = [torch.empty((L, N, E), dtype=torch.float32).pin_memory() for _ in range(2)]
-    stage_done = [None, None]
-    ld = torch.empty((N, E), dtype=torch.float32, device="cuda")
-    rho, W, K = 0.9, args.cache_warmup, args.cache_blocks
-    out = {}
-    for policy, name in ((B.MOE_CACHE_LRU, "lru"), (B.MOE_CACHE_KEEP_MULTI_ROW, "keep_multi_row")):
-        rng = np.random.default_rng(SEED + 1)
-        bias = rng.normal(size=(L, E)).astype(np.float32)
-        state = rng.normal(size=(L, E)).astype(np.float32)
-        cache = DeviceExpertCache(d, sh.d_ff, E, k, n_slots=slots, n_streams=8, policy=policy)
-        stream = torch.cuda.current_stream()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        unique = 0
-        st0 = None
-        for blk in range(W + K):
-            state = rho * state + np.sqrt(1 - rho * rho) * rng.normal(size=(L, E)).astype(np.float32)
-            lg = bias[:, None, :] + state[:, None, :] + 0.5 * rng.normal(size=(L, N, E)).astype(np.float32)
-            buf = blk & 1
-            if stage_done[buf] is not None:
-                stage_done[buf].synchronize()
-            stage[buf].copy_(torch.from_numpy(lg))
-            if blk == W:
+class StackedDecode:
+    """92 stacked Kimi-shaped MoE layers (routed experts only) served from a device
+    expert cache through the real decode flow (GPU routing -> host slot requests ->
+    resident-first expert kernel).  (layer, expert) maps to one of n_bodies slabs of a
+    pinned host pool; router logits per layer = a fixed per-layer popularity N(0,1) + a
+    block base drifting as AR(1) (rho 0.9) + per-row noise N(0, 0.5)."""
+
+    def __init__(self, torch, args):
+        from mxfp4_mixture_experts_router_gb300.layer import MoeLayer
+        sh = syn.KIMI
+        self.torch = torch
+        self.L, self.NB, self.slots = args.cache_layers, args.cache_bodies, args.cache_slots
+        self.E, self.k, self.d = sh.n_experts, sh.top_k, sh.d_model
+        t0 = time.perf_counter()
+        self.host = gpu_body_pool(torch, self.NB, SEED + 5)
+        base = np.uint64(self.host.data_ptr())
+        body = np.array([[syn.body_of(l, e, self.NB) for e in range(self.E)] for l in range(self.L)], dtype=np.uint64)
+        self.body_ptr = lambda l, ex: (base + body[l, np.asarray(ex, dtype=np.int64)] * np.uint64(SLAB)).astype(np.uint64)
+        self.lay = MoeLayer(self.d, sh.d_ff, self.E, self.k, n_rows_max=16, n_shared=0)
+        self.x = torch.from_numpy(syn.x_rows(SEED, range(16), self.d).view(np.int16)).cuda().view(torch.uint16)
+        self.setup_s = time.perf_counter() - t0
+
+    def logits_stream(self, seed):
+        rng = np.random.default_rng(seed)
+        bias = rng.normal(size=(self.L, self.E)).astype(np.float32)
+        state = rng.normal(size=(self.L, self.E)).astype(np.float32)
+        rho = 0.9
+
+        def next_block(n):
+            nonlocal state
+            state = rho * state + np.sqrt(1 - rho * rho) * rng.normal(size=(self.L, self.E)).astype(np.float32)
+            lg = bias[:, None, :] + state[:, None, :] + 0.5 * rng.normal(size=(self.L, n, self.E)).astype(np.float32)
+            return self.torch.from_numpy(lg).cuda()
+        return next_block
+
+    def run(self, policy, prefetch, n, warm, timed, seed=SEED + 1, plain_rows=None):
+        """Blocks of n rows through all layers; returns seconds per block (median), the
+        cache's counters over the timed blocks and the unique experts per layer."""
+        from mxfp4_mixture_experts_router_gb300.cache import CachedLayerRunner, DeviceExpertCache
+        torch = self.torch
+        cache = DeviceExpertCache(self.d, syn.KIMI.d_ff, self.E, self.k, n_slots=self.slots, n_streams=8,
+                                  policy=policy)
+        runner = CachedLayerRunner(cache, self.lay, self.body_ptr, prefetch=prefetch)
+        nxt = self.logits_stream(seed)
+        secs, unique, st0 = [], 0, None
+        try:
+            for blk in range(warm + timed):
+                lg = nxt(n)
                 torch.cuda.synchronize()
                 cache.sync()
-                st0 = cache.stats()
-                t_wall = time.perf_counter()
-                ev0.record()
-            for l in range(L):
-                idx = host_topk(lg[l], k)
-                experts, rows = np.unique(idx, return_counts=True)
-                if blk >= W:
-                    unique += experts.size
-                ptrs = base + body[l, experts] * np.uint64(SLAB)
-                cache.prepare(l, experts, rows, ptrs, lay, stream)
-                ld.copy_(stage[buf][l], non_blocking=True)
-                lay.forward(x, x, logits_in=ld)
-            ev = torch.cuda.Event()
-            ev.record()
-            stage_done[buf] = ev
-        ev1.record()
-        torch.cuda.synchronize()
-        cache.sync()
-        wall = time.perf_counter() - t_wall
-        sec = ev0.elapsed_time(ev1) * 1e-3
-        st = cache.stats()
-        err = lay.error_bits()
-        up = st["bytes_uploaded"] - st0["bytes_uploaded"]
-        hits, miss = st["hits"] - st0["hits"], st["misses"] - st0["misses"]
-        out[name] = {"tok_s": round(N * K / sec, 2), "block_ms": round(sec / K * 1e3, 2),
-                     "h2d_gbs": round(up / sec / 1e9, 1), "hbm_expert_gbs": round(unique * SLAB / sec / 1e9, 1),
-                     "hits": hits, "misses": miss, "hit_rate": round(hits / max(1, hits + miss), 4),
-                     "unique_experts_per_layer": round(unique / (K * L), 1), "error_bits": err,
-                     "wall_s": round(wall, 3)}
-        cache.close()
-    best = max(out.values(), key=lambda v: v["tok_s"])
-    return {"metric": "stacked decode tok/s through the device expert cache (8-row blocks, all drafts accepted)",
-            "value": best["tok_s"], "unit": "tok/s", "n_gpus": 1, "higher_is_better": True,
-            "config": {"workload": f"{L} Kimi K3.1 MoE layers (routed experts only), 8-row blocks, "
-                                   f"{NB} seeded bodies in a pinned host pool ({NB * SLAB / 1e9:.1f} GB), "
-                                   f"{slots}-slot device cache ({slots * SLAB / 1e9:.1f} GB), 8 upload streams",
-                       "blocks": K, "warmup_blocks": W},
-            "policies": out, "setup_s": round(setup_s, 1), "data": "synthetic"}
+                if blk == warm:
+                    st0 = cache.stats()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for l in range(self.L):
+                    u, _ = runner.run_layer(l, n, self.x, lg[l], self.L)
+                    if blk >= warm:
+                        unique += u
+                b.record()
+                torch.cuda.synchronize()
+                cache.sync()
+                if blk >= warm:
+                    secs.append(a.elapsed_time(b) * 1e-3)
+            st = cache.stats()
+            err = self.lay.error_bits()
+        finally:
+            cache.close()
+        d = {k: st[k] - st0[k] for k in ("hits", "misses", "bytes_uploaded")}
+        t = statistics.median(secs)
+        return {"s_per_block": t, "sum_s": sum(secs), "hits": d["hits"], "misses": d["misses"],
+                "hit_rate": round(d["hits"] / max(1, d["hits"] + d["misses"]), 4),
+                "h2d_gbs": round(d["bytes_uploaded"] / sum(secs) / 1e9, 1),
+                "hbm_expert_gbs": round(unique * SLAB / sum(secs) / 1e9, 1),
+                "unique_experts_per_layer": round(unique / (timed * self.L), 1), "error_bits": err,
+                "prefetched": runner.prefetched, "prefetch_uploads": runner.prefetch_uploads}
 
 
-def run_prefill_bench(args):
-    """Prefill blocks of 270 and 1,533 rows through the layer (routed experts on the
-    block-scaled tcgen05 path), all 896 experts resident, independent N(0,1) router
-    logits per row, L2 flushed before every block outside the events."""
+def run_stacked_legs(torch, args):
+    """The device-expert-cache leg (8-row blocks, both eviction policies, with and
+    without the shallow next-layer prefetch) and the block-verification harness
+    (16-row blocks with synthetic accept-up-to-first-disagreement against 16 plain
+    1-row steps), all through the real decode flow."""
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    sd = StackedDecode(torch, args)
+    out = {"workload": f"{sd.L} Kimi K3.1 MoE layers (routed experts only), {sd.NB} seeded bodies in a pinned "
+                       f"host pool ({sd.NB * SLAB / 1e9:.1f} GB), {sd.slots}-slot device cache "
+                       f"({sd.slots * SLAB / 1e9:.1f} GB), 8 upload streams; per layer: GPU routing -> host "
+                       f"slot requests -> resident-first expert kernel", "setup_s": round(sd.setup_s, 1)}
+    cache = {}
+    for policy, pname in ((B.MOE_CACHE_LRU, "lru"), (B.MOE_CACHE_KEEP_MULTI_ROW, "keep_multi_row")):
+        for pf in (0, 8):
+            r = sd.run(policy, pf, 8, warm=args.cache_warmup, timed=args.cache_blocks)
+            r["tok_s"] = round(8 / r["s_per_block"], 2)
+            cache[f"{pname}{'+prefetch8' if pf else ''}"] = r
+    out["cache_8row_blocks_all_accepted"] = cache
+    # block verification: 16-row blocks, each draft row accepted with probability 0.7 up
+    # to the first rejection (+1 token the block itself yields), against plain steps
+    rng = np.random.default_rng(SEED + 11)
+    blocks = sd.run(B.MOE_CACHE_KEEP_MULTI_ROW, 8, 16, warm=1, timed=args.verify_blocks, seed=SEED + 21)
+    accepted = []
+    for _ in range(max(200, args.verify_blocks)):
+        a = 0
+        while a < 15 and rng.random() < 0.7:
+            a += 1
+        accepted.append(a + 1)
+    tok_per_block = statistics.mean(accepted)
+    plain = sd.run(B.MOE_CACHE_KEEP_MULTI_ROW, 8, 1, warm=2, timed=args.verify_plain_steps, seed=SEED + 21)
+    out["block_verification"] = {
+        "block_rows": 16, "accept_rule": "each draft row accepted with probability 0.7 up to the first rejection",
+        "tokens_per_block_mean": round(tok_per_block, 2),
+        "block_s": round(blocks["s_per_block"], 4), "plain_step_s": round(plain["s_per_block"], 4),
+        "sixteen_plain_steps_s": round(16 * plain["s_per_block"], 4),
+        "tok_s_blocks": round(tok_per_block / blocks["s_per_block"], 2),
+        "tok_s_plain": round(1 / plain["s_per_block"], 2),
+        "block_hit_rate": blocks["hit_rate"], "plain_hit_rate": plain["hit_rate"],
+        "blocks_timed": args.verify_blocks, "plain_steps_timed": args.verify_plain_steps}
+    return out
+
+
+def run_prefill_bench(args, pool=None):
+    """Prefill blocks of 270 and 1,533 rows through the whole layer (routing, routed
+    experts on the block-scaled tcgen05 path, the 2 Q8_0 shared experts, combine), all
+    896 experts resident, independent N(0,1) router logits per row, L2 flushed before
+    every block outside the events.  pool: (tensor, slot_bytes, n_slots) of an
+    existing resident pool to reuse."""
     import torch
 
     from mxfp4_mixture_experts_router_gb300 import binding as B
@@ -671,12 +758,16 @@ def run_prefill_bench(args):
     E, k, d = sh.n_experts, sh.top_k, sh.d_model
     sizes = [int(v) for v in args.prefill_rows.split(",")]
     nmax = max(sizes)
-    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=nmax, n_shared=0)
-    lay.alloc_pool(E)
-    threads = max(2, min(16, os.cpu_count() or 2))
-    for e, slab in syn.mxfp4_slabs_parallel(SEED, range(E), sh, threads=threads):
-        lay.put_slab(e, slab)
+    lay = MoeLayer(d, sh.d_ff, E, k, n_rows_max=nmax, n_shared=2)
+    if pool is None:
+        lay.alloc_pool(E)
+        threads = max(2, min(16, os.cpu_count() or 2))
+        for e, slab in syn.mxfp4_slabs_parallel(SEED, range(E), sh, threads=threads):
+            lay.put_slab(e, slab)
+    else:  # the decode layer's resident pool
+        lay.attach_pool(*pool)
     lay.set_expert_slots(np.arange(E, dtype=np.int32))
+    lay.set_shared([syn.q8_0_shared_slab(SEED, s, sh) for s in range(2)])
     flush = L2Flush(torch, torch.device("cuda"))
     peak, peak_kind = load_peaks()
     res = {}
@@ -701,11 +792,12 @@ def run_prefill_bench(args):
         gbs = u * SLAB / t / 1e9
         res[str(n)] = {"ms_median": round(t * 1e3, 3), "unique_experts": u, "gbs_unique": round(gbs, 1),
                        "frac_of_hbm_peak": round(gbs / peak, 4),
-                       "tflops": round(2 * 3 * n * k * d * sh.d_ff / t / 1e12, 1)}
-    return {"metric": "prefill layer ms and GB/s on unique MXFP4 expert bytes (routed experts)",
+                       "gbs_all_bytes": round((u * SLAB + 2 * Q8_SLAB) / t / 1e9, 1),
+                       "tflops": round(2 * 3 * n * (k + 2) * d * sh.d_ff / t / 1e12, 1)}
+    return {"metric": "prefill layer ms and GB/s on unique MXFP4 expert bytes",
             "unit": "GB/s", "value": res[str(nmax)]["gbs_unique"], "n_gpus": 1,
-            "config": {"workload": "Kimi K3.1 MoE layer prefill, routed experts only (no shared experts), "
-                                   "all 896 experts resident, independent N(0,1) logits per row",
+            "config": {"workload": "Kimi K3.1 MoE layer prefill: routing, 16 routed experts per row, 2 Q8_0 shared "
+                                   "experts, combine; all 896 experts resident, independent N(0,1) logits per row",
                        "rows": sizes, "steps": args.prefill_steps,
                        "l2": "flushed before every block, outside the events"},
             "peak_gbs": peak, "peak_kind": peak_kind, "blocks": res, "data": "synthetic"}
@@ -778,17 +870,21 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-blocks", action="store_true")
     ap.add_argument("--block-reps", type=int, default=10)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-stacked", action="store_true")
+    ap.add_argument("--verify-blocks", type=int, default=2)
+    ap.add_argument("--verify-plain-steps", type=int, default=8)
     ap.add_argument("--_oracle-rows", default="", dest="oracle_rows")
     ap.add_argument("--profile-case", action="store_true",
                     help="run the small ncu case (a few layers, <1 GB on the device) and exit")
     ap.add_argument("--profile-rows", type=int, default=1)
     ap.add_argument("--cache-bench", action="store_true",
-                    help="stacked decode through the device expert cache (one JSON line) and exit")
+                    help="only the stacked legs (device expert cache, block verification; one JSON line) and exit")
     ap.add_argument("--cache-layers", type=int, default=92)
     ap.add_argument("--cache-bodies", type=int, default=1024)
     ap.add_argument("--cache-slots", type=int, default=1567)
-    ap.add_argument("--cache-blocks", type=int, default=4)
-    ap.add_argument("--cache-warmup", type=int, default=2)
+    ap.add_argument("--cache-blocks", type=int, default=2)
+    ap.add_argument("--cache-warmup", type=int, default=1)
     ap.add_argument("--prefill-bench", action="store_true",
                     help="prefill blocks through the layer (one JSON line) and exit")
     ap.add_argument("--prefill-rows", default="270,1533")
@@ -807,7 +903,11 @@ def main():
         return
 
     if args.cache_bench:
-        print(json.dumps(run_cache_bench(args)))
+        import torch
+        from mxfp4_mixture_experts_router_gb300 import build as build_mod
+        build_mod.build()
+        print(json.dumps({"metric": "stacked decode through the device expert cache", "unit": "tok/s",
+                          "n_gpus": 1, "data": "synthetic", "stacked": run_stacked_legs(torch, args)}))
         return
 
     if args.profile_case:

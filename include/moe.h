@@ -81,9 +81,17 @@ extern "C" {
                                       the same stream (which itself directly follows
                                       moe_route): the routed experts' kernel does not
                                       wait for the shared experts to complete before
-                                      it starts (its CTAs get SMs only as the shared
-                                      experts' CTAs leave, each of which has seen the
-                                      routing complete), only before it completes */
+                                      it starts (its CTAs run only once every CTA of
+                                      the shared experts has seen the routing
+                                      complete), only before it completes */
+
+#define MOE_MODE_ORDERED 0x1000 /* routed experts in the order given by the workspace's
+                                   uorder array (moe_ws_offsets.uorder: int32 [U], a
+                                   permutation of 0..U-1, written by the caller after
+                                   moe_route): position p works on expert uexp[uorder[p]].
+                                   Only the schedule changes (e.g. experts already in a
+                                   device cache first, those still uploading last); every
+                                   output is bit-identical to the default order */
 
 /* weight formats of a pool */
 /* bits of a slot's ready flag (moe_expert_block's slot_ready; the device expert cache
@@ -157,6 +165,7 @@ typedef struct moe_ws_offsets {
     int64_t error_word;   /* uint32 */
     int64_t n_unique;     /* int32 U */
     int64_t uexp;         /* int32 [U] selected experts, ascending */
+    int64_t uorder;       /* int32 [E] work order of MOE_MODE_ORDERED (caller-written) */
     int64_t off;          /* int32 [U+1] */
     int64_t pair;         /* int32 [N*k] row*k + slot, grouped by expert */
     int64_t dbg_g;        /* float [pairs][f] gate projection (MOE_MODE_DEBUG_GU) */
@@ -211,10 +220,16 @@ MOE_API int moe_route(const moe_desc* desc, int32_t n_rows,
  * The shared experts alone, straight from the block's rows: they depend on x
  * only, not on the routing ("Run Kimi K3 and K3.1 Pro Locally": every token
  * also runs the 2 shared experts; their matmuls load each weight once for all
- * rows), so this call may run on a second stream while moe_route runs, joining
- * before moe_combine.  It keeps its own copy of the activations and its own
- * counters in the workspace, so it never races with moe_route or with the
- * routed part of moe_expert_block (MOE_MODE_ROUTED_ONLY) on the same workspace.
+ * rows), so this call may run on a second stream while moe_route and the routed
+ * experts run, joining before moe_combine.  It keeps its own copy of the
+ * activations and its own counters in the workspace, so it never races with
+ * moe_route or with the routed part of moe_expert_block (MOE_MODE_ROUTED_ONLY)
+ * on the same workspace.  Any n_rows up to the workspace's n_rows_max: blocks
+ * of up to 16 rows run on the TMA-fed tensor-core engine (one persistent
+ * kernel), larger (prefill) blocks on three register-streaming launches (row
+ * preparation, gate/up with SwiGLU, down) that read the weights from HBM once
+ * and from L2 for every further 16 rows.  A row's result does not depend on
+ * the other rows of its block (within each of the two size classes).
  *
  *  x        bf16 [n_rows][d] (device, 16-byte aligned)
  *  shared   pool of n_shared (1..8) Q8_0 shared experts in slots 0..n_shared-1

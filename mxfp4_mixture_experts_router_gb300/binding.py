@@ -30,6 +30,7 @@ MOE_SLOT_READY = 3
 MOE_MODE_SHARED_ONLY = 0x200
 MOE_MODE_ROUTED_ONLY = 0x400
 MOE_MODE_AFTER_SHARED = 0x800
+MOE_MODE_ORDERED = 0x1000
 MOE_FMT_MXFP4 = 0
 MOE_FMT_Q8_0 = 1
 MOE_EPI_NONE = 0
@@ -60,7 +61,8 @@ class MoePool(ctypes.Structure):
 
 class MoeWsOffsets(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
-                ("error_word", "n_unique", "uexp", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y", "timeline")]
+                ("error_word", "n_unique", "uexp", "uorder", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y",
+                 "timeline")]
 
 
 class MoeCacheStats(ctypes.Structure):

@@ -70,3 +70,77 @@ class DeviceExpertCache:
             self.close()
         except Exception:
             pass
+
+
+class CachedLayerRunner:
+    """Runs stacked MoE layers whose routed experts live in a ``DeviceExpertCache``,
+    in the order a decode engine has to: the routing runs on the GPU, the block's
+    selected experts come back to the host, the cache is asked for their slots
+    (uploading the misses from the pinned host pool on its upload streams), and the
+    expert kernel then runs with the experts already resident first
+    (MOE_MODE_ORDERED) while the misses' slabs are still landing.
+
+    After a layer is enqueued, a shallow prefetch asks for up to ``prefetch`` experts
+    of the next layer: the ones that layer used on the most rows in the previous
+    block (its slabs upload behind the current layer's misses on the same streams).
+
+    body_ptr(layer, experts) -> uint64 numpy array of the experts' pinned host slabs.
+    Pages: "Run Kimi 3.1 locally on one GPU", section "Read the experts the router
+    needs" (experts scheduled after the router selects them, resident experts first,
+    a shallow next-layer prefetch)."""
+
+    def __init__(self, cache: DeviceExpertCache, layer, body_ptr, prefetch: int = 0):
+        self.cache = cache
+        self.layer = layer
+        self.body_ptr = body_ptr
+        self.prefetch = prefetch
+        o = layer.offsets
+        self._o = o
+        self._hdr_bytes = o.off + (layer.E + 1) * 4
+        self._hdr = torch.empty(self._hdr_bytes, dtype=torch.uint8).pin_memory()
+        self._ord = [torch.empty(layer.E, dtype=torch.int32).pin_memory() for _ in range(4)]
+        self._ord_done = [None] * 4
+        self._ord_next = 0
+        self._ev = torch.cuda.Event()
+        self.last_used = {}        # layer -> (experts, rows) of the previous block
+        self.prefetched = 0
+        self.prefetch_uploads = 0
+
+    def run_layer(self, l: int, n: int, x, logits, n_layers: int, stream=None):
+        """One layer for a block of n rows (caller logits on the device); returns the
+        number of unique experts and of those uploaded."""
+        lay = self.layer
+        stream = torch.cuda.current_stream() if stream is None else stream
+        lay.route(n, x, logits_in=logits)
+        self._hdr.copy_(lay.ws[:self._hdr_bytes], non_blocking=True)
+        self._ev.record(stream)
+        self._ev.synchronize()
+        h = self._hdr.numpy()
+        U = int(h[self._o.n_unique:self._o.n_unique + 4].view(np.int32)[0])
+        uexp = h[self._o.uexp:self._o.uexp + 4 * U].view(np.int32)
+        off = h[self._o.off:self._o.off + 4 * (U + 1)].view(np.int32)
+        rows = np.diff(off)
+        slots, miss = self.cache.prepare(l, uexp, rows, self.body_ptr(l, uexp), lay, stream)
+        order = np.argsort(miss, kind="stable").astype(np.int32)  # resident experts first
+        i = self._ord_next
+        self._ord_next = (i + 1) % len(self._ord)
+        if self._ord_done[i] is not None:
+            self._ord_done[i].synchronize()
+        buf = self._ord[i]
+        buf[:U].copy_(torch.from_numpy(order))
+        lay.ws_view(self._o.uorder, U, torch.int32).copy_(buf[:U], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        self._ord_done[i] = ev
+        from . import binding as B
+        lay.experts(n, mode=B.MOE_MODE_DECODE | B.MOE_MODE_ORDERED)
+        lay.combine(n, x)
+        self.last_used[l] = (uexp.copy(), rows.copy())
+        if self.prefetch and l + 1 < n_layers and (l + 1) in self.last_used:
+            e1, r1 = self.last_used[l + 1]
+            top = e1[np.argsort(-r1, kind="stable")[: self.prefetch]]
+            _, up = B.moe_cache_request(self.cache.handle, l + 1, top, np.ones(len(top), np.int32),
+                                        self.body_ptr(l + 1, top), stream)
+            self.prefetched += len(top)
+            self.prefetch_uploads += int(up.sum())
+        return U, int(miss.sum())

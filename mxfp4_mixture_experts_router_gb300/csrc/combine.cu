@@ -99,6 +99,7 @@ extern "C" int moe_workspace_offsets(const moe_desc* desc, int32_t n_rows_max, i
     o->error_word = (int64_t)L.ctrl + 4 * CTRL_ERROR;
     o->n_unique = (int64_t)L.ctrl + 4 * CTRL_UNIQUE;
     o->uexp = (int64_t)L.uexp;
+    o->uorder = (int64_t)L.uorder;
     o->off = (int64_t)L.off;
     o->pair = (int64_t)L.pair;
     o->dbg_g = (int64_t)L.dbg_g;

@@ -36,6 +36,14 @@ enum Ctrl : int {
     CTRL_WORDS = 128
 };
 
+// position p of the routed experts' work order -> index into uexp/off (MOE_MODE_ORDERED),
+// clamped into [0, U) so that a malformed order stays in bounds
+__device__ __forceinline__ int ordered_index(const int* order, int u, int U) {
+    if (order == nullptr) return u;
+    const int v = __ldcg(order + u);
+    return v < 0 ? 0 : (v >= U ? U - 1 : v);
+}
+
 // kernels of the timeline (CTRL_TL)
 enum TlKernel : int { TL_ROUTE = 0, TL_SHARED = 1, TL_ROUTED = 2 };
 
@@ -44,10 +52,13 @@ constexpr int TC_GU_SPLIT = 2;
 // E2M1 terms an activation value is split into for that kernel (each term with
 // its own E8M0 scale per 32 elements): about 16 significant bits survive
 constexpr int MX_TERMS = 5;
+// K slices of the shared experts' gate/up projection
+constexpr int SH_K_SPLIT = 8;
 
 struct WsLayout {
-    size_t ctrl, uexp, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, rbits, rbits2, rbase, total;
+    size_t ctrl, uexp, uorder, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
+        rbits, rbits2, rbase, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -63,6 +74,7 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     const int64_t V = n_shared + (N * k < E ? N * k : E);
     L.ctrl = take(CTRL_WORDS * 4);
     L.uexp = take((size_t)E * 4);
+    L.uorder = take((size_t)E * 4);
     L.off = take((size_t)(E + 1) * 4);
     L.pair = take((size_t)N * k * 4);
     L.x16 = take((size_t)N * d * 2);
@@ -98,6 +110,11 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.gu_done_sh = take(64 * 4);
     L.hmax_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * 4);
     L.h_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
+    // the shared experts' gate/up partial sums [s][f/16 tiles][16-row chunks][K slices][2][16][16]
+    // and per (s, tile, chunk) the slices finished
+    const int64_t sh_units = (int64_t)(n_shared > 0 ? n_shared : 1) * (f / 16) * ((N + 15) / 16);
+    L.sh_part = take((size_t)sh_units * SH_K_SPLIT * 512 * 4);
+    L.sh_cnt = take((size_t)sh_units * 4);
     // grouping of blocks of more than 32 rows: per (32-row group, expert) the bitmap
     // of rows that selected it (zeroed again after use), its copy, and the offset of
     // the group's first pair of the expert
@@ -440,6 +457,11 @@ __device__ __forceinline__ uint32_t lds16(uint32_t addr) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
     return v;
 }
+
+// the shared experts (shared.cu): from the routing kernel's f16 rows (prep = false)
+// or from x through the preparation kernel (prep = true)
+int shared_launch(const moe_desc* desc, int n_rows, int n_rows_max, const uint16_t* x, const moe_pool* shared,
+                  int n_shared, void* ws, bool prep, bool wait_first, cudaStream_t s);
 
 // the block-scaled tensor-core path for routed MXFP4 experts (experts_tc.cu)
 bool tc_expert_supported(int d, int f, int n_rows);

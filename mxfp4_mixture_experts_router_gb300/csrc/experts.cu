@@ -77,6 +77,7 @@ struct ExParams {
     int n_slots;
     uint32_t* ctrl;
     const int* uexp;
+    const int* uorder;   // MOE_MODE_ORDERED: position -> index into uexp/off, else null
     const int* off;
     const int* pair;
     const __half* x16;
@@ -572,7 +573,7 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
         const CUtensorMap* mp = &p.map[shared ? 6 : 0];
         int z = v;
         if (!shared) {
-            const int e = __ldg(p.uexp + (v - S));
+            const int e = __ldg(p.uexp + ordered_index(p.uorder, v - S, V - S));
             z = __ldg(p.expert_slot + e);
             if (z < 0 || z >= p.n_slots) {
                 set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
@@ -701,7 +702,7 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
                 c.pb = m.v * N;
                 c.u_off = 0;
             } else {
-                const int u = m.v - S;
+                const int u = ordered_index(p.uorder, m.v - S, V - S);
                 const int o0 = __ldg(p.off + u), o1 = __ldg(p.off + u + 1);
                 c.r = o1 - o0;
                 c.pb = S * N + o0;
@@ -1231,6 +1232,7 @@ extern "C" int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mo
     p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
     p.uexp = reinterpret_cast<const int*>(base + L.uexp);
     p.off = reinterpret_cast<const int*>(base + L.off);
+    p.uorder = (mode & MOE_MODE_ORDERED) ? reinterpret_cast<const int*>(base + L.uorder) : nullptr;
     p.pair = reinterpret_cast<const int*>(base + L.pair);
     p.x16 = reinterpret_cast<const __half*>(base + L.x16);
     p.xexp = reinterpret_cast<const int*>(base + L.xexp);
@@ -1268,10 +1270,14 @@ static int shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* 
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
     if (desc->group != 32 || d <= 0 || d % 256 || f <= 0 || f % 64 || E <= 0 || E > 1024 || k < 1 || k > 32 || k > E)
         return MOE_ERR_UNSUPPORTED;
-    if (n_rows < 1 || n_rows > 16 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
+    if (n_rows < 1 || n_rows > n_rows_max) return MOE_ERR_UNSUPPORTED;
     if (n_shared < 1 || n_shared > 8) return MOE_ERR_UNSUPPORTED;
     if (!pool_ok(desc, shared, MOE_FMT_Q8_0) || shared->n_slots < n_shared) return MOE_ERR_INVALID_ARG;
     if (((uintptr_t)ws & 255) || ((uintptr_t)x & 15)) return MOE_ERR_INVALID_ARG;
+    // blocks of more than 16 rows (prefill): the register-streaming kernels of shared.cu
+    if (n_rows > 16)
+        return shared_launch(desc, n_rows, n_rows_max, x, shared, n_shared, ws, true, !after_route,
+                             static_cast<cudaStream_t>(stream));
     if (d > F16_ROW_PER * EX_CT * 8) return MOE_ERR_UNSUPPORTED;
 
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);

@@ -105,6 +105,7 @@ struct Params {
     uint32_t* ctrl;
     const int* uexp;
     const int* off;
+    const int* order;      // MOE_MODE_ORDERED: position -> index into uexp/off, else null
     const int* pair;
     uint32_t* gu_done;
     uint32_t* gu_cnt;
@@ -885,9 +886,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     }
     // the set-up above overlaps the previous kernel on the stream; everything below
     // reads the routing's results.  Directly after the shared experts that ran beside
-    // the routing, this CTA only starts once a CTA of theirs has left its SM, and each
-    // of those leaves only after the routing has completed: no wait here (the acquire
-    // below drops stale L1 lines), and the wait for the shared experts is at the end.
+    // the routing, this CTA only starts once a CTA of theirs has triggered its
+    // dependents, which each does only after the routing has completed: no wait here
+    // (the acquire below drops stale L1 lines), and the wait for the shared experts
+    // is at the end.
     if (!p.after_shared) griddep_wait();
     griddep_launch_dependents();
     __shared__ int s_u;
@@ -902,8 +904,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     // every expert's slot and pair range (all loads in flight at once), then the
     // prefix of its chunk counts (one warp: contiguous runs per lane, then a scan)
     for (int u = tid; u < U; u += NTHREADS) {
-        int z = __ldg(p.expert_slot + __ldcg(p.uexp + u));
-        const int o0 = __ldcg(p.off + u), r = __ldcg(p.off + u + 1) - o0;
+        const int ui = ordered_index(p.order, u, U);
+        int z = __ldg(p.expert_slot + __ldcg(p.uexp + ui));
+        const int o0 = __ldcg(p.off + ui), r = __ldcg(p.off + ui + 1) - o0;
         if (z < 0 || z >= p.n_slots) {
             set_error(p.ctrl, MOE_EBIT_BAD_SLOT);
             z = 0;
@@ -1092,6 +1095,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
     p.uexp = reinterpret_cast<const int*>(base + L.uexp);
     p.off = reinterpret_cast<const int*>(base + L.off);
+    p.order = (mode & MOE_MODE_ORDERED) ? reinterpret_cast<const int*>(base + L.uorder) : nullptr;
     p.pair = reinterpret_cast<const int*>(base + L.pair);
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
     p.gu_cnt = reinterpret_cast<uint32_t*>(base + L.gu_cnt);

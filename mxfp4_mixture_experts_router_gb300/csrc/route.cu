@@ -923,6 +923,98 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(const RouteParams p)
 
 using namespace moe;
 
+// ---------------------------------------------------------------------------
+// router GEMM for blocks of more than 32 rows: logit[n][e] = sum_c x[n][c] Wr[e][c]
+// on the tensor cores (bf16 products are exact, fp32 accumulate); the selection
+// then runs on these logits as on caller logits
+// ---------------------------------------------------------------------------
+
+constexpr int RG_TM = 64;     // experts per CTA tile
+constexpr int RG_TN = 64;     // rows per CTA tile
+constexpr int RG_TK = 64;     // K per stage
+constexpr int RG_LD = RG_TK + 8;  // padded smem row (halves): conflict-free fragment loads
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+// D[16x8] += A[16x16] * B[16x8], bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One CTA: 64 experts x 64 rows; warp w: experts 16w..16w+15 x all 64 rows (8 MMA
+// column tiles); K in stages of 64, double-buffered through cp.async.
+__global__ void __launch_bounds__(128) route_gemm_kernel(int d, int E, int N, const uint16_t* __restrict__ x,
+                                                         const uint16_t* __restrict__ w, float* __restrict__ logits) {
+    __shared__ __align__(16) uint16_t sa[2][RG_TM * RG_LD];
+    __shared__ __align__(16) uint16_t sb[2][RG_TN * RG_LD];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, g = lane >> 2, i = lane & 3;
+    const int e0 = blockIdx.x * RG_TM, n0 = blockIdx.y * RG_TN;
+    auto load = [&](int buf, int kc) {
+        // 64 rows x 128 B per operand: 512 pieces of 16 B each, 4 per thread
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const int piece = tid + 128 * t, row = piece >> 3, c8 = (piece & 7) * 8;
+            const int e = e0 + row, n = n0 + row;
+            cp_async16(&sa[buf][row * RG_LD + c8], w + (size_t)(e < E ? e : 0) * d + kc + c8, e < E);
+            cp_async16(&sb[buf][row * RG_LD + c8], x + (size_t)(n < N ? n : 0) * d + kc + c8, n < N);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float acc[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; nt++)
+#pragma unroll
+        for (int t = 0; t < 4; t++) acc[nt][t] = 0.f;
+    const int nk = d / RG_TK;
+    load(0, 0);
+    for (int kc = 0; kc < nk; kc++) {
+        const int buf = kc & 1;
+        if (kc + 1 < nk) {
+            load(buf ^ 1, (kc + 1) * RG_TK);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const uint16_t* A = sa[buf] + (warp * 16) * RG_LD;
+        const uint16_t* Bm = sb[buf];
+#pragma unroll
+        for (int ks = 0; ks < RG_TK / 16; ks++) {
+            const int k = ks * 16 + 2 * i;
+            const uint32_t a0 = *reinterpret_cast<const uint32_t*>(A + g * RG_LD + k);
+            const uint32_t a1 = *reinterpret_cast<const uint32_t*>(A + (g + 8) * RG_LD + k);
+            const uint32_t a2 = *reinterpret_cast<const uint32_t*>(A + g * RG_LD + k + 8);
+            const uint32_t a3 = *reinterpret_cast<const uint32_t*>(A + (g + 8) * RG_LD + k + 8);
+#pragma unroll
+            for (int nt = 0; nt < 8; nt++) {
+                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(Bm + (nt * 8 + g) * RG_LD + k);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(Bm + (nt * 8 + g) * RG_LD + k + 8);
+                mma_bf16(acc[nt], a0, a1, a2, a3, b0, b1);
+            }
+        }
+        __syncthreads();
+    }
+    // C fragment: rows (experts) g and g + 8 of the warp's 16, columns (rows n) 2i, 2i + 1
+#pragma unroll
+    for (int nt = 0; nt < 8; nt++) {
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            const int e = e0 + warp * 16 + g + (t >= 2 ? 8 : 0);
+            const int n = n0 + nt * 8 + 2 * i + (t & 1);
+            if (e < E && n < N) logits[(size_t)n * E + e] = acc[nt][t];
+        }
+    }
+}
+
 extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x, const uint16_t* w_router,
                          const float* logits_in, float* logits_out, int32_t* topk_idx, float* topk_w,
                          void* ws, int32_t n_rows_max, int32_t n_shared, void* stream) {
@@ -933,7 +1025,6 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
         return MOE_ERR_UNSUPPORTED;
     if (n_rows < 1 || n_rows > n_rows_max || n_shared < 0) return MOE_ERR_UNSUPPORTED;
     if (!logits_in && (!x || !w_router)) return MOE_ERR_INVALID_ARG;
-    if (n_rows > RT_MAX_ROWS && !logits_in) return MOE_ERR_UNSUPPORTED;  // the router GEMV serves <= 32 rows
     if (((uintptr_t)ws & 255) || (x && ((uintptr_t)x & 15)) || (w_router && ((uintptr_t)w_router & 15)))
         return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
@@ -969,8 +1060,16 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     p.pairs_cap = L.pairs;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     if (n_rows > RT_MAX_ROWS) {
-        // prefill: top-k and bitmaps per row (+ activation terms), counts and offsets,
-        // then every pair at its place
+        // prefill: the router GEMM (unless the caller gives logits), then top-k and
+        // bitmaps per row (+ activation terms), counts and offsets, then every pair at
+        // its place
+        if (!logits_in) {
+            if (d % RG_TK) return MOE_ERR_UNSUPPORTED;
+            float* lg = logits_out ? logits_out : reinterpret_cast<float*>(base + L.logits);
+            route_gemm_kernel<<<dim3((E + RG_TM - 1) / RG_TM, (n_rows + RG_TN - 1) / RG_TN), 128, 0, cs>>>(
+                d, E, n_rows, x, w_router, lg);
+            p.logits_in = lg;
+        }
         p.n_ks = p.n_eg = p.n_gemv_ctas = 0;
         const int topk_ctas = (n_rows + RT_THREADS / 32 - 1) / (RT_THREADS / 32);
         const int prep = x ? n_rows * ((d + RT_CHUNK - 1) / RT_CHUNK) : 0;

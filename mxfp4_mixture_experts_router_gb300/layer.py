@@ -2,8 +2,8 @@
 
 ``MoeLayer`` owns the device buffers of one layer (router matrix, expert slab
 pool and slot map, shared-expert pool, workspace, per-block outputs) and runs a
-block of rows through ``moe_route`` -> ``moe_expert_block`` -> ``moe_combine``
-on one stream.  PyTorch only allocates memory and provides the stream; every
+block of rows through ``moe_route`` -> ``moe_shared_experts_after_route`` ->
+``moe_expert_block`` (routed experts) -> ``moe_combine`` on one stream.  PyTorch only allocates memory and provides the stream; every
 step runs in the library's kernels.
 """
 
@@ -139,7 +139,7 @@ class MoeLayer:
         and at the end; the middle three on a side branch, so the chained launches of
         the main stream keep overlapping."""
         main = torch.cuda.current_stream()
-        chain = self.n_shared > 0 and (mode & 0xFF) == B.MOE_MODE_DECODE and not (mode & B.MOE_MODE_DEBUG_GU)
+        chain = self.n_shared > 0 and not (mode & B.MOE_MODE_DEBUG_GU)
 
         def mark(ev):
             side = self._side()

@@ -10,6 +10,7 @@ import torch
 
 import moe_synth as syn
 from gpu_util import SeededLayer, assert_close_to_oracle, topk_gap
+from mxfp4_mixture_experts_router_gb300 import binding as B
 from oracle import moe_oracle as orc
 
 pytestmark = pytest.mark.gpu
@@ -151,4 +152,33 @@ def test_chained_layer_equals_sequential_calls(kimi, n):
     torch.cuda.synchronize()
     seq = L.out[:n].view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(chained["out"], seq)
+    assert L.error_bits() == 0
+
+
+def _orders(U, seed):
+    rng = np.random.default_rng(seed)
+    ident = np.arange(U, dtype=np.int32)
+    resident_first = np.concatenate([ident[1::3], ident[0::3], ident[2::3]]).astype(np.int32)
+    return {"reversed": ident[::-1].copy(), "random": rng.permutation(U).astype(np.int32),
+            "resident_first": resident_first}
+
+
+def test_expert_compute_order_does_not_change_bits(kimi):
+    """The routed experts worked in another order (MOE_MODE_ORDERED: reversed, random,
+    a third of them first as a device cache would put its resident experts) give every
+    output bit of the default order ("Run Kimi 3.1 locally on one GPU", section "What
+    is established": outputs match with and without resident-first ordering)."""
+    lay, _, blocks = kimi
+    L = lay.layer
+    n = 8
+    logits = blocks[2.0][:n]
+    x = syn.x_rows(SEED + 9, range(n), KIMI.d_model)
+    base = lay.run(x, x, logits=logits)
+    U = int(L.ws_view(L.offsets.n_unique, 1, torch.int32).item())
+    assert U > 40
+    for name, order in _orders(U, 3).items():
+        L.ws_view(L.offsets.uorder, U, torch.int32).copy_(torch.from_numpy(order))
+        got = lay.run(x, x, logits=logits, mode=B.MOE_MODE_DECODE | B.MOE_MODE_ORDERED)
+        assert np.array_equal(got["out"], base["out"]), name
+        assert np.array_equal(got["y"].view(np.uint32), base["y"].view(np.uint32)), name
     assert L.error_bits() == 0

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import moe_synth as syn
-from gpu_util import SeededLayer, assert_close_to_oracle
+from gpu_util import SeededLayer, assert_close_to_oracle, topk_gap
 from mxfp4_mixture_experts_router_gb300 import binding as B
 from oracle import moe_oracle as orc
 
@@ -73,3 +73,36 @@ def test_prefill_rows_match_oracle(prefill):
         assert_close_to_oracle(blk["out"][r:r + 1], one, f"prefill row {r}")
         rel_y = np.linalg.norm(blk["y"][r] - o["y"][i]) / np.linalg.norm(o["y"][i])
         assert rel_y < 1e-3, (r, rel_y)
+
+
+def test_prefill_whole_layer_router_gemm_and_shared_experts():
+    """A prefill block of 40 rows as a whole layer: the router GEMM (blocks of more
+    than 32 rows), top-16 selection, the routed experts on the block-scaled path and
+    the 2 Q8_0 shared experts for every row, against the oracle on sampled rows.  A
+    Kimi-shaped layer with 64 routed experts keeps the pool and the oracle small."""
+    sh = syn.Shape(d_model=KIMI.d_model, d_ff=KIMI.d_ff, n_experts=64, top_k=16, group=32, n_shared=2)
+    n = 40
+    lay = SeededLayer(sh, seed=43, n_rows_max=n)
+    x = syn.x_rows(43, range(n), sh.d_model)
+    res = syn.x_rows(43, range(n), sh.d_model, tag=syn.TAG_RESIDUAL)
+    g = lay.run(x, res, mode=B.MOE_MODE_PREFILL)
+    assert lay.layer.error_bits() == 0
+    rows = [0, 9, 17, 26, 39]
+    o = lay.oracle(x[rows], res[rows])
+    np.testing.assert_allclose(g["logits"][rows], o["logits"], rtol=0, atol=2e-4)
+    for i, r in enumerate(rows):
+        if topk_gap(o["logits"][i:i + 1], sh.top_k)[0] > 1e-3:
+            assert np.array_equal(g["idx"][r], o["idx"][i]), r
+            want = {"out": o["out"][i:i + 1], "out_bf16": o["out_bf16"][i:i + 1]}
+        else:  # a near tie at the top-16 boundary: compare on the GPU's own logits
+            oo = lay.oracle(x[r:r + 1], res[r:r + 1], logits=g["logits"][r:r + 1])
+            want = {"out": oo["out"], "out_bf16": oo["out_bf16"]}
+        assert_close_to_oracle(g["out"][r:r + 1], want, f"prefill whole layer row {r}")
+    # the shared experts' outputs of every row against the oracle's
+    sy = lay.layer.shared_y(n).cpu().numpy()
+    xf = orc.bf16_bits_to_float(x[rows])
+    for s in range(2):
+        wg, wu, wd = orc.q8_0_expert_mats(lay.shared[s], sh.d_model, sh.d_ff)
+        want = orc.swiglu_expert(xf, wg, wu, wd)[3]
+        err = np.linalg.norm(sy[s][rows] - want) / np.linalg.norm(want)
+        assert err < 1e-4, (s, err)

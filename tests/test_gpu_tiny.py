@@ -257,3 +257,20 @@ def test_topk_expert_count_not_a_multiple_of_four():
         assert np.array_equal(one["w"][0].view(np.uint32), g["w"][r].view(np.uint32)), r
     o = lay.oracle(x, x, logits=lg)
     assert_close_to_oracle(g["out"], o, "30 experts")
+
+
+def test_expert_compute_order_does_not_change_bits_generic_path(tiny):
+    """The same invariance on the engine that serves shapes the block-scaled kernel
+    does not (the tiny layer): reversed and random expert orders."""
+    L = tiny.layer
+    n = 16
+    x = syn.x_rows(14, range(n), TINY.d_model)
+    base = tiny.run(x, x)
+    U = int(L.ws_view(L.offsets.n_unique, 1, torch.int32).item())
+    rng = np.random.default_rng(4)
+    for order in (np.arange(U)[::-1], rng.permutation(U)):
+        L.ws_view(L.offsets.uorder, U, torch.int32).copy_(torch.from_numpy(np.ascontiguousarray(order, np.int32)))
+        got = tiny.run(x, x, mode=B.MOE_MODE_DECODE | B.MOE_MODE_ORDERED)
+        assert np.array_equal(got["out"], base["out"])
+        assert np.array_equal(got["y"].view(np.uint32), base["y"].view(np.uint32))
+    assert L.error_bits() == 0
