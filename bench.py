@@ -652,9 +652,9 @@ class StackedDecode:
 
         def next_block(n):
             nonlocal state
-            state = rho * state + np.sqrt(1 - rho * rho) * rng.normal(size=(self.L, self.E)).astype(np.float32)
-            lg = bias[:, None, :] + state[:, None, :] + 0.5 * rng.normal(size=(self.L, n, self.E)).astype(np.float32)
-            return self.torch.from_numpy(lg).cuda()
+            state = (rho * state + np.sqrt(1 - rho * rho) * rng.normal(size=(self.L, self.E))).astype(np.float32)
+            lg = bias[:, None, :] + state[:, None, :] + 0.5 * rng.normal(size=(self.L, n, self.E))
+            return self.torch.from_numpy(np.ascontiguousarray(lg, dtype=np.float32)).cuda()
         return next_block
 
     def run(self, policy, prefetch, n, warm, timed, seed=SEED + 1, plain_rows=None):

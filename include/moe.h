@@ -60,6 +60,7 @@ extern "C" {
 #define MOE_ERR_CUDA 3          /* a CUDA runtime call failed */
 #define MOE_ERR_TIMEOUT 4       /* device error word: a bounded wait ran out */
 #define MOE_ERR_NAN 5           /* device error word: a NaN logit was seen */
+#define MOE_ERR_IO 6            /* a read of the NVMe expert tier failed */
 
 /* bits of the device error word returned by moe_get_error */
 #define MOE_EBIT_TIMEOUT 0x1u
@@ -414,6 +415,71 @@ MOE_API int moe_cache_request(moe_cache* cache, int32_t layer, int32_t count, co
                       const int32_t* rows, const void* const* host_src, int32_t* slot_out,
                       int32_t* miss_out, void* compute_stream);
 MOE_API int moe_cache_stats_get(const moe_cache* cache, moe_cache_stats* out /* host */);
+
+/* Which of `count` experts of `layer` hold a slot now (host int32 [count], 1 or 0),
+   without touching the cache's state: a caller fetching misses from a lower tier
+   asks this before moe_cache_request_staged. */
+MOE_API int moe_cache_lookup(const moe_cache* cache, int32_t layer, int32_t count, const int32_t* experts,
+                     int32_t* resident_out /* host */);
+
+/*
+ * moe_cache_request for slabs that are still being filled in host memory (by the
+ * NVMe tier below): host_ready[i] points to a uint32 flag in pinned host memory
+ * that receives MOE_SLOT_GATE_UP once the gate/up part of host_src[i] is in place
+ * and MOE_SLOT_DOWN once the rest is.  Before each chunk's copy the upload stream
+ * runs a host function that waits for the chunk's bit (bounded: 10 s), so the
+ * call returns at once, the chunks move as soon as they have been read, and the
+ * GPU never waits on host memory.  The NVMe tier sets both bits even when a read
+ * fails (with MOE_NVME_FAILED).  Other arguments as moe_cache_request.
+ */
+MOE_API int moe_cache_request_staged(moe_cache* cache, int32_t layer, int32_t count, const int32_t* experts,
+                      const int32_t* rows, const void* const* host_src,
+                      const uint32_t* const* host_ready, int32_t* slot_out,
+                      int32_t* miss_out, void* compute_stream);
+
+/*
+ * NVMe expert tier (host side).  The expert slabs live in files, one per drive,
+ * each drive holding a replica of the same n_bodies slabs (slab b at byte offset
+ * b * slab_stride).  Pages: "Run Kimi 3.1 locally on one GPU", section "Read the
+ * experts the router needs" (experts on several NVMe drives read with O_DIRECT
+ * into pinned memory, per-drive concurrency caps, replica choice by expected
+ * completion time, decode fills in two chunks).
+ *
+ * moe_nvme_open: n_replicas files (the same slabs on each), depth reader threads
+ *   per file (its cap on reads in flight).  O_DIRECT is used where the file system
+ *   allows it and the read is 4 KiB aligned (buffer, offset, length), buffered
+ *   reads otherwise.  Files shorter than the slabs they must hold: MOE_ERR_INVALID_ARG.
+ * moe_nvme_read: queues the read of slab `body` into host memory dst (pinned, at
+ *   least slab_bytes), first the bytes [0, first_bytes) then the rest, on the
+ *   replica whose pending bytes plus this read, over its measured bandwidth, is
+ *   smallest (*replica_out, may be NULL).  *flag (host) is zeroed, then gets
+ *   MOE_SLOT_GATE_UP after the first chunk and MOE_SLOT_READY after the whole
+ *   slab, plus MOE_NVME_FAILED if a read failed.  Returns at once.
+ * moe_nvme_wait: host wait until (*flag & bits) == bits (MOE_ERR_TIMEOUT after
+ *   timeout_ns; MOE_ERR_IO if the read failed).
+ * moe_nvme_close waits for every queued read, then closes the files.
+ */
+#define MOE_NVME_FAILED 0x80000000u
+
+typedef struct moe_nvme moe_nvme;
+
+typedef struct moe_nvme_stats {
+    int64_t reads;
+    int64_t bytes;
+    int64_t failures;
+    int64_t pending_bytes;
+    double bandwidth;      /* bytes/s, exponentially weighted over completed reads */
+    double busy_seconds;   /* summed read time of its threads */
+    int32_t direct;        /* 1 if the file was opened with O_DIRECT */
+} moe_nvme_stats;
+
+MOE_API int moe_nvme_open(const char* const* paths /* host */, int32_t n_replicas, int64_t slab_bytes,
+                  int64_t slab_stride, int32_t n_bodies, int32_t depth, moe_nvme** out /* host */);
+MOE_API int moe_nvme_read(moe_nvme* nvme, int32_t body, void* dst, int64_t first_bytes,
+                  volatile uint32_t* flag, int32_t* replica_out);
+MOE_API int moe_nvme_wait(const volatile uint32_t* flag, uint32_t bits, int64_t timeout_ns);
+MOE_API int moe_nvme_stats_get(moe_nvme* nvme, int32_t replica, moe_nvme_stats* out /* host */);
+MOE_API int moe_nvme_close(moe_nvme* nvme);
 MOE_API int moe_cache_sync(moe_cache* cache);
 MOE_API int moe_cache_destroy(moe_cache* cache);
 

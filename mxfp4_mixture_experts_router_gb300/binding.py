@@ -46,6 +46,8 @@ EXPORTED = [
     "moe_combine", "q8_0_workspace_size", "q8_0_block_matmul", "moe_get_error", "moe_device_sm_count",
     "q8_0_block_matmul_noalloc", "q8_0_noalloc_get_error", "moe_shared_experts", "moe_shared_experts_after_route",
     "moe_cache_create", "moe_cache_request", "moe_cache_stats_get", "moe_cache_sync", "moe_cache_destroy",
+    "moe_cache_request_staged", "moe_cache_lookup", "moe_nvme_open", "moe_nvme_read", "moe_nvme_wait", "moe_nvme_stats_get",
+    "moe_nvme_close",
 ]
 
 
@@ -63,6 +65,12 @@ class MoeWsOffsets(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("error_word", "n_unique", "uexp", "uorder", "off", "pair", "dbg_g", "dbg_u", "h", "shared_y",
                  "timeline")]
+
+
+class MoeNvmeStats(ctypes.Structure):
+    _fields_ = [("reads", ctypes.c_int64), ("bytes", ctypes.c_int64), ("failures", ctypes.c_int64),
+                ("pending_bytes", ctypes.c_int64), ("bandwidth", ctypes.c_double), ("busy_seconds", ctypes.c_double),
+                ("direct", ctypes.c_int32)]
 
 
 class MoeCacheStats(ctypes.Structure):
@@ -105,6 +113,13 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_stats_get.argtypes = [P, ctypes.POINTER(MoeCacheStats)]
         L.moe_cache_sync.argtypes = [P]
         L.moe_cache_destroy.argtypes = [P]
+        L.moe_cache_request_staged.argtypes = [P, I32, I32, P, P, P, P, P, P, P]
+        L.moe_cache_lookup.argtypes = [P, I32, I32, P, P]
+        L.moe_nvme_open.argtypes = [P, I32, I64, I64, I32, I32, ctypes.POINTER(P)]
+        L.moe_nvme_read.argtypes = [P, I32, P, I64, P, P]
+        L.moe_nvme_wait.argtypes = [P, ctypes.c_uint32, I64]
+        L.moe_nvme_stats_get.argtypes = [P, I32, ctypes.POINTER(MoeNvmeStats)]
+        L.moe_nvme_close.argtypes = [P]
         L.moe_combine.argtypes = [D, I32, P, P, P, P, I32, P, P]
         L.q8_0_workspace_size.argtypes = [I32, I32, I32]
         L.q8_0_workspace_size.restype = SZ
@@ -283,3 +298,69 @@ def moe_cache_sync(handle: int):
 
 def moe_cache_destroy(handle: int):
     _check(lib().moe_cache_destroy(ctypes.c_void_p(handle)), "moe_cache_destroy")
+
+
+# --- NVMe expert tier ------------------------------------------------------------
+
+MOE_NVME_FAILED = 0x80000000
+MOE_ERR_IO = 6
+
+
+def moe_nvme_open(paths, slab_bytes: int, slab_stride: int, n_bodies: int, depth: int) -> int:
+    """Opaque handle (an int) of an expert store replicated over the given files."""
+    arr = (ctypes.c_char_p * len(paths))(*[p.encode() for p in paths])
+    h = ctypes.c_void_p()
+    _check(lib().moe_nvme_open(ctypes.cast(arr, ctypes.c_void_p), len(paths), slab_bytes, slab_stride, n_bodies,
+                               depth, ctypes.byref(h)), "moe_nvme_open")
+    return h.value
+
+
+def moe_nvme_read(handle: int, body: int, dst_addr: int, first_bytes: int, flag_addr: int) -> int:
+    """Queue one slab read into host memory at dst_addr; returns the replica chosen."""
+    rep = ctypes.c_int32(-1)
+    _check(lib().moe_nvme_read(ctypes.c_void_p(handle), body, ctypes.c_void_p(dst_addr), first_bytes,
+                               ctypes.c_void_p(flag_addr), ctypes.byref(rep)), "moe_nvme_read")
+    return rep.value
+
+
+def moe_nvme_wait(flag_addr: int, bits: int, timeout_ns: int = 10_000_000_000) -> int:
+    """MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_IO (returned, not raised)."""
+    return lib().moe_nvme_wait(ctypes.c_void_p(flag_addr), bits, timeout_ns)
+
+
+def moe_nvme_stats(handle: int, replica: int) -> dict:
+    st = MoeNvmeStats()
+    _check(lib().moe_nvme_stats_get(ctypes.c_void_p(handle), replica, ctypes.byref(st)), "moe_nvme_stats_get")
+    return {f: getattr(st, f) for f, _ in MoeNvmeStats._fields_}
+
+
+def moe_nvme_close(handle: int):
+    _check(lib().moe_nvme_close(ctypes.c_void_p(handle)), "moe_nvme_close")
+
+
+def moe_cache_request_staged(handle: int, layer: int, experts, rows, host_src, host_ready, stream=None):
+    """moe_cache_request whose slabs may still be landing in host memory: host_ready is a
+    numpy uint64 array of the addresses of their pinned uint32 ready flags."""
+    import numpy as np
+    e = np.ascontiguousarray(experts, dtype=np.int32)
+    n = int(e.shape[0])
+    r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
+    src = np.ascontiguousarray(host_src, dtype=np.uint64)
+    rdy = np.ascontiguousarray(host_ready, dtype=np.uint64)
+    slots = np.empty(n, dtype=np.int32)
+    miss = np.empty(n, dtype=np.int32)
+    _check(lib().moe_cache_request_staged(ctypes.c_void_p(handle), layer, n, e.ctypes.data,
+                                          None if r is None else r.ctypes.data, src.ctypes.data, rdy.ctypes.data,
+                                          slots.ctypes.data, miss.ctypes.data, _cache_stream(stream)),
+           "moe_cache_request_staged")
+    return slots, miss
+
+
+def moe_cache_lookup(handle: int, layer: int, experts):
+    """1 where the (layer, expert) slab holds a device slot now, else 0 (no side effects)."""
+    import numpy as np
+    e = np.ascontiguousarray(experts, dtype=np.int32)
+    out = np.empty(e.shape[0], dtype=np.int32)
+    _check(lib().moe_cache_lookup(ctypes.c_void_p(handle), layer, int(e.shape[0]), e.ctypes.data, out.ctypes.data),
+           "moe_cache_lookup")
+    return out

@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "_moe_gb300.so")
-SOURCES = ["route.cu", "experts.cu", "experts_tc.cu", "shared.cu", "combine.cu", "cache.cu"]
+SOURCES = ["route.cu", "experts.cu", "experts_tc.cu", "shared.cu", "combine.cu", "cache.cu", "nvme.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

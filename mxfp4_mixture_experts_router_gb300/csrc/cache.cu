@@ -25,12 +25,15 @@
 // no CUDA calls): the policy logic runs the same way without a GPU.
 #include "common.cuh"
 
+#include <chrono>
 #include <list>
 #include <new>
+#include <thread>
 #include <unordered_map>
 #include <vector>
 
 typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
 
 __global__ void cache_flag_kernel(uint32_t* flag, uint32_t value) { *flag = value; }
 
@@ -106,6 +109,35 @@ int write_flag(moe_cache* c, cudaStream_t s, uint32_t* flag, uint32_t value) {
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// A host function on an upload stream that returns once (*flag & bits) != 0: the
+// stream's next copy then reads a chunk the lower tier has finished writing.  The
+// wait is bounded (10 s), so the stream always moves on; the GPU itself never waits
+// on host memory.
+struct HostWait {
+    const uint32_t* flag;
+    uint32_t bits;
+};
+
+void CUDART_CB host_wait(void* arg) {
+    HostWait* w = static_cast<HostWait*>(arg);
+    const auto t0 = std::chrono::steady_clock::now();
+    while ((__atomic_load_n(w->flag, __ATOMIC_ACQUIRE) & w->bits) == 0u) {
+        if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) break;
+        std::this_thread::yield();
+    }
+    delete w;
+}
+
+int enqueue_host_wait(cudaStream_t s, const uint32_t* flag, uint32_t bits) {
+    HostWait* w = new (std::nothrow) HostWait{flag, bits};
+    if (!w) return MOE_ERR_CUDA;
+    if (cudaLaunchHostFunc(s, host_wait, w) != cudaSuccess) {
+        delete w;
+        return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
 void release(moe_cache* c) {
     for (cudaStream_t s : c->streams) {
         cudaStreamSynchronize(s);
@@ -144,6 +176,7 @@ extern "C" int moe_cache_create(const moe_desc* desc, void* slot_base, int64_t s
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             c->write_value = reinterpret_cast<WriteValue32Fn>(fn);
+
         for (int i = 0; i < n_streams; i++) {
             cudaStream_t s;
             if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) {
@@ -170,9 +203,9 @@ extern "C" int moe_cache_create(const moe_desc* desc, void* slot_base, int64_t s
     return MOE_OK;
 }
 
-extern "C" int moe_cache_request(moe_cache* c, int32_t layer, int32_t count, const int32_t* experts,
-                                 const int32_t* rows, const void* const* host_src, int32_t* slot_out,
-                                 int32_t* miss_out, void* compute_stream) {
+static int cache_request(moe_cache* c, int32_t layer, int32_t count, const int32_t* experts, const int32_t* rows,
+                         const void* const* host_src, const uint32_t* const* host_ready, int32_t* slot_out,
+                         int32_t* miss_out, void* compute_stream) {
     if (!c || count < 0 || (count > 0 && (!experts || !slot_out))) return MOE_ERR_INVALID_ARG;
     if (count > c->n_slots) return MOE_ERR_UNSUPPORTED;
     const bool gpu = !c->streams.empty();
@@ -238,14 +271,39 @@ extern "C" int moe_cache_request(moe_cache* c, int32_t layer, int32_t count, con
         char* dst = c->base + (size_t)s * (size_t)c->slot_bytes;
         const char* src = static_cast<const char*>(host_src[i]);
         if (!src) return MOE_ERR_INVALID_ARG;
+        const uint32_t* hr = host_ready ? host_ready[i] : nullptr;
+        // a slab still being read into host memory: each chunk waits for its bit
+        if (hr && enqueue_host_wait(us, hr, MOE_SLOT_GATE_UP) != MOE_OK) return MOE_ERR_CUDA;
         if (cudaMemcpyAsync(dst, src, (size_t)c->gu_bytes, cudaMemcpyHostToDevice, us) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (write_flag(c, us, c->ready + s, MOE_SLOT_GATE_UP) != MOE_OK) return MOE_ERR_CUDA;
+        if (hr && enqueue_host_wait(us, hr, MOE_SLOT_DOWN) != MOE_OK) return MOE_ERR_CUDA;
         if (cudaMemcpyAsync(dst + c->gu_bytes, src + c->gu_bytes, (size_t)(c->slab_bytes - c->gu_bytes),
                             cudaMemcpyHostToDevice, us) != cudaSuccess)
             return MOE_ERR_CUDA;
         if (write_flag(c, us, c->ready + s, MOE_SLOT_READY) != MOE_OK) return MOE_ERR_CUDA;
     }
+    return MOE_OK;
+}
+
+extern "C" int moe_cache_request(moe_cache* c, int32_t layer, int32_t count, const int32_t* experts,
+                                 const int32_t* rows, const void* const* host_src, int32_t* slot_out,
+                                 int32_t* miss_out, void* compute_stream) {
+    return cache_request(c, layer, count, experts, rows, host_src, nullptr, slot_out, miss_out, compute_stream);
+}
+
+extern "C" int moe_cache_request_staged(moe_cache* c, int32_t layer, int32_t count, const int32_t* experts,
+                                        const int32_t* rows, const void* const* host_src,
+                                        const uint32_t* const* host_ready, int32_t* slot_out, int32_t* miss_out,
+                                        void* compute_stream) {
+    if (count > 0 && !host_ready) return MOE_ERR_INVALID_ARG;
+    return cache_request(c, layer, count, experts, rows, host_src, host_ready, slot_out, miss_out, compute_stream);
+}
+
+extern "C" int moe_cache_lookup(const moe_cache* c, int32_t layer, int32_t count, const int32_t* experts,
+                                int32_t* resident_out) {
+    if (!c || count < 0 || (count > 0 && (!experts || !resident_out))) return MOE_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < count; i++) resident_out[i] = c->where.count(cache_key(layer, experts[i])) ? 1 : 0;
     return MOE_OK;
 }
 

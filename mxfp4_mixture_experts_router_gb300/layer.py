@@ -96,6 +96,11 @@ class MoeLayer:
 
     # --- the layer -------------------------------------------------------------
     def route(self, n_rows: int, x, logits_in=None, stream=None):
+        if logits_in is not None and (logits_in.dtype != torch.float32 or not logits_in.is_contiguous()
+                                      or logits_in.numel() < n_rows * self.E):
+            raise ValueError("logits_in must be a contiguous float32 tensor of n_rows x n_experts")
+        if x.element_size() != 2 or not x.is_contiguous():
+            raise ValueError("x must be contiguous bf16 rows (2-byte elements)")
         B.moe_route(self.desc, n_rows, x, self.router if logits_in is None else None, logits_in,
                     self.logits if logits_in is None else None, self.topk_idx, self.topk_w, self.ws,
                     self.n_rows_max, self.n_shared, stream)
