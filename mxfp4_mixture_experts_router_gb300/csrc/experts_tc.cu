@@ -79,10 +79,14 @@ struct Cfg {
     static constexpr uint32_t TM_COLS = TM_SFB + NST * SF_COLS <= 256 ? 256 : 512;
     // per expert: (slot, first pair | pairs << 16) and the prefix of its chunk counts
     static constexpr int MAX_U = NBM == 32 ? 128 : 1024;
-    // blocks of up to 5 rows: the block row of every (row, slot) pair (5 x k <= 160)
+    // blocks of up to 5 rows: the block row of every (row, slot) pair (5 x k <= 160);
+    // then the block rows of the pairs of the chunks in the two scale buffers' items
     static constexpr int TOKS = NBM == 32 ? 160 : 0;
-    static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 12;
-    static constexpr size_t SMEM = (size_t)NST * STAGE + 2 * SCB + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
+    static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 2 * CHUNK * 2 + 12;
+    // each scale-mover warp's staging of the activation scale bytes, per stage
+    static constexpr int SBS_BYTES = 4 * NST * NBM * 16;
+    static constexpr size_t SMEM =
+        (size_t)NST * STAGE + 2 * SCB + SBS_BYTES + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
     static_assert(TM_SFB + NST * SF_COLS <= TM_COLS && NBM <= ACC_COLS && NBM <= 128, "tensor memory columns");
@@ -251,6 +255,7 @@ __device__ bool wait_bits(const Params& p, const uint32_t* flag, uint32_t bits) 
 // a claimed work item, decoded: its type, chunk, block, K split, slot and pairs
 struct Plan {
     int item, type, cid, blk, split, z, p0, rc;
+    int pv[CHUNK];  // gate/up items of blocks without a pair table in shared memory: the chunk's pairs
 };
 
 __device__ __forceinline__ void plan_item(const Params& p, int V, int U, const uint2* umeta, const int* cp, int item,
@@ -264,6 +269,17 @@ __device__ __forceinline__ void plan_item(const Params& p, int V, int U, const u
     q.z = (int)mu.x;
     q.p0 = o0 + CHUNK * (q.cid - cp[u]);  // the chunk's first pair
     q.rc = min(CHUNK, o0 + r - q.p0);     // and its pairs
+}
+
+// the chunk's pair entries (gate/up items gather the rows of their tokens); loaded
+// one item ahead, written for the scale movers at the item's first stage
+__device__ __forceinline__ void plan_pairs(const Params& p, int total, Plan& q) {
+#pragma unroll
+    for (int i = 0; i < CHUNK; i++) q.pv[i] = 0;
+    if (q.item >= total || q.type != IT_GU) return;
+#pragma unroll
+    for (int i = 0; i < CHUNK; i++)
+        if (i < q.rc) q.pv[i] = __ldcg(p.pair + q.p0 + i);
 }
 
 // bounded wait until *flag >= target; false (with the timeout bit set) if it gave up
@@ -286,7 +302,7 @@ __device__ bool wait_at_least(const Params& p, const uint32_t* flag, uint32_t ta
 template <int NBM>
 __device__ void producer(const Params& p, int U, const uint2* umeta, const int* cp, unsigned char* smem,
                          unsigned char* scbuf, uint64_t* full, uint64_t* empty, uint64_t* mready, uint64_t* scf,
-                         uint64_t* sce, Meta* meta, int first) {
+                         uint64_t* sce, Meta* meta, int first, uint16_t* tokb) {
     using C = Cfg<NBM>;
     tma_prefetch_desc(&p.a_gu);
     tma_prefetch_desc(&p.a_dn);
@@ -303,6 +319,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
     // decoding) waits in line with the stages.
     Plan cur, nxt;
     plan_item(p, V, U, umeta, cp, first, total, cur);
+    if (tokb != nullptr) plan_pairs(p, total, cur);
     int claim_next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
     uint32_t dep_cur = 0u;  // the current item's dependency word as last read
     if (cur.item < total) {
@@ -367,6 +384,11 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
                     break;
                 }
                 mbar_arrive_expect_tx(&scf[sbuf], tx_sc);
+                if (gu && tokb != nullptr) {  // the chunk's tokens, read by the scale movers after the claim
+#pragma unroll
+                    for (int i = 0; i < CHUNK; i++)
+                        if (i < rc) tokb[sbuf * CHUNK + i] = (uint16_t)(cur.pv[i] / p.k);
+                }
                 if (gu)
                     tma_load_4d(sa, &p.s_gu, &scf[sbuf], kbase / 32, row0, 0, z);
                 else
@@ -395,6 +417,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
                 // one item ago) with its dependency load, which lands during this item
                 claim_after = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
                 plan_item(p, V, U, umeta, cp, claim_next, total, nxt);
+                if (tokb != nullptr) plan_pairs(p, total, nxt);
                 if (nxt.item < total) {
                     if (p.slot_ready != nullptr) dep_nxt = ld_acquire(p.slot_ready + nxt.z);
                     else if (nxt.type != IT_GU) dep_nxt = ld_acquire(p.gu_done + nxt.cid);
@@ -421,30 +444,31 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
         if (sc_any & (1u << b)) mbar_wait(&scf[b], ((sc_cnt >> b) & 1u) ^ 1u);
 }
 
-// One stage's activation operand, held in registers between its loads and its
-// stores: 16-byte piece j = t + 128 i (row j / (8 KCH), piece j % (8 KCH) of the
-// row's KC/2 packed bytes) of this thread t, and the stage's KC/32 scale bytes of
-// rows lane, 32 + lane and 64 + lane (every warp loads the scales its own lane
-// quadrant needs).
+// The activation operand of a stage (B) is copied by the four scale-mover warps
+// straight from global memory into the stage's shared memory (16-byte cp.async,
+// L2 only) as soon as the producer has claimed the stage, so the copies of every
+// claimed stage are in flight at once and their latency hides behind the ring.
+// Thread t copies 16-byte pieces j = t + 128 i (row j / (8 KCH), piece j % (8 KCH)
+// of the row's KC/2 packed bytes) into the 128-byte-swizzled K-major layout the
+// MMA reads (KCH regions of NBM rows of 128 bytes, piece cc of row r at
+// 16 * (cc ^ (r % 8))).  Every warp also copies the stage's E8M0 scale bytes of
+// activation rows lane, 32 + lane and 64 + lane into its own staging area, so
+// each lane later reads only what it copied itself.
 constexpr int BP = 8 * KCH;  // 16-byte pieces of a B row per stage
-template <int NBM>
-struct BStage {
-    uint4 d[NBM * BP / 128];
-    uint4 s[3];
-};
 
 // source row of activation row `row` of a stage: gate/up gathers the E2M1 terms of
 // the block rows of the chunk's pairs (T x the pair's token + term), down reads the
-// chunk's rows of h (T x pair + term) in place
-__device__ __forceinline__ int b_src_row(const Params& p, const Meta& m, int row, const uint16_t* tok) {
+// chunk's rows of h (T x pair + term) in place.  tok: the block row of every pair
+// (small blocks); else tokb, the block rows of the chunk's pairs (from the producer)
+__device__ __forceinline__ int b_src_row(const Meta& m, int row, const uint16_t* tok, const uint16_t* tokb) {
     if (m.type != IT_GU) return m.brow + row;
     const int q = row / T;
-    const int n = tok != nullptr ? (int)tok[m.p0 + q] : __ldcg(p.pair + m.p0 + q) / p.k;
+    const int n = tok != nullptr ? (int)tok[m.p0 + q] : (int)tokb[m.sbuf * CHUNK + q];
     return T * n + (row - T * q);
 }
 
-// the source rows this thread reads for an item (data rows j / BP of its pieces j,
-// scale rows lane, 32 + lane and 64 + lane), resolved once per item
+// the source rows this thread copies for an item (data rows j / BP of its pieces
+// j, scale rows lane, 32 + lane and 64 + lane), resolved once per item
 template <int NBM>
 struct BRows {
     int item = -1;
@@ -452,118 +476,128 @@ struct BRows {
     int s[3];
 };
 
-template <int NBM>
-__device__ __forceinline__ void b_rows(const Params& p, const Meta& m, int t, int lane, BRows<NBM>& r,
-                                       const uint16_t* tok) {
-    if (r.item == m.item) return;
-    r.item = m.item;
-#pragma unroll
-    for (int i = 0; i < NBM * BP / 128; i++) {
-        const int row = (t + 128 * i) / BP;
-        r.d[i] = row < m.nrow ? b_src_row(p, m, row, tok) : 0;
-    }
-#pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const int row = 32 * c + lane;
-        r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(p, m, row, tok) : 0;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait(int pending) {
+    switch (pending) {  // the oldest group of the thread is complete once at most `pending` remain
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
     }
 }
 
-// the lines b_load will read for stage `chunk` of item m, into L1 (one prefetch per
-// 128-byte row of packed activation codes, one per scale row); rows from r
+// issue the copies of one claimed stage (one cp.async group per thread and stage)
 template <int NBM>
-__device__ __forceinline__ void b_prefetch(const Params& p, const Meta& m, int chunk, int t, int lane,
-                                           const BRows<NBM>& r) {
-    const bool gu = m.type == IT_GU;
-    const uint8_t* src = gu ? p.x_mx : p.h_mx;
-    const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
-    const int ld = gu ? p.d : p.f;
-    const int k0 = m.kbase + chunk * KC;
-#pragma unroll
-    for (int i = 0; i < NBM * BP / 128; i++) {
-        const int j = t + 128 * i, row = j / BP, c16 = j % BP;
-        if (row < m.nrow && (c16 & 7) == 0)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(src + (size_t)r.d[i] * (ld / 2) + k0 / 2 + c16 * 16));
-    }
-#pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const int row = 32 * c + lane;
-        if (row < m.nrow && row < NBM)
-            asm volatile("prefetch.global.L1 [%0];" ::"l"(ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32));
-    }
-}
-
-template <int NBM>
-__device__ __forceinline__ void b_load(const Params& p, const Meta& m, int chunk, int t, int lane, BStage<NBM>& b,
-                                       BRows<NBM>& rows, const uint16_t* tok) {
-    b_rows<NBM>(p, m, t, lane, rows, tok);
-    const bool gu = m.type == IT_GU;
-    const uint8_t* src = gu ? p.x_mx : p.h_mx;
-    const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
-    const int ld = gu ? p.d : p.f;
-    const int k0 = m.kbase + chunk * KC;
-#pragma unroll
-    for (int i = 0; i < NBM * BP / 128; i++) {
-        const int j = t + 128 * i, row = j / BP, c16 = j % BP;
-        b.d[i] = row < m.nrow
-                     ? __ldca(reinterpret_cast<const uint4*>(src + (size_t)rows.d[i] * (ld / 2) + k0 / 2 + c16 * 16))
-                     : make_uint4(0, 0, 0, 0);
-    }
-    static_assert(KC / 32 == 16, "one 16-byte scale load per row and stage");
-#pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const int row = 32 * c + lane;
-        b.s[c] = (row < m.nrow && row < NBM)
-                     ? __ldca(reinterpret_cast<const uint4*>(ssrc + (size_t)rows.s[c] * (ld / 32) + k0 / 32))
-                     : make_uint4(0, 0, 0, 0);
-    }
-}
-
-// warps 2..5: per stage, the activation rows into the stage's B area (the
-// 128-byte-swizzled K-major layout the MMA reads: KCH regions of NBM rows of 128
-// packed bytes, piece cc of row r at 16 * (cc ^ (r % 8))) and every E8M0 scale
-// into tensor memory.  Scale of row m (A: weight row, B: activation row) for the stage's K
-// blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word at lane m % 32,
-// column base + set*4 + m / 32; each warp writes the copy in its own lane
-// quadrant.  A stage is prepared as soon as the producer has claimed it (its
-// codes may still be in flight); the next stage's activations are loaded ahead
-// when it belongs to the same item.  After an item's last stage the warps release
-// its scale buffer (sce).
-template <int NBM>
-__device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char* scbuf, uint32_t tbase,
-                            uint64_t* mready, uint64_t* scf, uint64_t* sce, uint64_t* sfr, const Meta* meta,
-                            const uint16_t* tok) {
-    using C = Cfg<NBM>;
-    const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
-    uint32_t stage = 0, phase = 0;
-    uint32_t scph = 0;  // parity of the next phase of each scale buffer
-    BStage<NBM> b;
-    BRows<NBM> rows;
-    int have_item = -1, have_chunk = -1;
-    while (true) {
-        if (__shfl_sync(0xffffffffu, mbar_wait(&mready[stage], phase) ? 1 : 0, 0) == 0) {
-            if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
-            break;
-        }
-        const Meta m = meta[stage];
-        if (m.item < 0) break;
-        if (have_item != m.item || have_chunk != m.chunk) b_load<NBM>(p, m, m.chunk, t, lane, b, rows, tok);
-        unsigned char* bst = smem + (size_t)stage * C::STAGE + A_BYTES;
+__device__ __forceinline__ void b_issue(const Params& p, const Meta& m, int t, int lane, uint32_t bst, uint32_t sbs,
+                                        BRows<NBM>& r, const uint16_t* tok, const uint16_t* tokb) {
+    if (r.item != m.item) {
+        r.item = m.item;
 #pragma unroll
         for (int i = 0; i < NBM * BP / 128; i++) {
-            const int j = t + 128 * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
-            if (row < m.nrow)
-                *reinterpret_cast<uint4*>(bst + kh * (NBM * 128) + row * 128 + ((cc ^ (row & 7)) << 4)) = b.d[i];
+            const int row = (t + 128 * i) / BP;
+            r.d[i] = row < m.nrow ? b_src_row(m, row, tok, tokb) : 0;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+        for (int c = 0; c < 3; c++) {
+            const int row = 32 * c + lane;
+            r.s[c] = (row < m.nrow && row < NBM) ? b_src_row(m, row, tok, tokb) : 0;
+        }
+    }
+    const bool gu = m.type == IT_GU;
+    const uint8_t* src = gu ? p.x_mx : p.h_mx;
+    const uint8_t* ssrc = gu ? p.x_sc : p.h_sc;
+    const int ld = gu ? p.d : p.f;
+    const int k0 = m.kbase + m.chunk * KC;
+#pragma unroll
+    for (int i = 0; i < NBM * BP / 128; i++) {
+        const int j = t + 128 * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
+        if (row < m.nrow)
+            cp_async16(bst + kh * (NBM * 128) + row * 128 + ((cc ^ (row & 7)) << 4),
+                       src + (size_t)r.d[i] * (ld / 2) + k0 / 2 + c16 * 16);
+    }
+    static_assert(KC / 32 == 16, "one 16-byte scale copy per row and stage");
+#pragma unroll
+    for (int c = 0; c < 3; c++) {
+        const int row = 32 * c + lane;
+        if (row < m.nrow && row < NBM) cp_async16(sbs + row * 16, ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// warps 2..5: per stage, the activation rows into the stage's B area (above) and
+// every E8M0 scale into tensor memory.  Scale of row m (A: weight row, B: activation
+// row) for the stage's K blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word
+// at lane m % 32, column base + set*4 + m / 32; each warp writes the copy in its own
+// lane quadrant.  Stages are finished in order: once the thread's copies of the
+// oldest stage have landed (and, for an item's first stage, its A scales), the
+// scales go to tensor memory and the warp releases the stage to the MMA.  After an
+// item's last stage the warps release its scale buffer (sce).
+template <int NBM>
+__device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char* scbuf, unsigned char* sbs_all,
+                            uint32_t tbase, uint64_t* mready, uint64_t* scf, uint64_t* sce, uint64_t* sfr,
+                            const Meta* meta, const uint16_t* tok, const uint16_t* tokb) {
+    using C = Cfg<NBM>;
+    const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
+    const uint32_t sbs = smem_u32(sbs_all) + (uint32_t)(q * C::NST * NBM * 16);  // this warp's scale staging
+    uint32_t is = 0, iph = 0;   // next stage to issue, and the parity of its claim
+    uint32_t fs = 0;            // next stage to finish
+    int inflight = 0;
+    bool ended = false, ok = true;
+    uint32_t scph = 0;          // parity of the next phase of each A-scale buffer
+    BRows<NBM> rows;
+    while (ok) {
+        // every claimed stage goes out, up to the whole ring
+        while (!ended && inflight < C::NST) {
+            bool claimed;
+            if (inflight == 0) {
+                claimed = __shfl_sync(0xffffffffu, mbar_wait(&mready[is], iph) ? 1 : 0, 0) != 0;
+                if (!claimed) {
+                    if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                    ok = false;
+                    break;
+                }
+            } else {
+                claimed = __all_sync(0xffffffffu, mbar_peek(&mready[is], iph));
+                if (!claimed) break;
+            }
+            const Meta& m = meta[is];
+            if (m.item < 0) {
+                ended = true;
+                break;
+            }
+            b_issue<NBM>(p, m, t, lane, smem_u32(smem + (size_t)is * C::STAGE + A_BYTES), sbs + is * (NBM * 16),
+                         rows, tok, tokb);
+            inflight++;
+            if (++is == (uint32_t)C::NST) {
+                is = 0;
+                iph ^= 1u;
+            }
+        }
+        if (!ok || inflight == 0) break;
+        // finish the oldest stage
+        const Meta m = meta[fs];
+        cp_async_wait(inflight - 1);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the copies, for the MMA's reads
         if (m.chunk == 0) {  // the item's A scales have landed
             if (__shfl_sync(0xffffffffu, mbar_wait(&scf[m.sbuf], (scph >> m.sbuf) & 1u) ? 1 : 0, 0) == 0) {
                 if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                ok = false;
                 break;
             }
             scph ^= 1u << m.sbuf;
         }
         const uint32_t sa = smem_u32(scbuf + m.sbuf * C::SCB);
+        const uint32_t sb = sbs + fs * (NBM * 16);
+        uint4 bs[3];
+#pragma unroll
+        for (int c = 0; c < 3; c++) {
+            const int row = 32 * c + lane;
+            bs[c] = (row < m.nrow && row < NBM) ? lds128(sb + row * 16) : make_uint4(0, 0, 0, 0);
+        }
         const int kb_off = m.chunk * (KC / 32);
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
 #pragma unroll
@@ -571,60 +605,24 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
             uint32_t wa[4];
 #pragma unroll
             for (int c = 0; c < 4; c++) wa[c] = lds32(sa + (32 * c + lane) * m.sc + kb_off + 4 * set);
-            const uint32_t w0 = set == 0 ? b.s[0].x : set == 1 ? b.s[0].y : set == 2 ? b.s[0].z : b.s[0].w;
-            const uint32_t w1 = set == 0 ? b.s[1].x : set == 1 ? b.s[1].y : set == 2 ? b.s[1].z : b.s[1].w;
-            const uint32_t w2 = set == 0 ? b.s[2].x : set == 1 ? b.s[2].y : set == 2 ? b.s[2].z : b.s[2].w;
-            tm_st4(tbase + C::TM_SFA + stage * SF_COLS + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
-            tm_st4(tbase + C::TM_SFB + stage * SF_COLS + set * 4 + lane_base, w0, w1, w2, 0u);
+            const uint32_t w0 = set == 0 ? bs[0].x : set == 1 ? bs[0].y : set == 2 ? bs[0].z : bs[0].w;
+            const uint32_t w1 = set == 0 ? bs[1].x : set == 1 ? bs[1].y : set == 2 ? bs[1].z : bs[1].w;
+            const uint32_t w2 = set == 0 ? bs[2].x : set == 1 ? bs[2].y : set == 2 ? bs[2].z : bs[2].w;
+            tm_st4(tbase + C::TM_SFA + fs * SF_COLS + set * 4 + lane_base, wa[0], wa[1], wa[2], wa[3]);
+            tm_st4(tbase + C::TM_SFB + fs * SF_COLS + set * 4 + lane_base, w0, w1, w2, 0u);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         fence_before();
         __syncwarp();
         if (lane == 0) {
-            mbar_arrive(&sfr[stage]);
+            mbar_arrive(&sfr[fs]);
             if (m.chunk == m.nchunks - 1) mbar_arrive(&sce[m.sbuf]);  // done reading the item's scales
         }
-        const uint32_t nstage = stage + 1 == (uint32_t)C::NST ? 0u : stage + 1;
-        const uint32_t nphase = nstage == 0u ? phase ^ 1u : phase;
-        if (m.chunk + 1 < m.nchunks) {
-            // the next stage of the same item: its activations are known now
-            b_load<NBM>(p, m, m.chunk + 1, t, lane, b, rows, tok);
-            have_item = m.item;
-            have_chunk = m.chunk + 1;
-        } else if (__all_sync(0xffffffffu, mbar_peek(&mready[nstage], nphase))) {
-            // the next stage is already claimed (the producer runs ahead while the
-            // ring is full): load the first activations of its item now
-            const Meta mn = meta[nstage];
-            have_item = -1;
-            if (mn.item >= 0) {
-                b_load<NBM>(p, mn, mn.chunk, t, lane, b, rows, tok);
-                have_item = mn.item;
-                have_chunk = mn.chunk;
-            }
-        } else {
-            have_item = -1;
-        }
-        // two stages ahead, into L1: a later chunk of the same item, or the stage
-        // the producer has already claimed (its item's dependencies are met)
-        if (m.chunk + 2 < m.nchunks) {
-            BRows<NBM> r2 = rows;
-            if (r2.item != m.item) b_rows<NBM>(p, m, t, lane, r2, tok);
-            b_prefetch<NBM>(p, m, m.chunk + 2, t, lane, r2);
-        } else if (tok != nullptr) {
-            const uint32_t s2 = nstage + 1 == (uint32_t)C::NST ? 0u : nstage + 1;
-            const uint32_t ph2 = s2 == 0u ? nphase ^ 1u : nphase;
-            if (__all_sync(0xffffffffu, mbar_peek(&mready[s2], ph2))) {
-                const Meta m2 = meta[s2];
-                if (m2.item >= 0) {
-                    BRows<NBM> r2;
-                    b_rows<NBM>(p, m2, t, lane, r2, tok);
-                    b_prefetch<NBM>(p, m2, m2.chunk, t, lane, r2);
-                }
-            }
-        }
-        stage = nstage;
-        phase = nphase;
+        inflight--;
+        if (++fs == (uint32_t)C::NST) fs = 0;
     }
+    // no copy may still be in flight when the CTA exits
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // warp 1, one thread: four MMAs (K = 64 each) per stage into the item's accumulator
@@ -837,12 +835,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     unsigned char* scbuf = smem + (size_t)C::NST * C::STAGE;
-    float* xch = reinterpret_cast<float*>(scbuf + 2 * C::SCB);
+    unsigned char* sbs = scbuf + 2 * C::SCB;
+    float* xch = reinterpret_cast<float*>(sbs + C::SBS_BYTES);
     uint2* umeta = reinterpret_cast<uint2*>(xch + XCH_FLOATS);
     int* cp = reinterpret_cast<int*>(umeta + C::MAX_U);  // [MAX_U + 1] chunk prefix
     uint16_t* tok = C::TOKS > 0 ? reinterpret_cast<uint16_t*>(cp + C::MAX_U + 1) : nullptr;  // [TOKS]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)C::NST * C::STAGE + 2 * C::SCB + XCH_FLOATS * 4 +
-                                                 ((C::META_BYTES + 15) & ~15));
+    uint16_t* tokb = reinterpret_cast<uint16_t*>(cp + C::MAX_U + 1) + C::TOKS;              // [2][CHUNK]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)C::NST * C::STAGE + 2 * C::SCB + C::SBS_BYTES +
+                                                 XCH_FLOATS * 4 + ((C::META_BYTES + 15) & ~15));
     uint64_t* full = bars;
     uint64_t* empty = full + C::NST;
     uint64_t* sfr = empty + C::NST;
@@ -938,11 +938,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const uint32_t tbase = *tslot;
 
     if (warp == 0) {
-        if ((tid & 31) == 0) producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, sce, meta, first);
+        if ((tid & 31) == 0)
+            producer<NBM>(p, U, umeta, cp, smem, scbuf, full, empty, mready, scf, sce, meta, first,
+                          tok != nullptr ? nullptr : tokb);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
     } else if (warp < 6) {
-        scale_mover<NBM>(p, smem, scbuf, tbase, mready, scf, sce, sfr, meta, tok);
+        scale_mover<NBM>(p, smem, scbuf, sbs, tbase, mready, scf, sce, sfr, meta, tok, tokb);
     } else {
         epilogue<NBM>(p, tbase, xch, eflag, acc_full, acc_empty, am);
     }
