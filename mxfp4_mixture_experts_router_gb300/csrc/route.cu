@@ -25,6 +25,7 @@ constexpr int RT_EG = 64;       // experts per group (8 per warp)
 constexpr int RT_MAX_ROWS = 32;
 constexpr int RT_MAX_KS = 16;   // K slices: d <= 8192
 constexpr int RT_TICKET_EG = 32;  // ctrl words [32, 64) hold the per-group tickets
+constexpr int RT_CAND_ROWS = 4;   // router-GEMV blocks of up to this many rows merge per-group candidates
 
 struct RouteParams {
     int d, E, k, N, n_shared;
@@ -34,6 +35,7 @@ struct RouteParams {
     const float* logits_in;
     float* logits;        // logits_out, or the workspace copy
     float* part;          // [n_ks][N][E] partial logits
+    uint64_t* cand;       // [N][n_eg][k] per-group top-k candidates (selection key << 32 | ~expert), ranked
     int32_t* topk_idx;
     float* topk_w;
     uint32_t* ctrl;
@@ -594,6 +596,156 @@ __device__ void topk_row_cta(const RouteParams& p, const float* lrow, int n, boo
     __syncthreads();  // s is reused by the next row
 }
 
+// Selection order of a row's experts as one 64-bit key: the logit's selection key
+// above the complemented expert index, so equal logits rank by lower index and no
+// two experts of a row compare equal (0 = no candidate).
+__device__ __forceinline__ uint64_t cand_key(float v, int e) {
+    return ((uint64_t)sel_key(v) << 32) | (uint64_t)(~(uint32_t)e);
+}
+
+// A group finisher of a router-GEMV block of up to RT_CAND_ROWS rows: the k best of
+// its experts e_lo .. e_lo + span - 1 in every row (logits in s_lg[n][RT_EG]),
+// ranked, into p.cand.  One thread per (row, expert) counts the group's experts
+// that rank above it; ranks the group cannot fill (span < k) get no candidate.
+__device__ void group_candidates(const RouteParams& p, int eg, int span, const float* s_lg, uint64_t* s_ck) {
+    const int tid = threadIdx.x, K = p.k;
+    const int total = p.N * RT_EG;
+    bool nan = false;
+    for (int i = tid; i < total; i += RT_THREADS) {
+        const int j = i % RT_EG;
+        uint64_t c = 0;
+        if (j < span) {
+            const float v = s_lg[i];
+            nan |= isnan(v);
+            c = cand_key(v, eg * RT_EG + j);
+        }
+        s_ck[i] = c;
+    }
+    if (__syncthreads_or(nan) && tid == 0) set_error(p.ctrl, MOE_EBIT_NAN);
+    for (int i = tid; i < total; i += RT_THREADS) {
+        const int n = i / RT_EG, j = i - n * RT_EG;
+        if (j >= span) continue;
+        const uint64_t mine = s_ck[i];
+        const uint64_t* row = s_ck + n * RT_EG;
+        int rank = 0;
+#pragma unroll 8
+        for (int t = 0; t < RT_EG; t++) rank += row[t] > mine ? 1 : 0;
+        if (rank < K) p.cand[((size_t)n * p.n_eg + eg) * K + rank] = mine;
+    }
+    for (int i = tid; i < p.N * K; i += RT_THREADS) {
+        const int n = i / K, r = i - n * K;
+        if (r >= span) p.cand[((size_t)n * p.n_eg + eg) * K + r] = 0;
+    }
+}
+
+// The last CTA of a router-GEMV block of up to RT_CAND_ROWS rows: every row's k
+// winners from the groups' ranked candidates.  A candidate's rank in the row is
+// its rank in its own group plus, for every other group, the number of that
+// group's candidates above it (a binary search in the group's descending list).
+// The winners are then weighted by a warp per row with the arithmetic of topk_row.
+// s_c: [N][n_eg k] candidates, s_sel: [N][k] winners (shared memory).
+__device__ void select_from_candidates(const RouteParams& p, uint64_t* s_c, uint64_t* s_sel, int* sidx) {
+    const int tid = threadIdx.x, K = p.k, G = p.n_eg, M = G * K;
+    const int total = p.N * M;
+    for (int i = tid; i < total; i += RT_THREADS) s_c[i] = __ldcg(p.cand + i);
+    __syncthreads();
+    for (int i = tid; i < total; i += RT_THREADS) {
+        const int n = i / M, rest = i - n * M, g = rest / K, r = rest - g * K;
+        const uint64_t mine = s_c[i];
+        if (mine == 0) continue;
+        const uint64_t* rowc = s_c + n * M;
+        int rank = r;
+        for (int g2 = 0; g2 < G && rank < K; g2++) {
+            if (g2 == g) continue;
+            const uint64_t* l = rowc + g2 * K;
+            int lo = 0, hi = K;  // the first entry of list g2 that is not above `mine`
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (l[mid] > mine) lo = mid + 1;
+                else hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank < K) s_sel[n * K + rank] = mine;
+    }
+    __syncthreads();
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int n = warp; n < p.N; n += RT_THREADS / 32) {
+        const uint64_t c = lane < K ? s_sel[n * K + lane] : 0;
+        const uint32_t my_key = (uint32_t)(c >> 32);
+        const int my_idx = (int)~(uint32_t)c;
+        const float my_val = (lane < K) ? key_value(my_key) : 0.f;
+        // weights: exp(l_j - l_0) / sum_i exp(l_i - l_0), summed in slot order
+        const float l0 = __shfl_sync(0xffffffffu, my_val, 0);
+        const float ex = (lane < K) ? expf(my_val - l0) : 0.f;
+        float sum = 0.f;
+        for (int j = 0; j < K; j++) sum += __shfl_sync(0xffffffffu, ex, j);
+        if (lane < K) {
+            p.topk_idx[(size_t)n * K + lane] = my_idx;
+            p.topk_w[(size_t)n * K + lane] = ex / sum;
+            sidx[n * K + lane] = my_idx;
+        }
+    }
+}
+
+// the expert kernels' counters and maxima, cleared by the routing for its block
+__device__ void reset_expert_state(const RouteParams& p) {
+    const int tid = threadIdx.x;
+    for (int i = tid; i < p.v_cap; i += RT_THREADS) p.gu_done[i] = 0;
+    for (int i = tid; i < p.E; i += RT_THREADS) p.gu_done_tc[i] = 0;
+    for (int64_t i = tid; i < p.pairs_cap; i += RT_THREADS) p.hmax[i] = 0;
+    if (tid == 0) {
+        p.ctrl[CTRL_WORK] = 0;
+        p.ctrl[CTRL_EXIT] = 0;
+        p.ctrl[CTRL_WORK_TC] = 0;
+        p.ctrl[CTRL_EXIT_TC] = 0;
+    }
+}
+
+// Group a block of N k <= RT_THREADS pairs by expert (s_idx: the selections, pair
+// i = row * k + slot): pair i's place among the pairs sorted by (expert, i) is the
+// number of pairs before it in that order, and an expert's place among the
+// selected experts the number of distinct experts below it (counted over the
+// first pair of each).  The same order as group_block.
+__device__ void group_small(const RouteParams& p, const int* s_idx, int* s_first) {
+    const int tid = threadIdx.x, NK = p.N * p.k;
+    int e = 0, pos = 0;
+    bool first = false, valid = false;
+    if (tid < NK) {
+        e = s_idx[tid];
+        valid = e >= 0 && e < p.E;
+        first = valid;
+        for (int j = 0; j < NK; j++) {
+            const int ej = s_idx[j];
+            const bool vj = ej >= 0 && ej < p.E;
+            pos += (vj && (ej < e || (ej == e && j < tid))) ? 1 : 0;
+            if (ej == e && j < tid) first = false;
+        }
+        s_first[tid] = first ? e : INT_MAX;
+    }
+    __syncthreads();
+    if (valid) {
+        int u = 0;
+        for (int j = 0; j < NK; j++) u += s_first[j] < e ? 1 : 0;
+        p.pair[pos] = tid;
+        if (first) {
+            p.uexp[u] = e;
+            p.off[u] = pos;
+        }
+    }
+    if (tid == 0) {
+        int U = 0, total = 0;
+        for (int j = 0; j < NK; j++) {
+            U += s_first[j] != INT_MAX ? 1 : 0;
+            total += (s_idx[j] >= 0 && s_idx[j] < p.E) ? 1 : 0;
+        }
+        p.off[U] = total;
+        p.ctrl[CTRL_UNIQUE] = (uint32_t)U;
+        p.ctrl[CTRL_ROWS] = (uint32_t)p.N;
+    }
+    reset_expert_state(p);
+}
+
 // Group the block's pairs by expert (N <= 32): smem counts and row bitmaps; s_idx
 // holds the block's selections (N k words, written by topk_row).
 __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, int* s_off, int* s_idx) {
@@ -673,16 +825,7 @@ __device__ void group_block(const RouteParams& p, int* s_cnt, uint32_t* s_bits, 
         const int rank = __popc(s_bits[e] & ((1u << n) - 1u));
         p.pair[s_off[e] + rank] = i;
     }
-    // clean state for the expert kernel
-    for (int i = tid; i < p.v_cap; i += RT_THREADS) p.gu_done[i] = 0;
-    for (int i = tid; i < p.E; i += RT_THREADS) p.gu_done_tc[i] = 0;
-    for (int64_t i = tid; i < p.pairs_cap; i += RT_THREADS) p.hmax[i] = 0;
-    if (tid == 0) {
-        p.ctrl[CTRL_WORK] = 0;
-        p.ctrl[CTRL_EXIT] = 0;
-        p.ctrl[CTRL_WORK_TC] = 0;
-        p.ctrl[CTRL_EXIT_TC] = 0;
-    }
+    reset_expert_state(p);
 }
 
 __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams p) {
@@ -723,9 +866,13 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
         __syncthreads();
         if (s_flag) {
             __threadfence();
-            // sum the K slices in slice order for this group's experts
+            // sum the K slices in slice order for this group's experts (small blocks
+            // also keep them in shared memory for the group's candidates)
             const int e_lo = eg * RT_EG, e_hi = min(p.E, e_lo + RT_EG);
             const int span = e_hi - e_lo;
+            const bool cand = p.N <= RT_CAND_ROWS;
+            float* s_lg = smem;                                            // [N][RT_EG]
+            uint64_t* s_ck = reinterpret_cast<uint64_t*>(smem_raw + 4096);  // [N][RT_EG]
             for (int base = 0; base < p.N * span; base += 4 * RT_THREADS) {
                 float v[4][RT_MAX_KS];
 #pragma unroll
@@ -747,7 +894,12 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
                     for (int ks2 = 0; ks2 < RT_MAX_KS; ks2++)
                         if (ks2 < p.n_ks) a += v[q][ks2];
                     p.logits[(size_t)n * p.E + e] = a;
+                    if (cand) s_lg[n * RT_EG + (e - e_lo)] = a;
                 }
+            }
+            if (cand) {
+                __syncthreads();
+                group_candidates(p, eg, span, s_lg, s_ck);
             }
             if (tid == 0) p.ctrl[RT_TICKET_EG + eg] = 0;
             group_finisher = true;
@@ -776,7 +928,10 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
         uint32_t* s_bits = reinterpret_cast<uint32_t*>(s_cnt + 1024);
         int* s_off = reinterpret_cast<int*>(s_bits + 1024);
         int* s_idx = s_off + 1024;
-        if (p.N <= 2) {  // the whole CTA on each row
+        if (p.n_gemv_ctas > 0 && p.N <= RT_CAND_ROWS) {  // merge the groups' candidates
+            select_from_candidates(p, reinterpret_cast<uint64_t*>(smem_raw + 16384),
+                                   reinterpret_cast<uint64_t*>(smem_raw + 32768), s_idx);
+        } else if (p.N <= 2) {  // the whole CTA on each row
             uint32_t* s_topk = reinterpret_cast<uint32_t*>(smem_raw + 32768);
             for (int n = 0; n < p.N; n++)
                 topk_row_cta(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, s_topk, s_idx + n * p.k);
@@ -786,7 +941,10 @@ __global__ void __launch_bounds__(RT_THREADS, 2) route_kernel(const RouteParams 
                 topk_row(p, L + (size_t)n * p.E, n, p.logits_in == nullptr, sel, s_idx + n * p.k);
         }
         __syncthreads();
-        group_block(p, s_cnt, s_bits, s_off, s_idx);
+        if (p.N * p.k <= RT_THREADS)
+            group_small(p, s_idx, s_cnt);
+        else
+            group_block(p, s_cnt, s_bits, s_off, s_idx);
         if (tid == 0) p.ctrl[CTRL_TICKET] = 0;
         if (stamp) tl_end(p.ctrl, TL_ROUTE);  // the routing is complete
         if (!gemv_finisher) {  // caller logits: every row's f16 copy is already written
@@ -1082,8 +1240,10 @@ extern "C" int moe_route(const moe_desc* desc, int32_t n_rows, const uint16_t* x
     p.n_ks = d / KS;
     p.n_eg = (E + RT_EG - 1) / RT_EG;
     if (p.n_eg > 32 || p.n_ks > RT_MAX_KS) return MOE_ERR_UNSUPPORTED;
-    // the partial logits must fit in the h buffer: n_ks * N * E floats
-    if ((size_t)p.n_ks * n_rows * E * 4 > L.dbg_g - L.h) return MOE_ERR_UNSUPPORTED;
+    // the partial logits and the groups' candidates must fit in the h buffer
+    const size_t part_bytes = ((size_t)p.n_ks * n_rows * E * 4 + 7) & ~(size_t)7;
+    if (part_bytes + (size_t)n_rows * p.n_eg * k * 8 > L.dbg_g - L.h) return MOE_ERR_UNSUPPORTED;
+    p.cand = reinterpret_cast<uint64_t*>(base + L.h + part_bytes);
     p.n_gemv_ctas = logits_in ? 0 : p.n_ks * p.n_eg;
     const int prep_ctas = (logits_in && x) ? n_rows * ((d + RT_CHUNK - 1) / RT_CHUNK) : n_rows;
     int grid = p.n_gemv_ctas > prep_ctas ? p.n_gemv_ctas : prep_ctas;
