@@ -12,12 +12,21 @@
  * table in "Kimi K3 and K3.1 Pro in numbers", adds the 2 shared experts.
  *
  * One layer for a block of N rows is four calls on one stream:
- *   moe_route         router GEMV (or caller logits), top-k, weights, grouping
- *   moe_expert_block  every selected expert's SwiGLU MLP on its rows, each
- *                     expert's weights streamed from HBM once per block, plus
- *                     the shared Q8_0 experts
- *   moe_combine       out = bf16(residual + sum_j w_j y_j + sum_s shared_s)
- * and q8_0_block_matmul is the stand-alone Q8_0 N-row matmul.
+ *   moe_route                       router GEMV (or caller logits), top-k,
+ *                                   renormalised weights, grouping by expert
+ *   moe_shared_experts_after_route  the 2 shared Q8_0 experts on every row,
+ *                                   beside the routing (they need x only)
+ *   moe_expert_block                every selected expert's SwiGLU MLP on its
+ *                                   rows (MOE_MODE_ROUTED_ONLY |
+ *                                   MOE_MODE_AFTER_SHARED), each expert's
+ *                                   weights streamed from HBM once per block
+ *   moe_combine                     out = bf16(residual + sum_j w_j y_j +
+ *                                   sum_s shared_s)
+ * (moe_expert_block alone also runs the shared experts, after the routing.)
+ * q8_0_block_matmul is the stand-alone Q8_0 N-row matmul; moe_cache_* is the
+ * device expert cache that holds routed experts in HBM slots filled from pinned
+ * host memory, and moe_nvme_* the tier below it that reads expert slabs from
+ * files into pinned host memory.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -288,7 +297,11 @@ MOE_API int moe_expert_block(const moe_desc* desc, int32_t n_rows, int32_t mode,
                      void* ws, int32_t n_rows_max, float* y_part, void* stream);
 
 /*
- * Weighted combine into the residual, in a fixed order per element:
+ * Weighted combine into the residual ("Run Kimi 3.1 locally on one GPU": each
+ * token's 16 selected experts; "Run Kimi K3 and K3.1 Pro Locally", table in
+ * "Kimi K3 and K3.1 Pro in numbers": plus 2 shared experts; the routed outputs
+ * are weighted by the renormalised router weights and added, with the shared
+ * experts' outputs, to the residual stream), in a fixed order per element:
  *   acc = 0; for j in 0..k-1: acc = fma(w[n][j], y[n][j][c], acc);
  *   for s in 0..n_shared-1: acc += shared_y[s][n][c];
  *   out[n][c] = bf16_rne(residual[n][c] + acc)
