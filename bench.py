@@ -737,7 +737,11 @@ def run_stacked_legs(torch, args):
         "tok_s_blocks": round(tok_per_block / blocks["s_per_block"], 2),
         "tok_s_plain": round(1 / plain["s_per_block"], 2),
         "block_hit_rate": blocks["hit_rate"], "plain_hit_rate": plain["hit_rate"],
-        "blocks_timed": args.verify_blocks, "plain_steps_timed": args.verify_plain_steps}
+        "blocks_timed": args.verify_blocks, "plain_steps_timed": args.verify_plain_steps,
+        # the block's cost does not depend on how many drafts are accepted: tokens per block
+        # for other acceptance probabilities p, in closed form (sum of p^j, j = 0..15)
+        "tok_s_blocks_by_acceptance": {
+            str(q): round(sum(q ** j for j in range(16)) / blocks["s_per_block"], 2) for q in (0.5, 0.7, 0.8, 0.9)}}
     return out
 
 
