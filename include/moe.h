@@ -323,8 +323,14 @@ MOE_API int moe_combine(const moe_desc* desc, int32_t n_rows, const uint16_t* re
  *  q, d    int8 [n_out][k_in] and fp16 [n_out][k_in/32]; 32-byte aligned
  *  q2, d2  the up matrix for MOE_EPI_SWIGLU (same shape), else NULL
  *  y       fp32 [n_rows][n_out]
- *  ws      scratch of q8_0_workspace_size() bytes, zeroed once before first use
+ *  ws      scratch of q8_0_workspace_size(n_rows, k_in, n_out) bytes, zeroed once
+ *          before first use; a call leaves it ready for the next call of that shape
  * MOE_EPI_SWIGLU requires bf16 x.
+ * Without SwiGLU, K may be split into ranges (more work items when n_out is small
+ * for the GPU: 7168 -> 1536 has 24 blocks of 64 outputs).  The number of ranges
+ * depends on k_in, n_out and the GPU's SM count, never on n_rows; the last range of
+ * a 64-output block to finish adds the ranges' fp32 sums in range order, so every
+ * row's result is the same in every block and from run to run.
  */
 MOE_API size_t q8_0_workspace_size(int32_t n_rows, int32_t k_in, int32_t n_out);
 MOE_API int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out,
@@ -341,7 +347,7 @@ MOE_API int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out,
  * this entry point; it is a deployment convenience of this library.
  *
  * Same arguments and results as q8_0_block_matmul, minus ws.  Its scratch is a
- * file-scope __device__ array of 720,896 bytes that every GPU loading this
+ * file-scope __device__ array of 2,789,376 bytes that every GPU loading this
  * library holds until the process exits; limits: n_rows <= 16 and
  * k_in <= 7168 (larger sizes return MOE_ERR_UNSUPPORTED before any launch).
  * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.

@@ -27,6 +27,7 @@
 // * A row's arithmetic never depends on the other rows of the block: K is
 //   always reduced in the same order, the row's tensor-core column does not
 //   change its result, and scale exponents are per row.
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -90,11 +91,20 @@ struct ExParams {
     float* out_shared;
     float* y_part;
     int64_t pairs_cap;
+    // plain Q8_0 job: each 64-row down item is split into ksplit K ranges (0 or 1: not
+    // split); the ranges' sums go to kpart [ksplit][n_rows][m_dn] and the last of a row
+    // block's items to finish (karrive [m_dn / 64]) adds them in range order
+    int ksplit;
+    float* kpart;
+    uint32_t* karrive;
 };
 
 struct Meta {
-    int item, type, v, blk, chunk, nchunks, slot, pad;
+    int item, type, v, blk, chunk, nchunks, slot;
+    int c0;  // first chunk of the item (its chunks are c0 .. nchunks - 1)
 };
+
+__device__ __forceinline__ int ksplit_of(const ExParams& p) { return p.ksplit > 1 ? p.ksplit : 1; }
 
 __device__ __forceinline__ void item_counts(const ExParams& p, bool& has_gu, bool& has_dn, int& lag) {
     has_gu = p.job != J_Q8_PLAIN;
@@ -106,7 +116,7 @@ __device__ __forceinline__ int total_items(const ExParams& p, int V) {
     bool g, d;
     int lag;
     item_counts(p, g, d, lag);
-    return V * ((g ? p.n_gu : 0) + (d ? p.n_dn : 0));
+    return V * ((g ? p.n_gu : 0) + (d ? p.n_dn * ksplit_of(p) : 0));
 }
 
 // Item order: round i holds the gate/up items of expert i, then the down items
@@ -128,13 +138,15 @@ __device__ void decode_item(const ExParams& p, int V, int item, int& type, int& 
         }
         const int vd = i - lag;
         if (has_dn && vd >= 0 && vd < V) {
-            if (rest < p.n_dn) {
+            // a split down item's blk is row block * ksplit + K range
+            const int n_dn = p.n_dn * ksplit_of(p);
+            if (rest < n_dn) {
                 type = IT_DN;
                 v = vd;
                 blk = rest;
                 return;
             }
-            rest -= p.n_dn;
+            rest -= n_dn;
         }
     }
     type = IT_GU;
@@ -594,8 +606,16 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
                 }
             }
         }
-        const int row0 = blk * G.rows_item;
-        for (int c = 0; c < G.chunks; c++) {
+        int rb = blk, c0 = 0, c1 = G.chunks;
+        if (type == IT_DN && ksplit_of(p) > 1) {
+            const int ks = ksplit_of(p);
+            rb = blk / ks;
+            const int r = blk - rb * ks;
+            c0 = r * G.chunks / ks;
+            c1 = (r + 1) * G.chunks / ks;
+        }
+        const int row0 = rb * G.rows_item;
+        for (int c = c0; c < c1; c++) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
                 set_error(p.ctrl, MOE_EBIT_TIMEOUT);
                 ok = false;
@@ -608,7 +628,8 @@ __device__ void producer(const ExParams& p, int V, unsigned char* ring, uint64_t
             mt.v = v;
             mt.blk = blk;
             mt.chunk = c;
-            mt.nchunks = G.chunks;
+            mt.nchunks = c1;
+            mt.c0 = c0;
             mt.slot = z;
             mbar_arrive_expect_tx(&full[stage], G.tx);
             unsigned char* st = ring + (size_t)stage * EX_STAGE;
@@ -682,6 +703,7 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
     // (final once its gate/up items are done; the same for all its down items)
     __shared__ int s_hexp[EX_NT * 8];
     __shared__ int s_hexp_v;
+    __shared__ int s_klast;  // this CTA finished the last K range of a split row block
     if (tid == 0) s_hexp_v = -1;
     consumer_sync<EX_CT>();
 
@@ -692,7 +714,7 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
         }
         const Meta m = meta[stage];
         if (m.item < 0) break;
-        if (m.chunk == 0) {
+        if (m.chunk == m.c0) {
             type = m.type;
             blk = m.blk;
             c.v = m.v;
@@ -764,7 +786,8 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
 #pragma unroll
                     for (int nt = 0; nt < EX_NT; nt++)
                         if (bval[nt] && (lane & 3) < T)
-                            asm volatile("prefetch.global.L1 [%0];" ::"l"(hrow[nt] + (cw * T + (lane & 3)) * 32));
+                            asm volatile("prefetch.global.L1 [%0];" ::"l"(
+                                hrow[nt] + (m.chunk * 8 * T + cw * T + (lane & 3)) * 32));
                 }
             }
         }
@@ -876,6 +899,8 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
 #pragma unroll
                     for (int t = 0; t < 4; t++) red[((cw * 4 + mt) * EX_NT + nt) * 128 + t * 32 + lane] = acc[mt][nt][t];
             consumer_sync<EX_CT>();
+            const int ks = ksplit_of(p);
+            const int rb = blk / ks, kr = blk - rb * ks;  // row block and K range of a split item
             const int per_mt = c.NT * 128;
             for (int idx = tid; idx < 4 * per_mt; idx += EX_CT) {
                 const int mt = idx / per_mt, rem = idx - mt * per_mt;
@@ -885,13 +910,33 @@ __device__ void consumer(const ExParams& p, int V, const __half* x16, const int*
                 float y = 0.f;
                 for (int w = 0; w < EX_CW; w++) y += red[((w * 4 + mt) * EX_NT + nt) * 128 + t * 32 + ln];
                 y *= exp2i(s_hexp[col]);
-                const int mrow = blk * 64 + mt * 16 + (ln >> 2) + 8 * (t >> 1);
-                if (c.shared) {
+                const int mrow = rb * 64 + mt * 16 + (ln >> 2) + 8 * (t >> 1);
+                if (ks > 1) {
+                    p.kpart[((size_t)kr * N + c.pb + col) * p.m_dn + mrow] = y;
+                } else if (c.shared) {
                     float* dst = p.out_shared + (size_t)(c.pb + col) * p.m_dn + mrow;
                     *dst = p.accum ? (*dst + y) : y;
                 } else {
                     const int pid = __ldg(p.pair + c.u_off + col);
                     p.y_part[(size_t)pid * p.m_dn + mrow] = y;
+                }
+            }
+            if (ks > 1) {
+                // the row block's last item to finish adds the K ranges' sums in range order
+                __threadfence();
+                consumer_sync<EX_CT>();
+                if (tid == 0) s_klast = atomicAdd(p.karrive + rb, 1u) == (uint32_t)(ks - 1);
+                consumer_sync<EX_CT>();
+                if (s_klast) {
+                    __threadfence();
+                    for (int idx = tid; idx < c.r * 64; idx += EX_CT) {
+                        const int col = idx >> 6, mrow = rb * 64 + (idx & 63);
+                        const float* src = p.kpart + (size_t)(c.pb + col) * p.m_dn + mrow;
+                        float y = __ldcg(src);
+                        for (int r = 1; r < ks; r++) y += __ldcg(src + (size_t)r * N * p.m_dn);
+                        float* dst = p.out_shared + (size_t)(c.pb + col) * p.m_dn + mrow;
+                        *dst = p.accum ? (*dst + y) : y;
+                    }
                 }
             }
         }
@@ -925,7 +970,11 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
     // launched after the previous kernel on the stream: wait for it here, unless this
     // launch reads nothing that kernel writes (the shared experts beside the routing),
     // in which case it waits before it completes
-    if (!p.dep_at_end) griddep_wait();
+    // the stand-alone Q8_0 jobs' producer reads only weights and this launch's work
+    // counter, which the preparation kernel before it does not touch: it starts
+    // streaming at once, and the consumers wait for the prepared rows
+    const bool early_weights = p.job != J_LAYER && tid >= EX_CT;
+    if (!p.dep_at_end && !early_weights) griddep_wait();
     griddep_launch_dependents();
     const int S = p.n_shared;
     const int U = (p.job == J_LAYER && !p.routed_off) ? (int)p.ctrl[CTRL_UNIQUE] : 0;
@@ -961,6 +1010,8 @@ __global__ void __launch_bounds__(EX_THREADS, 1) expert_kernel(const __grid_cons
         __threadfence();
         for (int i = tid; i < V; i += EX_CT) p.gu_done[i] = 0;
         for (int64_t i = tid; i < p.pairs_cap; i += EX_CT) p.hmax[i] = 0;
+        if (ksplit_of(p) > 1)
+            for (int i = tid; i < p.n_dn; i += EX_CT) p.karrive[i] = 0;
         if (tid == 0) {
             p.ctrl[p.work_word] = 0;
             p.ctrl[p.exit_word] = 0;
@@ -1335,10 +1386,42 @@ extern "C" int moe_shared_experts_after_route(const moe_desc* desc, int32_t n_ro
 // ---------------------------------------------------------------------------
 
 struct Q8Ws {
-    size_t ctrl, x16, xexp, hmax, h, gu_done, total;
+    size_t ctrl, x16, xexp, hmax, h, gu_done, kpart, karrive, karrive_bytes, total;
 };
 
-static Q8Ws q8_layout(int n_rows, int k_in) {
+// K ranges of the plain job's 64-row down items.  Unsplit, a narrow projection has
+// only n_out / 64 items for the whole GPU (7168 -> 1536: 24 items on 152 SMs, each
+// streaming 7168 bytes of codes for 64 rows), so most SMs stay idle; split into ks
+// ranges it has n_dn * ks items of about C / ks chunks (C = k_in / 256 chunks of 64
+// rows x 256 bytes).  ks minimises ceil(items / SMs) * (chunks per item + 1), the + 1
+// standing for an item's partial store and hand-over.  It depends on the shape and
+// the SM count, never on n_rows, so a row's result is the same in every block.  At
+// most Q8_KSPLIT_ELEMS / n_out ranges, which bounds the partial sums' scratch.
+constexpr int Q8_KSPLIT_MAX = 32;
+constexpr int Q8_KSPLIT_ELEMS = 32768;  // ks * n_out
+
+static int q8_ksplit_cap(int k_in, int n_out) {
+    int cap = Q8_KSPLIT_ELEMS / n_out;
+    cap = std::min(cap, k_in / 256);
+    cap = std::min(cap, Q8_KSPLIT_MAX);
+    return cap >= 2 ? cap : 1;
+}
+
+static int q8_ksplit(int k_in, int n_out, int n_sm) {
+    const int C = k_in / 256, n_dn = n_out / 64, cap = q8_ksplit_cap(k_in, n_out);
+    int best = 1;
+    int64_t best_cost = (int64_t)((n_dn + n_sm - 1) / n_sm) * C;
+    for (int ks = 2; ks <= cap; ks++) {
+        const int64_t cost = (int64_t)((n_dn * ks + n_sm - 1) / n_sm) * ((C + ks - 1) / ks + 1);
+        if (cost < best_cost) {
+            best = ks;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+static Q8Ws q8_layout(int n_rows, int k_in, int n_out) {
     Q8Ws L;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
@@ -1348,50 +1431,122 @@ static Q8Ws q8_layout(int n_rows, int k_in) {
     L.hmax = take((size_t)n_rows * 4);
     L.h = take((size_t)n_rows * k_in * 4);
     L.gu_done = take(4);
+    // partial sums and arrival counters of split down items (plain job), sized for the
+    // largest split the shape allows
+    const int cap = q8_ksplit_cap(k_in, n_out);
+    L.kpart = cap > 1 ? take((size_t)cap * n_rows * n_out * 4) : 0;
+    L.karrive_bytes = cap > 1 ? (size_t)(n_out / 64) * 4 : 0;
+    L.karrive = cap > 1 ? take(L.karrive_bytes) : 0;
     L.total = o;
     return L;
 }
 
-// prepares the rows of a stand-alone Q8_0 matmul: f16 rows (SwiGLU) or fp32
-// rows with their largest magnitude (plain)
-__global__ void q8_prep_kernel(int k_in, const void* x, int x_dtype, int swiglu, __half* x16, int* xexp,
-                               uint32_t* hmax, float* h) {
+// prepares the rows of a stand-alone Q8_0 matmul: f16 rows (SwiGLU) or fp32 rows
+// with their largest magnitude (plain).  One CTA per row; each thread loads all its
+// 8-element pieces of a pass before it uses any of them, so a row costs one or two
+// memory round trips instead of one per element.  It lets the matmul kernel launch
+// at once: that kernel's producer streams weights (which this kernel does not touch)
+// while its consumers wait for these rows.
+constexpr int Q8P_THREADS = 512;
+constexpr int Q8P_UNROLL = 2;  // 8-element pieces per thread and pass
+
+__device__ __forceinline__ void q8p_load8(const void* __restrict__ x, int x_dtype, bool vec, size_t i,
+                                          float (&v)[8]) {
+    if (x_dtype == MOE_DTYPE_BF16) {
+        const uint16_t* xb = static_cast<const uint16_t*>(x) + i;
+        if (vec) {
+            const uint4 u = __ldg(reinterpret_cast<const uint4*>(xb));
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                v[2 * e] = __uint_as_float(w[e] << 16);
+                v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = __uint_as_float((uint32_t)__ldg(xb + e) << 16);
+        }
+    } else {
+        const float* xf = static_cast<const float*>(x) + i;
+        if (vec) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(xf));
+            const float4 b = __ldg(reinterpret_cast<const float4*>(xf + 4));
+            v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = __ldg(xf + e);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(Q8P_THREADS) q8_prep_kernel(int k_in, const void* __restrict__ x, int x_dtype,
+                                                              int swiglu, int vec, __half* __restrict__ x16,
+                                                              int* __restrict__ xexp, uint32_t* __restrict__ hmax,
+                                                              float* __restrict__ h) {
+    griddep_launch_dependents();
     const int n = blockIdx.x, tid = threadIdx.x;
-    __shared__ uint32_t s_max[32];
+    __shared__ uint32_t s_max[Q8P_THREADS / 32];
     __shared__ int s_p;
+    const size_t row = (size_t)n * k_in;
+    constexpr int PASS = Q8P_THREADS * 8 * Q8P_UNROLL;
     uint32_t mx = 0;
-    for (int c = tid; c < k_in; c += blockDim.x) {
-        float v;
-        if (x_dtype == MOE_DTYPE_BF16)
-            v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[(size_t)n * k_in + c] << 16);
-        else
-            v = static_cast<const float*>(x)[(size_t)n * k_in + c];
-        mx = max(mx, __float_as_uint(v) & 0x7FFFFFFFu);
-        if (!swiglu) h[(size_t)n * k_in + c] = v;
+    for (int c0 = 0; c0 < k_in; c0 += PASS) {
+        float v[Q8P_UNROLL][8];
+#pragma unroll
+        for (int u = 0; u < Q8P_UNROLL; u++) {
+            const int c = c0 + (u * Q8P_THREADS + tid) * 8;  // k_in % 256 == 0: all 8 in range
+            if (c < k_in) q8p_load8(x, x_dtype, vec != 0, row + c, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < Q8P_UNROLL; u++) {
+            const int c = c0 + (u * Q8P_THREADS + tid) * 8;
+            if (c >= k_in) continue;
+#pragma unroll
+            for (int e = 0; e < 8; e++) mx = max(mx, __float_as_uint(v[u][e]) & 0x7FFFFFFFu);
+            if (!swiglu) {
+                float4* dst = reinterpret_cast<float4*>(h + row + c);
+                dst[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                dst[1] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+            }
+        }
     }
     for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((tid & 31) == 0) s_max[tid >> 5] = mx;
     __syncthreads();
     if (tid == 0) {
         uint32_t m = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); w++) m = max(m, s_max[w]);
+        for (int w = 0; w < Q8P_THREADS / 32; w++) m = max(m, s_max[w]);
         s_p = f16_scale_exponent(m);
         hmax[n] = m;
         xexp[n] = s_p;
     }
     __syncthreads();
     if (swiglu) {
-        const float s = exp2i(-s_p);
-        for (int c = tid; c < k_in; c += blockDim.x)
-            x16[(size_t)n * k_in + c] =
-                __float2half_rn(__uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[(size_t)n * k_in + c] << 16) * s);
+        const float sc = exp2i(-s_p);
+        for (int c0 = 0; c0 < k_in; c0 += PASS) {
+            float v[Q8P_UNROLL][8];
+#pragma unroll
+            for (int u = 0; u < Q8P_UNROLL; u++) {
+                const int c = c0 + (u * Q8P_THREADS + tid) * 8;
+                if (c < k_in) q8p_load8(x, x_dtype, vec != 0, row + c, v[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < Q8P_UNROLL; u++) {
+                const int c = c0 + (u * Q8P_THREADS + tid) * 8;
+                if (c >= k_in) continue;
+                __half2 hv[4];
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    hv[e] = __halves2half2(__float2half_rn(v[u][2 * e] * sc), __float2half_rn(v[u][2 * e + 1] * sc));
+                *reinterpret_cast<uint4*>(x16 + row + c) = *reinterpret_cast<const uint4*>(hv);
+            }
+        }
     }
 }
 
 extern "C" size_t q8_0_workspace_size(int32_t n_rows, int32_t k_in, int32_t n_out) {
-    (void)n_out;
-    if (n_rows <= 0 || k_in <= 0) return 0;
-    return q8_layout(n_rows, k_in).total;
+    if (n_rows <= 0 || k_in <= 0 || n_out <= 0) return 0;
+    return q8_layout(n_rows, k_in, n_out).total;
 }
 
 extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, const void* x, int32_t x_dtype,
@@ -1407,7 +1562,7 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
     if (((uintptr_t)q & 31) || ((uintptr_t)dq & 31) || ((uintptr_t)ws & 255)) return MOE_ERR_INVALID_ARG;
     if (swiglu && (((uintptr_t)q2 & 31) || ((uintptr_t)d2 & 31))) return MOE_ERR_INVALID_ARG;
 
-    const Q8Ws L = q8_layout(n_rows, k_in);
+    const Q8Ws L = q8_layout(n_rows, k_in, n_out);
     char* base = static_cast<char*>(ws);
     thread_local ExParams p;  // filled per call, copied into the launch
     memset(&p, 0, sizeof(p));
@@ -1459,11 +1614,19 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
     p.pairs_cap = 0;  // hmax rows are rewritten by the preparation kernel on every call
     p.work_word = CTRL_WORK;
     p.exit_word = CTRL_EXIT;
+    if (!swiglu) {
+        p.ksplit = q8_ksplit(k_in, n_out, sm_count());
+        if (p.ksplit > q8_ksplit_cap(k_in, n_out)) return MOE_ERR_UNSUPPORTED;
+        p.kpart = reinterpret_cast<float*>(base + L.kpart);
+        p.karrive = reinterpret_cast<uint32_t*>(base + L.karrive);
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    q8_prep_kernel<<<n_rows, 256, 0, s>>>(k_in, x, x_dtype, swiglu ? 1 : 0, reinterpret_cast<__half*>(base + L.x16),
-                                          reinterpret_cast<int*>(base + L.xexp),
-                                          reinterpret_cast<uint32_t*>(base + L.hmax),
-                                          reinterpret_cast<float*>(base + L.h));
+    const int vec = ((uintptr_t)x & 15) == 0;  // rows are then 16-byte aligned too (k_in % 256 == 0)
+    q8_prep_kernel<<<n_rows, Q8P_THREADS, 0, s>>>(k_in, x, x_dtype, swiglu ? 1 : 0, vec,
+                                                  reinterpret_cast<__half*>(base + L.x16),
+                                                  reinterpret_cast<int*>(base + L.xexp),
+                                                  reinterpret_cast<uint32_t*>(base + L.hmax),
+                                                  reinterpret_cast<float*>(base + L.h));
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     return launch_expert_kernel<MOE_FMT_Q8_0, MOE_FMT_Q8_0>(p, s);
 }
@@ -1481,7 +1644,10 @@ extern "C" int q8_0_block_matmul(int32_t n_rows, int32_t k_in, int32_t n_out, co
 
 constexpr int Q8_NOALLOC_MAX_ROWS = 16;
 constexpr int Q8_NOALLOC_MAX_K = 7168;
-constexpr size_t Q8_NOALLOC_BYTES = 720896;  // >= q8_layout(16, 7168).total, rounded to 4 KB
+// >= q8_layout(16, 7168, n_out).total for every n_out: 689,408 bytes of rows and
+// control words, at most 16 x Q8_KSPLIT_ELEMS floats of partial sums and 1 KB of
+// arrival counters (a split needs n_out <= Q8_KSPLIT_ELEMS / 2), rounded to 4 KB
+constexpr size_t Q8_NOALLOC_BYTES = 2789376;
 constexpr int Q8_NOALLOC_MAX_DEVICES = 64;
 
 static __device__ __align__(256) unsigned char q8_noalloc_scratch[Q8_NOALLOC_BYTES];
@@ -1542,7 +1708,7 @@ extern "C" int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n
                                          const uint16_t* d2, int32_t epilogue, float* y, void* stream) {
     if (n_rows < 1 || n_rows > Q8_NOALLOC_MAX_ROWS || k_in <= 0 || k_in > Q8_NOALLOC_MAX_K)
         return MOE_ERR_UNSUPPORTED;
-    const Q8Ws L = q8_layout(n_rows, k_in);
+    const Q8Ws L = q8_layout(n_rows, k_in, n_out);
     if (L.total > Q8_NOALLOC_BYTES) return MOE_ERR_UNSUPPORTED;
     unsigned char* ws = q8_noalloc_scratch_addr();
     if (ws == nullptr) return MOE_ERR_CUDA;
@@ -1554,6 +1720,7 @@ extern "C" int q8_0_block_matmul_noalloc(int32_t n_rows, int32_t k_in, int32_t n
     if (cudaMemsetAsync(ws + L.ctrl + 4 * (CTRL_ERROR + 1), 0, (CTRL_WORDS - CTRL_ERROR - 1) * 4, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (cudaMemsetAsync(ws + L.gu_done, 0, 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (L.karrive_bytes && cudaMemsetAsync(ws + L.karrive, 0, L.karrive_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
     return q8_0_block_matmul(n_rows, k_in, n_out, x, x_dtype, q, dq, q2, d2, epilogue, y, ws, stream);
 }
 

@@ -47,9 +47,11 @@ def test_plain_matmul_bf16(n, k_in, n_out):
     assert rel < 1e-5, rel
 
 
+# 1536 -> 7168 runs unsplit; 7168 -> 1536 has few 64-row items and splits K (the
+# ranges' sums are added by the last item of each row block, then accumulated into y)
+@pytest.mark.parametrize("k_in,n_out", [(1536, 7168), (7168, 1536)])
 @pytest.mark.parametrize("n", [1, 16])
-def test_plain_matmul_f32_input_and_accumulate(n):
-    k_in, n_out = 1536, 7168
+def test_plain_matmul_f32_input_and_accumulate(n, k_in, n_out):
     q, dq = _planes(n_out, k_in, seed=3)["down"]
     rng = np.random.default_rng(n)
     xf = (rng.standard_normal((n, k_in)) * 1e4).astype(np.float32)  # h-like magnitudes
@@ -62,9 +64,12 @@ def test_plain_matmul_f32_input_and_accumulate(n):
     assert rel < 1e-5, rel
 
 
-def test_plain_matmul_integer_exact():
-    """Unit scales and integer activations: every product and sum is exact."""
-    n, k_in, n_out = 4, 512, 128
+# 7168 -> 128: two 64-row blocks, K split into ranges of one 256-wide chunk each
+@pytest.mark.parametrize("k_in,n_out", [(512, 128), (7168, 128)])
+def test_plain_matmul_integer_exact(k_in, n_out):
+    """Unit scales and integer activations: every product and sum is exact (|partial
+    sums| < 127 * 6 * 7168 < 2^24), whatever the split of K."""
+    n = 4
     q = np.random.default_rng(1).integers(-127, 128, size=(n_out, k_in)).astype(np.int8)
     dq = np.full((n_out, k_in // 32), 0x3C00, dtype=np.uint16)  # fp16 1.0
     xi = np.random.default_rng(2).integers(-6, 7, size=(n, k_in))
@@ -101,3 +106,22 @@ def test_rows_do_not_depend_on_the_block():
     for r in (0, 7, 15):
         one = _run(1, d, f, to_dev_u16(x[r:r + 1]), B.MOE_DTYPE_BF16, *args, B.MOE_EPI_SWIGLU)
         assert np.array_equal(one[0].view(np.uint32), blk[r].view(np.uint32)), r
+
+
+def test_plain_matmul_reuses_its_workspace():
+    """Consecutive calls on one workspace with K split (7168 -> 1536) give the result
+    of a fresh workspace, bit for bit: every call leaves the arrival counters of its
+    split row blocks at zero."""
+    ensure_built()
+    k_in, n_out, n = 7168, 1536, 8
+    q, dq = _planes(n_out, k_in, seed=6)["down"]
+    args = (_dev(q, None), _dev(dq.view(np.int16), torch.int16), None, None, B.MOE_EPI_NONE)
+    x = to_dev_u16(syn.x_rows(23, range(n), k_in))
+    want = _run(n, k_in, n_out, x, B.MOE_DTYPE_BF16, *args)
+    ws = torch.zeros(B.q8_0_workspace_size(n, k_in, n_out), dtype=torch.uint8, device="cuda")
+    for rep in range(4):
+        y = torch.full((n, n_out), float("nan"), dtype=torch.float32, device="cuda")
+        B.q8_0_block_matmul(n, k_in, n_out, x, B.MOE_DTYPE_BF16, *args, y, ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32)), rep
+    assert B.moe_get_error(ws) == 0

@@ -59,7 +59,14 @@ def test_noalloc_matches_allocating_entry_point_on_consecutive_calls():
     h = torch.from_numpy(np.random.default_rng(32).standard_normal((16, f)).astype(np.float32) * 1e4).cuda()
     got, want = _both(16, f, d, h, B.MOE_DTYPE_F32, *w["down"], None, None, B.MOE_EPI_NONE)
     _close(got, want)
-    # no device-side error in either call (the error word collects them until read)
+    # call 3: a plain 16-row 7168 -> 1536 projection, whose K is split (partial sums
+    # and arrival counters in the array)
+    x3 = to_dev_u16(syn.x_rows(33, range(16), d))
+    qd, dd = w["gate"]
+    for _ in range(2):
+        got, want = _both(16, d, f, x3, B.MOE_DTYPE_BF16, qd, dd, None, None, B.MOE_EPI_NONE)
+        _close(got, want)
+    # no device-side error in any call (the error word collects them until read)
     assert B.q8_0_noalloc_get_error() == 0
 
 
