@@ -37,7 +37,10 @@ namespace moe {
 constexpr int EX_CW = 8;                      // consumer warps
 constexpr int EX_CT = EX_CW * 32;             // consumer threads
 constexpr int EX_THREADS = EX_CT + 32;        // + producer warp
-constexpr int EX_NST = 8;                     // ring stages
+// ring stages: the consumers, not the copies, set the pace (~15 GB/s per SM), so a
+// deeper ring only adds bytes in flight, which lengthens the memory round trips of
+// the kernels running beside it (the routing)
+constexpr int EX_NST = 4;
 constexpr int EX_CTAS_PER_SM = 1;
 constexpr int EX_CODE_BYTES = 16384;
 constexpr int EX_STAGE = 17408;               // codes + scales

@@ -58,11 +58,14 @@ constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
 
-// Two configurations: blocks of up to 5 rows (32 activation rows, 4-stage ring)
-// and of up to 16 rows or prefill chunks (80 activation rows, 3-stage ring).
+// Two configurations: blocks of up to 5 rows (32 activation rows) and of up to 16
+// rows or prefill chunks (80 activation rows), both with a 3-stage ring.  Three
+// 40 KB stages per SM stream the weights as fast as four did, and the fewer bytes
+// in flight shorten every other memory round trip of the launch (the hand-overs
+// from gate/up to down items, the claims).
 template <int NBM>
 struct Cfg {
-    static constexpr int NST = NBM == 32 ? 4 : 3;      // ring stages
+    static constexpr int NST = 3;                      // ring stages
     static constexpr int B_BYTES = KCH * NBM * 128;    // B of a stage: KCH regions of NBM rows x 128 B
     static constexpr int STAGE = A_BYTES + B_BYTES;    // a multiple of 1024
     static constexpr int SCB = SA_BYTES;               // one per-item A-scale buffer (two, by item parity)
