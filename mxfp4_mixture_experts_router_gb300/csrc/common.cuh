@@ -31,6 +31,7 @@ enum Ctrl : int {
     CTRL_PREP_SH = 10,   // rows of the block claimed for the shared experts' f16 copy
     CTRL_PREPD_SH = 11,  // rows of that copy written
     CTRL_RT_DONE = 12,   // routing finishers done with their rows' f16 copies
+    CTRL_EPOCH_TC = 13,  // launches of the block-scaled expert kernel on this workspace (tags its partial sums)
     CTRL_XMAX = 64,      // [64, 96): per-row max |x| bits published by the router GEMV CTAs
     CTRL_TL = 96,        // [96, 128): kernel timeline, 4 kernels x (~first start, last end) as u64 pairs
     CTRL_WORDS = 128
@@ -57,7 +58,7 @@ constexpr int SH_K_SPLIT = 8;
 
 struct WsLayout {
     size_t ctrl, uexp, uorder, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_cnt, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
         rbits, rbits2, rbase, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
@@ -99,10 +100,10 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     // at most E + N*k/16 of them; one finished-tile counter per chunk
     const int64_t chunks = E + (N * k + 15) / 16;
     L.gu_done_tc = take((size_t)chunks * 4);
-    // split-K gate/up partial sums: [f/64 tiles][TC_GU_SPLIT][routed pairs][64 gate + 64 up]
-    // floats, and one arrival counter per (chunk, tile)
-    L.gu_part = take((size_t)(f / 64) * TC_GU_SPLIT * (N * k) * 128 * 4);
-    L.gu_cnt = take((size_t)chunks * (f / 64) * 4);
+    // split-K gate/up partial sums of every split but the last (which adds them):
+    // [f/64 tiles][TC_GU_SPLIT - 1][routed pairs][64 gate + 64 up] 8-byte words, each a
+    // float and the tag of the launch that wrote it
+    L.gu_part = take((size_t)(f / 64) * (TC_GU_SPLIT - 1) * (N * k) * 128 * 8);
     // the shared-expert call's own activation copy and counters: it runs beside
     // the routing kernel, which resets the layer's counters
     L.x16s = take((size_t)N * d * 2);

@@ -115,8 +115,9 @@ struct Params {
     const int* order;      // MOE_MODE_ORDERED: position -> index into uexp/off, else null
     const int* pair;
     uint32_t* gu_done;
-    uint32_t* gu_cnt;
-    float* gu_part;
+    // the gate/up sums of every split but the last: 8-byte words (float bits, tag),
+    // [tile][split < S-1][pair][128]; a word is this launch's when its tag is
+    unsigned long long* gu_part;
     const uint8_t* x_mx;   // packed E2M1 terms of the block's rows (row T n + t) [rows][d/2], scales [rows][d/32]
     const uint8_t* x_sc;
     uint8_t* h_mx;         // packed E2M1 terms of the pairs' SwiGLU activations (row T P + t) [rows][f/2], scales
@@ -705,9 +706,40 @@ __device__ void mma_issuer(const Params& p, unsigned char* smem, uint32_t tbase,
     mbar_wait(done, 0);
 }
 
+// A partial sum with the tag of the launch that wrote it: one 8-byte word, written
+// and read whole, so a reader that sees the tag sees the value stored with it.
+__device__ __forceinline__ unsigned long long tagged(float v, uint32_t tag) {
+    return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+
+// The gate and up sums of one output row from another split: each word is read
+// from L2 until it carries this launch's tag (bounded: after the wait limit, or once
+// any wait of the launch has given up, the timeout bit is set and the words are
+// taken as they are).
+__device__ __forceinline__ void tagged_pair(const Params& p, const unsigned long long* pg,
+                                            const unsigned long long* pu, uint32_t tag, float& g, float& u) {
+    unsigned long long wg = __ldcg(pg), wu = __ldcg(pu);
+    if ((uint32_t)(wg >> 32) != tag || (uint32_t)(wu >> 32) != tag) {
+        const uint64_t t0 = global_ns();
+        while (true) {
+            __nanosleep(64);
+            if ((uint32_t)(wg >> 32) != tag) wg = __ldcg(pg);
+            if ((uint32_t)(wu >> 32) != tag) wu = __ldcg(pu);
+            if ((uint32_t)(wg >> 32) == tag && (uint32_t)(wu >> 32) == tag) break;
+            if (timed_out(p.ctrl)) break;
+            if (global_ns() - t0 > WAIT_LIMIT_NS) {
+                set_error(p.ctrl, MOE_EBIT_TIMEOUT);
+                break;
+            }
+        }
+    }
+    g = __uint_as_float((uint32_t)wg);
+    u = __uint_as_float((uint32_t)wu);
+}
+
 // warps 6..9: TMEM lane quadrant q = warp % 4, accumulator row m = 32q + lane
 template <int NBM>
-__device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag, uint64_t* acc_full,
+__device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t tag, uint64_t* acc_full,
                          uint64_t* acc_empty, const AccMeta* am) {
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
@@ -765,25 +797,25 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
                     xch[xch_at(m, n)] = sum;
                 }
             epi_sync();
-            // this split's sums for the expert's pairs: part[tile][split][pair][128]
-            const size_t tile_base = (size_t)a.blk * S * p.nk;
-            for (int task = ew; task < 2 * r; task += 4) {
-                const int col = task >> 1, half = task & 1;
-                const int P = o0 + col;
-                const int row = 64 * half + lane;
-                float* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + P) * 128;
-                dst[row] = xch[xch_at(row, col)];
-                dst[row + 32] = xch[xch_at(row + 32, col)];
-            }
-            __threadfence();
-            epi_sync();
-            if (ew == 0 && lane == 0)
-                *eflag = atomicAdd(p.gu_cnt + (size_t)a.c * p.n_gu + a.blk, 1u) == (uint32_t)(S - 1);
-            epi_sync();
-            if (*eflag) {
-                // the tile's last split: sum the splits in split order, then SwiGLU
-                __threadfence();
-                const int j0 = a.blk * 64;
+            const int j0 = a.blk * 64;
+            const size_t tile_base = (size_t)a.blk * (S - 1) * p.nk;
+            if (a.split < S - 1) {
+                // not the last split: its sums for the expert's pairs go out as tagged
+                // words, part[tile][split][pair][128]; each word is checked on its own by
+                // the last split, so neither a fence nor a counter is needed
+                for (int task = ew; task < 2 * r; task += 4) {
+                    const int col = task >> 1, half = task & 1;
+                    const int P = o0 + col;
+                    const int row = 64 * half + lane;
+                    unsigned long long* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + P) * 128;
+                    dst[row] = tagged(xch[xch_at(row, col)], tag);
+                    dst[row + 32] = tagged(xch[xch_at(row + 32, col)], tag);
+                }
+                epi_sync();  // every read of xch is done before the next item writes it
+            } else {
+                // the tile's last split: the splits' sums in split order (its own from
+                // shared memory, the others' once their words carry this launch's tag),
+                // then SwiGLU
                 bool wrote = false;
                 for (int task = ew; task < 2 * r; task += 4) {
                     const int col = task >> 1, jb = task & 1;
@@ -791,11 +823,15 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
                     const int j = 32 * jb + lane;
                     float g = 0.f, u = 0.f;
 #pragma unroll
-                    for (int s = 0; s < S; s++) {
-                        const float* src = p.gu_part + (tile_base + (size_t)s * p.nk + P) * 128;
-                        g += __ldcg(src + j);
-                        u += __ldcg(src + 64 + j);
+                    for (int s = 0; s < S - 1; s++) {
+                        const unsigned long long* src = p.gu_part + (tile_base + (size_t)s * p.nk + P) * 128;
+                        float gs, us;
+                        tagged_pair(p, src + j, src + 64 + j, tag, gs, us);
+                        g += gs;
+                        u += us;
                     }
+                    g += xch[xch_at(j, col)];
+                    u += xch[xch_at(64 + j, col)];
                     const float hv = g / (1.f + expf(-g)) * u;
                     if (p.debug) {
                         const size_t o = (size_t)(p.n_shared * N + P) * p.f + j0 + j;
@@ -812,7 +848,7 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, int* eflag
                     wrote = true;
                 }
                 if (wrote) __threadfence();
-                epi_sync();
+                epi_sync();  // also: every read of xch is done before the next item writes it
                 if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.c, 1u);
             }
         } else {
@@ -859,7 +895,6 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     AccMeta* am = reinterpret_cast<AccMeta*>(meta + C::NST);
     static_assert((4 * C::NST + 9) * 8 + C::NST * sizeof(Meta) + 2 * sizeof(AccMeta) + 8 <= 1024, "barrier area");
     uint32_t* tslot = reinterpret_cast<uint32_t*>(am + 2);
-    int* eflag = reinterpret_cast<int*>(tslot + 1);
     __shared__ int s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -896,10 +931,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     if (!p.after_shared) griddep_wait();
     griddep_launch_dependents();
     __shared__ int s_u;
+    __shared__ uint32_t s_tag;
     // the producer's first claim goes out now: its latency overlaps the loads below
     int first = 0;
     if (tid == 0) {
         s_u = (int)ld_acquire(p.ctrl + CTRL_UNIQUE);
+        // this launch's tag: one more than the launches before it on this workspace
+        // (never 0, the value of a zeroed workspace)
+        s_tag = __ldcg(p.ctrl + CTRL_EPOCH_TC) + 1u;
         first = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
     }
     __syncthreads();
@@ -949,7 +988,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     } else if (warp < 6) {
         scale_mover<NBM>(p, smem, scbuf, sbs, tbase, mready, scf, sce, sfr, meta, tok, tokb);
     } else {
-        epilogue<NBM>(p, tbase, xch, eflag, acc_full, acc_empty, am);
+        epilogue<NBM>(p, tbase, xch, s_tag, acc_full, acc_empty, am);
     }
 
     fence_before();
@@ -966,10 +1005,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         __threadfence();
         const int V = cp[U];
         for (int i = tid; i < V; i += NTHREADS) p.gu_done[i] = 0;
-        for (int i = tid; i < V * p.n_gu; i += NTHREADS) p.gu_cnt[i] = 0;
         if (tid == 0) {
             p.ctrl[CTRL_WORK_TC] = 0;
             p.ctrl[CTRL_EXIT_TC] = 0;
+            p.ctrl[CTRL_EPOCH_TC] = s_tag;  // the next launch tags with s_tag + 1
         }
     }
     if (tid == 0) tl_end(p.ctrl, TL_ROUTED);
@@ -1103,8 +1142,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.order = (mode & MOE_MODE_ORDERED) ? reinterpret_cast<const int*>(base + L.uorder) : nullptr;
     p.pair = reinterpret_cast<const int*>(base + L.pair);
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
-    p.gu_cnt = reinterpret_cast<uint32_t*>(base + L.gu_cnt);
-    p.gu_part = reinterpret_cast<float*>(base + L.gu_part);
+    p.gu_part = reinterpret_cast<unsigned long long*>(base + L.gu_part);
     p.x_mx = reinterpret_cast<const uint8_t*>(base + L.x_mx);
     p.x_sc = reinterpret_cast<const uint8_t*>(base + L.x_sc);
     p.h_mx = reinterpret_cast<uint8_t*>(base + L.h_mx);
