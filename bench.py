@@ -601,6 +601,32 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": "ok", "rows": len(rows), "pool_experts": len(experts)}))
 
 
+def run_spine_profile_case(args):
+    """Small case for `ncu`: the Q8_0 spine matmul 7168 -> 1536 on one row (11.8 MB of
+    weights, the first of SPINE_SHAPES), four calls, L2 flushed before each."""
+    import torch
+
+    from mxfp4_mixture_experts_router_gb300 import binding as B
+    from mxfp4_mixture_experts_router_gb300 import build as build_mod
+    build_mod.build()
+    k_in, n_out = SPINE_SHAPES[0]
+    n = args.profile_rows
+    key = int(syn.stream_key(SEED, 77, k_in, n_out))
+    q = torch.from_numpy(syn.u64(key, 0, n_out * k_in // 8).view(np.int8)).cuda()
+    dq = torch.from_numpy(((1e-3 + 9e-3 * syn.uniform01(key + 1, 0, n_out * k_in // 32)).astype(np.float16))
+                          .view(np.int16)).cuda()
+    x = torch.from_numpy(syn.x_rows(SEED, range(n), k_in).view(np.int16)).cuda().view(torch.uint16)
+    ws = torch.zeros(B.q8_0_workspace_size(n, k_in, n_out), dtype=torch.uint8, device="cuda")
+    y = torch.empty((n, n_out), dtype=torch.float32, device="cuda")
+    flush = L2Flush(torch, torch.device("cuda"))
+    for _ in range(4):
+        flush.zero_()
+        B.q8_0_block_matmul(n, k_in, n_out, x, B.MOE_DTYPE_BF16, q, dq, None, None, B.MOE_EPI_NONE, y, ws)
+    torch.cuda.synchronize()
+    assert B.moe_get_error(ws) == 0
+    print(json.dumps({"spine_profile_case": "ok", "shape": [k_in, n_out], "rows": n}))
+
+
 def gpu_body_pool(torch, n_bodies: int, seed: int):
     """n_bodies synthetic MXFP4 expert slabs in a pinned host pool, drawn on the GPU
     from a seeded generator: uniform code bytes, E8M0 scale bytes 120 + (byte mod 8)
@@ -894,10 +920,15 @@ def main():
     ap.add_argument("--prefill-rows", default="270,1533")
     ap.add_argument("--prefill-steps", type=int, default=5)
     ap.add_argument("--prefill-warmup", type=int, default=2)
+    ap.add_argument("--spine-profile-case", action="store_true",
+                    help="run the small Q8_0 spine matmul case for ncu and exit")
     ap.add_argument("--prefill-profile-case", action="store_true",
                     help="run the small prefill ncu case (270 rows over 160 experts, 2.8 GB) and exit")
     args = ap.parse_args()
 
+    if args.spine_profile_case:
+        run_spine_profile_case(args)
+        return
     if args.prefill_profile_case:
         run_prefill_profile_case(args)
         return

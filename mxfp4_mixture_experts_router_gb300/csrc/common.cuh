@@ -58,7 +58,7 @@ constexpr int SH_K_SPLIT = 8;
 
 struct WsLayout {
     size_t ctrl, uexp, uorder, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_state, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
         rbits, rbits2, rbase, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
@@ -100,10 +100,11 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     // at most E + N*k/16 of them; one finished-tile counter per chunk
     const int64_t chunks = E + (N * k + 15) / 16;
     L.gu_done_tc = take((size_t)chunks * 4);
-    // split-K gate/up partial sums of every split but the last (which adds them):
-    // [f/64 tiles][TC_GU_SPLIT - 1][routed pairs][64 gate + 64 up] 8-byte words, each a
-    // float and the tag of the launch that wrote it
-    L.gu_part = take((size_t)(f / 64) * (TC_GU_SPLIT - 1) * (N * k) * 128 * 8);
+    // split-K gate/up partial sums: [f/64 tiles][TC_GU_SPLIT][routed pairs][64 gate + 64
+    // up] 8-byte words, each a float and the tag of the launch that wrote it, and per
+    // (chunk, tile) the bits of the splits that published their sums
+    L.gu_part = take((size_t)(f / 64) * TC_GU_SPLIT * (N * k) * 128 * 8);
+    L.gu_state = take((size_t)chunks * (f / 64) * 4);
     // the shared-expert call's own activation copy and counters: it runs beside
     // the routing kernel, which resets the layer's counters
     L.x16s = take((size_t)N * d * 2);

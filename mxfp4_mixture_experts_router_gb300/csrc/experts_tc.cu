@@ -57,6 +57,7 @@ constexpr int CHUNK = 16;                   // pairs of one expert per work item
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
+static_assert(S == 2, "the gate/up hand-over pairs exactly two splits");
 
 // Two configurations: blocks of up to 5 rows (32 activation rows) and of up to 16
 // rows or prefill chunks (80 activation rows), both with a 3-stage ring.  Three
@@ -115,9 +116,10 @@ struct Params {
     const int* order;      // MOE_MODE_ORDERED: position -> index into uexp/off, else null
     const int* pair;
     uint32_t* gu_done;
-    // the gate/up sums of every split but the last: 8-byte words (float bits, tag),
-    // [tile][split < S-1][pair][128]; a word is this launch's when its tag is
+    // the gate/up sums a split publishes for the other: 8-byte words (float bits,
+    // tag), [tile][split][pair][128]; a word is this launch's when its tag is
     unsigned long long* gu_part;
+    uint32_t* gu_state;  // per (chunk, tile): bit s set once split s has published
     const uint8_t* x_mx;   // packed E2M1 terms of the block's rows (row T n + t) [rows][d/2], scales [rows][d/32]
     const uint8_t* x_sc;
     uint8_t* h_mx;         // packed E2M1 terms of the pairs' SwiGLU activations (row T P + t) [rows][f/2], scales
@@ -744,6 +746,7 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
     const int N = p.n_rows;
+    __shared__ int s_flag;  // the epilogue warps' shared decision of the current gate/up item
     uint32_t it = 0;
     while (true) {
         const uint32_t b = it & 1u;
@@ -796,42 +799,76 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
                     for (int tt = 1; tt < T; tt++) sum += __uint_as_float(v[T * n + tt]);
                     xch[xch_at(m, n)] = sum;
                 }
+            if (ew == 0 && lane == 0) s_flag = 1;
             epi_sync();
+            // The two splits of a tile meet here; exactly one of them adds the sums:
+            //  - split 1 reads split 0's words first; if they all carry this launch's
+            //    tag it combines at once, with no atomic;
+            //  - otherwise a split publishes its own sums as tagged words and sets its
+            //    bit in the tile's state word (split 0 always does); the one that finds
+            //    the other's bit already set combines.
+            // Either way the sums are added in split order, so the result does not
+            // depend on which split combined.
             const int j0 = a.blk * 64;
-            const size_t tile_base = (size_t)a.blk * (S - 1) * p.nk;
-            if (a.split < S - 1) {
-                // not the last split: its sums for the expert's pairs go out as tagged
-                // words, part[tile][split][pair][128]; each word is checked on its own by
-                // the last split, so neither a fence nor a counter is needed
+            const size_t tile_base = (size_t)a.blk * S * p.nk;
+            const unsigned long long* osrc = p.gu_part + (tile_base + (size_t)(1 - a.split) * p.nk + o0) * 128;
+            float og[2] = {0.f, 0.f}, ou[2] = {0.f, 0.f};  // the other split's sums of this thread's first two tasks
+            bool have = a.split == 1;
+            if (a.split == 1) {
+#pragma unroll
+                for (int q2 = 0; q2 < 2; q2++) {
+                    const int task = ew + 4 * q2;
+                    if (task < 2 * r) {
+                        const int col = task >> 1, jrow = 32 * (task & 1) + lane;
+                        const unsigned long long wg = __ldcg(osrc + (size_t)col * 128 + jrow);
+                        const unsigned long long wu = __ldcg(osrc + (size_t)col * 128 + 64 + jrow);
+                        have = have && (uint32_t)(wg >> 32) == tag && (uint32_t)(wu >> 32) == tag;
+                        og[q2] = __uint_as_float((uint32_t)wg);
+                        ou[q2] = __uint_as_float((uint32_t)wu);
+                    }
+                }
+                if (!have) s_flag = 0;
+                epi_sync();
+            }
+            int combine = a.split == 1 ? s_flag : 0;
+            if (!combine) {
+                // publish: part[tile][split][pair][128], one tagged word per sum (the
+                // reader checks every word's tag, so no fence is needed)
                 for (int task = ew; task < 2 * r; task += 4) {
                     const int col = task >> 1, half = task & 1;
-                    const int P = o0 + col;
                     const int row = 64 * half + lane;
-                    unsigned long long* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + P) * 128;
+                    unsigned long long* dst = p.gu_part + (tile_base + (size_t)a.split * p.nk + o0 + col) * 128;
                     dst[row] = tagged(xch[xch_at(row, col)], tag);
                     dst[row + 32] = tagged(xch[xch_at(row + 32, col)], tag);
                 }
-                epi_sync();  // every read of xch is done before the next item writes it
-            } else {
-                // the tile's last split: the splits' sums in split order (its own from
-                // shared memory, the others' once their words carry this launch's tag),
-                // then SwiGLU
+                epi_sync();
+                if (ew == 0 && lane == 0) {
+                    const uint32_t mine = 1u << a.split;
+                    s_flag = (atomicOr(p.gu_state + (size_t)a.c * p.n_gu + a.blk, mine) & (3u ^ mine)) != 0u;
+                }
+                epi_sync();
+                combine = s_flag;
+                have = false;  // the other split's words are read again below
+            }
+            if (combine) {
                 bool wrote = false;
-                for (int task = ew; task < 2 * r; task += 4) {
+                for (int task = ew, q2 = 0; task < 2 * r; task += 4, q2++) {
                     const int col = task >> 1, jb = task & 1;
                     const int P = o0 + col;
                     const int j = 32 * jb + lane;
-                    float g = 0.f, u = 0.f;
-#pragma unroll
-                    for (int s = 0; s < S - 1; s++) {
-                        const unsigned long long* src = p.gu_part + (tile_base + (size_t)s * p.nk + P) * 128;
-                        float gs, us;
-                        tagged_pair(p, src + j, src + 64 + j, tag, gs, us);
-                        g += gs;
-                        u += us;
+                    float go, uo;
+                    if (have && q2 < 2) {
+                        go = q2 == 0 ? og[0] : og[1];
+                        uo = q2 == 0 ? ou[0] : ou[1];
+                    } else {
+                        tagged_pair(p, osrc + (size_t)col * 128 + j, osrc + (size_t)col * 128 + 64 + j, tag, go, uo);
                     }
-                    g += xch[xch_at(j, col)];
-                    u += xch[xch_at(64 + j, col)];
+                    const float gm = xch[xch_at(j, col)], um = xch[xch_at(64 + j, col)];
+                    float g = 0.f, u = 0.f;  // split 0's sums, then split 1's
+                    g += a.split == 0 ? gm : go;
+                    u += a.split == 0 ? um : uo;
+                    g += a.split == 0 ? go : gm;
+                    u += a.split == 0 ? uo : um;
                     const float hv = g / (1.f + expf(-g)) * u;
                     if (p.debug) {
                         const size_t o = (size_t)(p.n_shared * N + P) * p.f + j0 + j;
@@ -848,8 +885,10 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
                     wrote = true;
                 }
                 if (wrote) __threadfence();
-                epi_sync();  // also: every read of xch is done before the next item writes it
+                epi_sync();  // also: every read of xch and s_flag is done before the next item
                 if (ew == 0 && lane == 0) red_release_add(p.gu_done + a.c, 1u);
+            } else {
+                epi_sync();  // every read of xch and s_flag is done before the next item
             }
         } else {
             const int m0 = a.blk * 128;
@@ -1005,6 +1044,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         __threadfence();
         const int V = cp[U];
         for (int i = tid; i < V; i += NTHREADS) p.gu_done[i] = 0;
+        for (int i = tid; i < V * p.n_gu; i += NTHREADS) p.gu_state[i] = 0;
         if (tid == 0) {
             p.ctrl[CTRL_WORK_TC] = 0;
             p.ctrl[CTRL_EXIT_TC] = 0;
@@ -1143,6 +1183,7 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.pair = reinterpret_cast<const int*>(base + L.pair);
     p.gu_done = reinterpret_cast<uint32_t*>(base + L.gu_done_tc);
     p.gu_part = reinterpret_cast<unsigned long long*>(base + L.gu_part);
+    p.gu_state = reinterpret_cast<uint32_t*>(base + L.gu_state);
     p.x_mx = reinterpret_cast<const uint8_t*>(base + L.x_mx);
     p.x_sc = reinterpret_cast<const uint8_t*>(base + L.x_sc);
     p.h_mx = reinterpret_cast<uint8_t*>(base + L.h_mx);
