@@ -31,7 +31,11 @@
  * Conventions shared by every call
  * --------------------------------
  * - Every pointer argument is a DEVICE pointer unless it is documented as a
- *   host pointer (descriptors and pools are host structs).
+ *   host pointer (descriptors and pools are host structs).  The block's rows and
+ *   the combine's residual and output (x of moe_route and moe_shared_experts*,
+ *   residual and out of moe_combine) may instead point into pinned host memory,
+ *   which the device addresses directly: the kernels then read the rows and write
+ *   the output in place over the host link, with no copy launches.
  * - The caller owns every buffer.  No call allocates device memory.
  * - Every compute call is asynchronous on the given stream (a cudaStream_t
  *   passed as void*; NULL means the legacy default stream) and returns a

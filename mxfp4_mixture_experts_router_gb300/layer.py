@@ -14,6 +14,13 @@ import torch
 from . import binding as B
 
 
+def _device_readable(t, name):
+    """The kernels take device memory or pinned host memory (mapped into the device's
+    address space); pageable host memory is refused."""
+    if not t.is_cuda and not t.is_pinned():
+        raise ValueError(f"{name} must be a device tensor or a pinned host tensor")
+
+
 class MoeLayer:
     def __init__(self, d_model: int, d_ff: int, n_experts: int, top_k: int, n_rows_max: int = 16,
                  n_shared: int = 0, device: str | int = "cuda"):
@@ -101,6 +108,7 @@ class MoeLayer:
             raise ValueError("logits_in must be a contiguous float32 tensor of n_rows x n_experts")
         if x.element_size() != 2 or not x.is_contiguous():
             raise ValueError("x must be contiguous bf16 rows (2-byte elements)")
+        _device_readable(x, "x")
         B.moe_route(self.desc, n_rows, x, self.router if logits_in is None else None, logits_in,
                     self.logits if logits_in is None else None, self.topk_idx, self.topk_w, self.ws,
                     self.n_rows_max, self.n_shared, stream)
@@ -116,28 +124,37 @@ class MoeLayer:
         fn = B.moe_shared_experts_after_route if after_route else B.moe_shared_experts
         fn(self.desc, n_rows, x, self.shared_pool_desc(), self.n_shared, self.ws, self.n_rows_max, stream)
 
-    def combine(self, n_rows: int, residual, stream=None):
+    def combine(self, n_rows: int, residual, stream=None, out=None):
+        _device_readable(residual, "residual")
+        out = self.out if out is None else out
+        _device_readable(out, "out")
+        if out.dtype != torch.uint16 or not out.is_contiguous() or out.numel() < n_rows * self.d:
+            raise ValueError("out must be a contiguous uint16 (bf16 bits) tensor of n_rows x d_model")
         shared_y = self.ws.data_ptr() + self.offsets.shared_y if self.n_shared else None
         B.moe_combine(self.desc, n_rows, residual, self.y_part, self.topk_w, shared_y, self.n_shared,
-                      self.out, stream)
+                      out, stream)
 
     def forward(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
-                stream=None):
-        """Run one block: x, residual bf16 bits [N][d] on the device; returns out bits [N][d].
+                stream=None, out=None):
+        """Run one block: x, residual bf16 bits [N][d]; returns out bits [N][d].
 
         One stream: the routing, the shared experts (their kernel starts beside the
         routing: they need x only), the routed experts, the combine; each launch after
-        the routing overlaps the tail of the one before it."""
+        the routing overlaps the tail of the one before it.
+
+        x, residual and out live on the device, or in pinned host memory: the kernels
+        then read the rows and write the output in place over the host link (no copy
+        launches).  out defaults to ``self.out``."""
         n = x.shape[0] if n_rows is None else n_rows
-        self._block(n, x, residual, logits_in, mode, None)
-        return self.out[:n]
+        self._block(n, x, residual, logits_in, mode, None, out)
+        return (self.out if out is None else out)[:n]
 
     def _side(self):
         if getattr(self, "_side_stream", None) is None:
             self._side_stream = torch.cuda.Stream(device=self.device)
         return self._side_stream
 
-    def _block(self, n, x, residual, logits_in, mode, evs):
+    def _block(self, n, x, residual, logits_in, mode, evs, out=None):
         """route -> shared experts -> routed experts -> combine on the current stream.
         evs, if given: 5 events recorded at the start, once the routing has completed,
         once the shared experts have (and the routing), once the routed experts have,
@@ -169,13 +186,13 @@ class MoeLayer:
             self.experts(n, mode=mode)
         if evs:
             mark(evs[3])
-        self.combine(n, residual)
+        self.combine(n, residual, out=out)
         if evs:
             main.wait_stream(self._side())
             evs[4].record(main)
 
     def capture(self, x, residual, n_rows: int | None = None, logits_in=None, mode=B.MOE_MODE_DECODE,
-                events: bool = False):
+                events: bool = False, host_in=None, host_out=None, out=None):
         """Capture one block (route -> experts -> combine) into a CUDA graph.
 
         The graph reads the block from the given device buffers (x, residual and, if
@@ -185,18 +202,32 @@ class MoeLayer:
         does.  With events=True five timing events are recorded inside the graph (at
         the start, after the routing, after the shared experts, after the routed
         experts, at the end) and returned; the events are None if the runtime refuses
-        them."""
+        them.
+
+        host_in / host_out: pinned host tensors shaped like x[:n] / self.out[:n]; the
+        graph then starts by copying host_in into x and ends by copying the output
+        into host_out, so one replay takes a block from host memory to host memory.
+        Without copies: pass pinned host tensors as x / residual and as out (as for
+        forward()); the kernels then read and write them in place."""
         import torch as _torch
         n = x.shape[0] if n_rows is None else n_rows
         side = _torch.cuda.Stream()
         side.wait_stream(_torch.cuda.current_stream())
         with _torch.cuda.stream(side):  # first launches (kernel attributes) outside the capture
-            self.forward(x, residual, n_rows=n, logits_in=logits_in, mode=mode)
+            self.forward(x, residual, n_rows=n, logits_in=logits_in, mode=mode, out=out)
         _torch.cuda.current_stream().wait_stream(side)
         _torch.cuda.synchronize()
 
+        for t, name in ((host_in, "host_in"), (host_out, "host_out")):
+            if t is not None and (t.is_cuda or not t.is_pinned()):
+                raise ValueError(f"{name} must be a pinned host tensor")
+
         def body(evs):
-            self._block(n, x, residual, logits_in, mode, evs)
+            if host_in is not None:
+                x[:n].copy_(host_in, non_blocking=True)
+            self._block(n, x, residual, logits_in, mode, evs, out)
+            if host_out is not None:
+                host_out.copy_((self.out if out is None else out)[:n], non_blocking=True)
 
         evs = None
         if events:

@@ -221,6 +221,57 @@ def test_layer_graph_with_timing_events_matches_forward():
     assert L.error_bits() == 0
 
 
+def test_layer_graph_from_host_to_host():
+    """A graph captured with pinned host buffers copies each block's rows in, runs the
+    layer and copies the output back: new rows written into the host buffer between
+    replays give the outputs of forward() on those rows."""
+    lay = SeededLayer(TINY_SHARED, seed=14, n_rows_max=16)
+    L = lay.layer
+    n = 2
+    rows = [syn.x_rows(14, range(5 * i, 5 * i + n), TINY.d_model) for i in range(3)]
+    x = to_dev_u16(rows[0])
+    res = to_dev_u16(syn.x_rows(14, range(n), TINY.d_model, tag=syn.TAG_RESIDUAL))
+    hin = torch.from_numpy(rows[0].view(np.int16)).view(torch.uint16).pin_memory()
+    hout = torch.zeros((n, TINY.d_model), dtype=torch.uint16).pin_memory()
+    g, _ = L.capture(x, res, host_in=hin, host_out=hout)
+    for r in rows:
+        want = L.forward(to_dev_u16(r), res).clone().cpu()
+        hin.copy_(torch.from_numpy(r.view(np.int16)).view(torch.uint16))
+        hout.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(hout, want)
+    with pytest.raises(ValueError):
+        L.capture(x, res, host_in=x)
+    assert L.error_bits() == 0
+
+
+def test_layer_reads_and_writes_pinned_host_rows_in_place():
+    """Rows and residual in pinned host memory, output to pinned host memory: forward()
+    and a captured graph give the bits of the device-resident layer; pageable host
+    memory is refused."""
+    lay = SeededLayer(TINY_SHARED, seed=15, n_rows_max=16)
+    L = lay.layer
+    n = 3
+    xr = syn.x_rows(15, range(n), TINY.d_model)
+    rr = syn.x_rows(15, range(n), TINY.d_model, tag=syn.TAG_RESIDUAL)
+    want = L.forward(to_dev_u16(xr), to_dev_u16(rr)).clone().cpu()
+    hx = torch.from_numpy(xr.view(np.int16)).view(torch.uint16).pin_memory()
+    hr = torch.from_numpy(rr.view(np.int16)).view(torch.uint16).pin_memory()
+    ho = torch.zeros((n, TINY.d_model), dtype=torch.uint16).pin_memory()
+    got = L.forward(hx, hr, out=ho)
+    torch.cuda.synchronize()
+    assert got.data_ptr() == ho.data_ptr() and torch.equal(ho, want)
+    ho.zero_()
+    g, _ = L.capture(hx, hr, out=ho)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(ho, want)
+    with pytest.raises(ValueError):
+        L.forward(torch.from_numpy(xr.view(np.int16)).view(torch.uint16), hr, out=ho)
+    assert L.error_bits() == 0
+
+
 def test_slot_ready_flag_never_set_times_out_cleanly():
     """A slab whose ready flag nothing sets: the kernel gives up after its bounded
     wait, records MOE_EBIT_TIMEOUT and returns; the context stays usable."""
