@@ -96,9 +96,10 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.x_sc = take((size_t)L.mx_rows_x * (d / 32));
     L.h_mx = take((size_t)L.mx_rows_h * (f / 2));
     L.h_sc = take((size_t)L.mx_rows_h * (f / 32));
-    // the block-scaled kernel works on chunks of at most 16 pairs of one expert:
-    // at most E + N*k/16 of them; one finished-tile counter per chunk
-    const int64_t chunks = E + (N * k + 15) / 16;
+    // the block-scaled kernel works on chunks of at most 16 (prefill) or 6 (blocks of up
+    // to 16 rows) pairs of one expert: fewer than E + N*k of them; one finished-tile
+    // counter per chunk
+    const int64_t chunks = E + N * k;
     L.gu_done_tc = take((size_t)chunks * 4);
     // split-K gate/up partial sums: [f/64 tiles][TC_GU_SPLIT][routed pairs][64 gate + 64
     // up] 8-byte words, each a float and the tag of the launch that wrote it, and per

@@ -53,14 +53,17 @@ constexpr int T = MX_TERMS;                 // B columns (activation terms) per 
 constexpr int SC_MAX = 112;                 // scale bytes per row of one item (its K range / 32)
 constexpr int SA_BYTES = 128 * SC_MAX;      // A scales of an item
 constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens (xor-swizzled)
-constexpr int CHUNK = 16;                   // pairs of one expert per work item (80 MMA columns)
+constexpr int CHUNK = 16;                   // most pairs of one expert per work item (80 MMA columns)
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
 static_assert(S == 2, "the gate/up hand-over pairs exactly two splits");
 
-// Two configurations: blocks of up to 5 rows (32 activation rows) and of up to 16
-// rows or prefill chunks (80 activation rows), both with a 3-stage ring.  Three
+// Two configurations, both with a 3-stage ring: blocks of up to 16 rows (32
+// activation rows, chunks of up to 6 pairs) and prefill (80 activation rows, chunks
+// of up to 16 pairs).  The 80-row configuration costs about 20 % more per byte on
+// small blocks (1 row: 121 against 101 us for the layer), so decode blocks take the
+// 32-row one and split an expert with more than 6 pairs into several chunks.  Three
 // 40 KB stages per SM stream the weights as fast as four did, and the fewer bytes
 // in flight shorten every other memory round trip of the launch (the hand-overs
 // from gate/up to down items, the claims).
@@ -82,10 +85,11 @@ struct Cfg {
     static constexpr uint32_t TM_SFB = TM_SFA + NST * SF_COLS;
     static constexpr uint32_t TM_COLS = TM_SFB + NST * SF_COLS <= 256 ? 256 : 512;
     // per expert: (slot, first pair | pairs << 16) and the prefix of its chunk counts
-    static constexpr int MAX_U = NBM == 32 ? 128 : 1024;
+    static constexpr int CH = NBM / T;                 // pairs per chunk: 6 (32 columns) or 16 (80)
+    static constexpr int MAX_U = NBM == 32 ? 256 : 1024;
     // blocks of up to 5 rows: the block row of every (row, slot) pair (5 x k <= 160);
     // then the block rows of the pairs of the chunks in the two scale buffers' items
-    static constexpr int TOKS = NBM == 32 ? 160 : 0;
+    static constexpr int TOKS = NBM == 32 ? 256 : 0;
     static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 2 * CHUNK * 2 + 12;
     // each scale-mover warp's staging of the activation scale bytes, per stage
     static constexpr int SBS_BYTES = 4 * NST * NBM * 16;
@@ -94,7 +98,7 @@ struct Cfg {
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
     static_assert(SMEM <= 232448, "shared memory per CTA");
     static_assert(TM_SFB + NST * SF_COLS <= TM_COLS && NBM <= ACC_COLS && NBM <= 128, "tensor memory columns");
-    static_assert(NBM % 16 == 0 && CHUNK * T <= 80, "MMA N");
+    static_assert(NBM % 16 == 0 && CHUNK * T <= 80 && CH <= CHUNK && ((CH * T + 15) & ~15) <= NBM, "MMA N");
 };
 
 enum { IT_GU = 0, IT_DN = 1 };
@@ -265,7 +269,7 @@ struct Plan {
 };
 
 __device__ __forceinline__ void plan_item(const Params& p, int V, int U, const uint2* umeta, const int* cp, int item,
-                                          int total, Plan& q) {
+                                          int total, int ch, Plan& q) {
     q.item = item;
     if (item >= total) return;
     decode_item(p, V, item, q.type, q.cid, q.blk, q.split);
@@ -273,8 +277,8 @@ __device__ __forceinline__ void plan_item(const Params& p, int V, int U, const u
     const uint2 mu = umeta[u];
     const int o0 = (int)(mu.y & 0xFFFFu), r = (int)(mu.y >> 16);
     q.z = (int)mu.x;
-    q.p0 = o0 + CHUNK * (q.cid - cp[u]);  // the chunk's first pair
-    q.rc = min(CHUNK, o0 + r - q.p0);     // and its pairs
+    q.p0 = o0 + ch * (q.cid - cp[u]);  // the chunk's first pair
+    q.rc = min(ch, o0 + r - q.p0);     // and its pairs
 }
 
 // the chunk's pair entries (gate/up items gather the rows of their tokens); loaded
@@ -324,7 +328,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
     // atomic's round trip nor the next item's dependency load (issued right after its
     // decoding) waits in line with the stages.
     Plan cur, nxt;
-    plan_item(p, V, U, umeta, cp, first, total, cur);
+    plan_item(p, V, U, umeta, cp, first, total, C::CH, cur);
     if (tokb != nullptr) plan_pairs(p, total, cur);
     int claim_next = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
     uint32_t dep_cur = 0u;  // the current item's dependency word as last read
@@ -422,7 +426,7 @@ __device__ void producer(const Params& p, int U, const uint2* umeta, const int* 
                 // the claim two items ahead, and the decoding of the next item (claimed
                 // one item ago) with its dependency load, which lands during this item
                 claim_after = (int)atomicAdd(p.ctrl + CTRL_WORK_TC, 1u);
-                plan_item(p, V, U, umeta, cp, claim_next, total, nxt);
+                plan_item(p, V, U, umeta, cp, claim_next, total, C::CH, nxt);
                 if (tokb != nullptr) plan_pairs(p, total, nxt);
                 if (nxt.item < total) {
                     if (p.slot_ready != nullptr) dep_nxt = ld_acquire(p.slot_ready + nxt.z);
@@ -1000,7 +1004,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     if (warp == 1) {
         const int lane = tid & 31, per = (U + 31) / 32, b0 = lane * per, b1 = min(U, b0 + per);
         int sum = 0;
-        for (int u = b0; u < b1; u++) sum += ((int)(umeta[u].y >> 16) + CHUNK - 1) / CHUNK;
+        for (int u = b0; u < b1; u++) sum += ((int)(umeta[u].y >> 16) + C::CH - 1) / C::CH;
         int incl = sum;
         for (int o = 1; o < 32; o <<= 1) {
             const int up = __shfl_up_sync(0xffffffffu, incl, o);
@@ -1009,7 +1013,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         int run = incl - sum;
         for (int u = b0; u < b1; u++) {
             cp[u] = run;
-            run += ((int)(umeta[u].y >> 16) + CHUNK - 1) / CHUNK;
+            run += ((int)(umeta[u].y >> 16) + C::CH - 1) / C::CH;
         }
         if (lane == 31) cp[U] = incl;
     }
@@ -1125,10 +1129,11 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
                      cudaStream_t stream) {
     using namespace tc;
     const int d = desc->d_model, f = desc->d_ff, E = desc->n_experts, k = desc->top_k;
-    // first pair and pair count share one 32-bit word per expert; a block of up to 5
-    // rows runs the 16-column configuration (at most 5 * k experts)
-    if (n_rows * k >= 65536 || E > Cfg<80>::MAX_U || (n_rows <= 5 && n_rows * k > Cfg<32>::MAX_U))
-        return MOE_ERR_UNSUPPORTED;
+    // first pair and pair count share one 32-bit word per expert; blocks of up to 16
+    // rows with at most 256 pairs run the 32-column configuration, in chunks of up
+    // to 6 pairs (a row's arithmetic is the same in both configurations)
+    const bool small = n_rows <= 16 && n_rows * k <= Cfg<32>::TOKS;
+    if (n_rows * k >= 65536 || E > Cfg<80>::MAX_U) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(d, f, E, k, n_rows_max, n_shared);
     char* base = static_cast<char*>(ws);
     thread_local Params p;  // filled per call, copied into the launch
@@ -1191,8 +1196,8 @@ int tc_expert_launch(const moe_desc* desc, int n_rows, int mode, const moe_pool*
     p.y_part = y_part;
     p.dbg_g = reinterpret_cast<float*>(base + L.dbg_g);
     p.dbg_u = reinterpret_cast<float*>(base + L.dbg_u);
-    // a chunk holds at most min(n_rows, 16) pairs, T MMA columns each
-    return n_rows <= 5 ? launch<32>(p, stream) : launch<80>(p, stream);
+    // a chunk holds at most 6 (small blocks) or 16 pairs, T MMA columns each
+    return small ? launch<32>(p, stream) : launch<80>(p, stream);
 }
 
 }  // namespace moe
