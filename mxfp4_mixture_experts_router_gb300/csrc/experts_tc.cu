@@ -508,6 +508,7 @@ __device__ __forceinline__ void b_issue(const Params& p, const Meta& m, int t, i
         r.item = m.item;
 #pragma unroll
         for (int i = 0; i < NBM * BP / 128; i++) {
+            if (128 * i >= m.nrow * BP) break;  // no row of this or later pieces is in use
             const int row = (t + 128 * i) / BP;
             r.d[i] = row < m.nrow ? b_src_row(m, row, tok, tokb) : 0;
         }
@@ -524,6 +525,7 @@ __device__ __forceinline__ void b_issue(const Params& p, const Meta& m, int t, i
     const int k0 = m.kbase + m.chunk * KC;
 #pragma unroll
     for (int i = 0; i < NBM * BP / 128; i++) {
+        if (128 * i >= m.nrow * BP) break;  // the same in the whole warp
         const int j = t + 128 * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
         if (row < m.nrow)
             cp_async16(bst + kh * (NBM * 128) + row * 128 + ((cc ^ (row & 7)) << 4),
@@ -761,48 +763,40 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
         fence_after();
         const AccMeta a = am[b];
         if (a.item < 0) break;
-        // the item's result: its accumulators summed in order
-        float acc[NBM];
+        // The item's result, read 16 columns at a time up to the MMA's width: each
+        // column is its accumulators summed in order (0 + acc0 + acc1), and each pair's
+        // T term columns are summed in order into ps[pair].  Columns are visited in
+        // order, so a pair whose columns straddle two 16-column pieces carries on.
+        float ps[NBM / T];
+        const uint32_t ta0 = tbase + b * C::ACC_SET + ((uint32_t)(32 * q) << 16);
 #pragma unroll
-        for (int i = 0; i < NBM; i++) acc[i] = 0.f;
+        for (int h = 0; h < NBM / 16; h++) {
+            if (h > 0 && a.nb <= 16 * h) break;  // the MMA wrote nb columns (same in the whole warp)
+            uint32_t w[C::NACC][16];
 #pragma unroll
-        for (int ai = 0; ai < C::NACC; ai++) {
-            const uint32_t ta = tbase + b * C::ACC_SET + ai * C::ACC_COLS + ((uint32_t)(32 * q) << 16);
-            uint32_t t16[NBM];
-#pragma unroll
-            for (int h = 0; h < NBM / 16; h++) {
-                uint32_t w[16];
-                if (h == 0 || a.nb > 16 * h) {
-                    tm_ld16(ta + 16 * h, w);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; i++) w[i] = 0u;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; i++) t16[16 * h + i] = w[i];
-            }
+            for (int ai = 0; ai < C::NACC; ai++) tm_ld16(ta0 + ai * C::ACC_COLS + 16 * h, w[ai]);
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-            for (int i = 0; i < NBM; i++) acc[i] += __uint_as_float(t16[i]);
-        }
-        uint32_t v[NBM];
+            for (int i = 0; i < 16; i++) {
+                const int col = 16 * h + i, n = col / T, tt = col - (col / T) * T;
+                if (n < NBM / T) {
+                    float v = 0.f;
 #pragma unroll
-        for (int i = 0; i < NBM; i++) v[i] = __float_as_uint(acc[i]);
+                    for (int ai = 0; ai < C::NACC; ai++) v += __uint_as_float(w[ai][i]);
+                    ps[n] = tt == 0 ? v : ps[n] + v;
+                }
+            }
+        }
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_empty[b]);
         const int m = 32 * q + lane;
         const int o0 = a.p0, r = a.rc;  // the chunk's pairs: o0 .. o0 + r - 1, MMA columns T per pair
         if (a.type == IT_GU) {
-            // the T term columns of each pair summed in order; rows 0..63 gate, 64..127 up
+            // each pair's sum over its T term columns; rows 0..63 gate, 64..127 up
 #pragma unroll
             for (int n = 0; n < NBM / T; n++)
-                if (n < r) {
-                    float sum = __uint_as_float(v[T * n]);
-#pragma unroll
-                    for (int tt = 1; tt < T; tt++) sum += __uint_as_float(v[T * n + tt]);
-                    xch[xch_at(m, n)] = sum;
-                }
+                if (n < r) xch[xch_at(m, n)] = ps[n];
             if (ew == 0 && lane == 0) s_flag = 1;
             epi_sync();
             // The two splits of a tile meet here; exactly one of them adds the sums:
@@ -899,11 +893,8 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
 #pragma unroll
             for (int col = 0; col < NBM / T; col++) {
                 if (col < r) {
-                    float y = __uint_as_float(v[T * col]);
-#pragma unroll
-                    for (int tt = 1; tt < T; tt++) y += __uint_as_float(v[T * col + tt]);
                     const int pid = __ldcg(p.pair + o0 + col);
-                    p.y_part[(size_t)pid * p.d + m0 + m] = y;
+                    p.y_part[(size_t)pid * p.d + m0 + m] = ps[col];
                 }
             }
         }
