@@ -486,8 +486,10 @@ struct BRows {
     int s[3];
 };
 
+// no memory clobber: the copy's destination is read only after cp_async_wait (which
+// has one), so the compiler may keep everything else in registers around the copies
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src));
 }
 
 __device__ __forceinline__ void cp_async_wait(int pending) {
@@ -501,8 +503,9 @@ __device__ __forceinline__ void cp_async_wait(int pending) {
 }
 
 // issue the copies of one claimed stage (one cp.async group per thread and stage)
+// m is a copy in registers: the loop below reads its fields between the copies
 template <int NBM>
-__device__ __forceinline__ void b_issue(const Params& p, const Meta& m, int t, int lane, uint32_t bst, uint32_t sbs,
+__device__ __forceinline__ void b_issue(const Params& p, const Meta m, int t, int lane, uint32_t bst, uint32_t sbs,
                                         BRows<NBM>& r, const uint16_t* tok, const uint16_t* tokb) {
     if (r.item != m.item) {
         r.item = m.item;
@@ -890,13 +893,12 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
             }
         } else {
             const int m0 = a.blk * 128;
+            int pid[NBM / T];  // the chunk's pair ids, all loaded before the first store
 #pragma unroll
-            for (int col = 0; col < NBM / T; col++) {
-                if (col < r) {
-                    const int pid = __ldcg(p.pair + o0 + col);
-                    p.y_part[(size_t)pid * p.d + m0 + m] = ps[col];
-                }
-            }
+            for (int col = 0; col < NBM / T; col++) pid[col] = col < r ? __ldcg(p.pair + o0 + col) : 0;
+#pragma unroll
+            for (int col = 0; col < NBM / T; col++)
+                if (col < r) p.y_part[(size_t)pid[col] * p.d + m0 + m] = ps[col];
         }
         it++;
     }
