@@ -1368,7 +1368,15 @@ static int shared_experts(const moe_desc* desc, int32_t n_rows, const uint16_t* 
     p.work_word = CTRL_WORK_SH;
     p.exit_word = CTRL_EXIT_SH;
     p.x_rows = x;
-    p.x_smem = (size_t)n_rows * d * 2 <= (size_t)EX_XS_BYTES ? 1 : 0;
+    // rows in device memory: every CTA makes its own f16 copy in shared memory (from
+    // L2).  Rows in host memory (read in place over the host link): one CTA makes the
+    // copy in the workspace and the others wait for it, so the rows cross the link
+    // once rather than once per CTA.  The copy is the same either way.
+    cudaPointerAttributes pa{};
+    const cudaError_t qe = cudaPointerGetAttributes(&pa, x);
+    if (qe != cudaSuccess) (void)cudaGetLastError();  // a failed query leaves no error behind
+    const bool x_host = qe == cudaSuccess && pa.type == cudaMemoryTypeHost;
+    p.x_smem = !x_host && (size_t)n_rows * d * 2 <= (size_t)EX_XS_BYTES ? 1 : 0;
     p.dep_at_end = after_route ? 1 : 0;
     return launch_expert_kernel<MOE_FMT_MXFP4, MOE_FMT_Q8_0>(p, static_cast<cudaStream_t>(stream));
 }
