@@ -17,9 +17,10 @@
 //   warp 0      producer: claims work items in order and TMA-loads them into a
 //               ring of shared-memory stages
 //   warp 1      one thread issues the MMAs and the commits
-//   warps 2..5  load each stage's activation rows and scales, move the block
+//   warps 2..    load each stage's activation rows (4 warps for decode blocks, 8
+//               for prefill); warps 2..5 also load its scales and move the block
 //               scales to tensor memory
-//   warps 6..9  epilogue: read the TMEM accumulators (double-buffered), reduce
+//   last 4 warps epilogue: read the TMEM accumulators (double-buffered), reduce
 //               the K splits of a gate/up tile, finish SwiGLU and re-split h into
 //               E2M1 terms, or write the outputs.
 // Work items: gate/up items (64 rows of gate + the same 64 rows of up = one
@@ -54,8 +55,6 @@ constexpr int SC_MAX = 112;                 // scale bytes per row of one item (
 constexpr int SA_BYTES = 128 * SC_MAX;      // A scales of an item
 constexpr int XCH_FLOATS = 128 * 16;        // gate/up exchange: 128 rows x 16 tokens (xor-swizzled)
 constexpr int CHUNK = 16;                   // most pairs of one expert per work item (80 MMA columns)
-constexpr int NWARPS = 10;
-constexpr int NTHREADS = NWARPS * 32;
 constexpr int S = TC_GU_SPLIT;
 static_assert(S == 2, "the gate/up hand-over pairs exactly two splits");
 
@@ -93,6 +92,13 @@ struct Cfg {
     static constexpr int META_BYTES = MAX_U * 8 + (MAX_U + 1) * 4 + TOKS * 2 + 2 * CHUNK * 2 + 12;
     // each scale-mover warp's staging of the activation scale bytes, per stage
     static constexpr int SBS_BYTES = 4 * NST * NBM * 16;
+    // activation-copy warps (2 .. 1 + NMOV; the first four also move the scales), then
+    // four epilogue warps.  A prefill stage carries 80 activation rows, whose copies
+    // take eight warps to issue; the 32-row configuration keeps four.
+    static constexpr int NMOV = NBM == 32 ? 4 : 8;
+    static constexpr int MOV_T = 32 * NMOV;     // copy threads
+    static constexpr int EPI_W0 = 2 + NMOV;     // first epilogue warp
+    static constexpr int NTHREADS = (EPI_W0 + 4) * 32;
     static constexpr size_t SMEM =
         (size_t)NST * STAGE + 2 * SCB + SBS_BYTES + XCH_FLOATS * 4 + META_BYTES + 1024 + 1024;
     static_assert(STAGE % 1024 == 0 && SCB % 128 == 0, "TMA destinations stay aligned");
@@ -482,7 +488,7 @@ __device__ __forceinline__ int b_src_row(const Meta& m, int row, const uint16_t*
 template <int NBM>
 struct BRows {
     int item = -1;
-    int d[NBM * BP / 128];
+    int d[NBM * BP / Cfg<NBM>::MOV_T];
     int s[3];
 };
 
@@ -507,12 +513,13 @@ __device__ __forceinline__ void cp_async_wait(int pending) {
 template <int NBM>
 __device__ __forceinline__ void b_issue(const Params& p, const Meta m, int t, int lane, uint32_t bst, uint32_t sbs,
                                         BRows<NBM>& r, const uint16_t* tok, const uint16_t* tokb) {
+    using C = Cfg<NBM>;
     if (r.item != m.item) {
         r.item = m.item;
 #pragma unroll
-        for (int i = 0; i < NBM * BP / 128; i++) {
-            if (128 * i >= m.nrow * BP) break;  // no row of this or later pieces is in use
-            const int row = (t + 128 * i) / BP;
+        for (int i = 0; i < NBM * BP / C::MOV_T; i++) {
+            if (C::MOV_T * i >= m.nrow * BP) break;  // no row of this or later pieces is in use
+            const int row = (t + C::MOV_T * i) / BP;
             r.d[i] = row < m.nrow ? b_src_row(m, row, tok, tokb) : 0;
         }
 #pragma unroll
@@ -527,24 +534,26 @@ __device__ __forceinline__ void b_issue(const Params& p, const Meta m, int t, in
     const int ld = gu ? p.d : p.f;
     const int k0 = m.kbase + m.chunk * KC;
 #pragma unroll
-    for (int i = 0; i < NBM * BP / 128; i++) {
-        if (128 * i >= m.nrow * BP) break;  // the same in the whole warp
-        const int j = t + 128 * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
+    for (int i = 0; i < NBM * BP / C::MOV_T; i++) {
+        if (C::MOV_T * i >= m.nrow * BP) break;  // the same in the whole warp
+        const int j = t + C::MOV_T * i, row = j / BP, c16 = j % BP, kh = c16 >> 3, cc = c16 & 7;
         if (row < m.nrow)
             cp_async16(bst + kh * (NBM * 128) + row * 128 + ((cc ^ (row & 7)) << 4),
                        src + (size_t)r.d[i] * (ld / 2) + k0 / 2 + c16 * 16);
     }
     static_assert(KC / 32 == 16, "one 16-byte scale copy per row and stage");
+    if (t < 128) {  // the four scale warps
 #pragma unroll
-    for (int c = 0; c < 3; c++) {
-        const int row = 32 * c + lane;
-        if (row < m.nrow && row < NBM) cp_async16(sbs + row * 16, ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32);
+        for (int c = 0; c < 3; c++) {
+            const int row = 32 * c + lane;
+            if (row < m.nrow && row < NBM) cp_async16(sbs + row * 16, ssrc + (size_t)r.s[c] * (ld / 32) + k0 / 32);
+        }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// warps 2..5: per stage, the activation rows into the stage's B area (above) and
-// every E8M0 scale into tensor memory.  Scale of row m (A: weight row, B: activation
+// the copy warps: per stage, the activation rows into the stage's B area (above);
+// warps 2..5 also every E8M0 scale into tensor memory.  Scale of row m (A: weight row, B: activation
 // row) for the stage's K blocks 4*set..4*set+3 is byte (kb % 4) of the 32-bit word
 // at lane m % 32, column base + set*4 + m / 32; each warp writes the copy in its own
 // lane quadrant.  Stages are finished in order: once the thread's copies of the
@@ -557,6 +566,7 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
                             const Meta* meta, const uint16_t* tok, const uint16_t* tokb) {
     using C = Cfg<NBM>;
     const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) & 3, t = threadIdx.x - 64;
+    const bool scw = t < 128;  // warps 2..5 also move the scales (warp w writes lane quadrant w % 4)
     const uint32_t sbs = smem_u32(sbs_all) + (uint32_t)(q * C::NST * NBM * 16);  // this warp's scale staging
     uint32_t is = 0, iph = 0;   // next stage to issue, and the parity of its claim
     uint32_t fs = 0;            // next stage to finish
@@ -597,6 +607,13 @@ __device__ void scale_mover(const Params& p, unsigned char* smem, unsigned char*
         const Meta m = meta[fs];
         cp_async_wait(inflight - 1);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the copies, for the MMA's reads
+        if (!scw) {  // a copy-only warp: the stage's copies of this warp have landed
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sfr[fs]);
+            inflight--;
+            if (++fs == (uint32_t)C::NST) fs = 0;
+            continue;
+        }
         if (m.chunk == 0) {  // the item's A scales have landed
             if (__shfl_sync(0xffffffffu, mbar_wait(&scf[m.sbuf], (scph >> m.sbuf) & 1u) ? 1 : 0, 0) == 0) {
                 if (lane == 0) set_error(p.ctrl, MOE_EBIT_TIMEOUT);
@@ -748,12 +765,12 @@ __device__ __forceinline__ void tagged_pair(const Params& p, const unsigned long
     u = __uint_as_float((uint32_t)wu);
 }
 
-// warps 6..9: TMEM lane quadrant q = warp % 4, accumulator row m = 32q + lane
+// the last four warps: TMEM lane quadrant q = warp % 4, accumulator row m = 32q + lane
 template <int NBM>
 __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t tag, uint64_t* acc_full,
                          uint64_t* acc_empty, const AccMeta* am) {
     using C = Cfg<NBM>;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - 6;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, q = warp & 3, ew = warp - Cfg<NBM>::EPI_W0;
     const int N = p.n_rows;
     __shared__ int s_flag;  // the epilogue warps' shared decision of the current gate/up item
     uint32_t it = 0;
@@ -905,7 +922,7 @@ __device__ void epilogue(const Params& p, uint32_t tbase, float* xch, uint32_t t
 }
 
 template <int NBM>
-__global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(Cfg<NBM>::NTHREADS, 1) tc_expert_kernel(const __grid_constant__ Params p) {
     using C = Cfg<NBM>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -939,7 +956,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         for (int s = 0; s < C::NST; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sfr[s], 4);
+            mbar_init(&sfr[s], C::NMOV);
             mbar_init(&mready[s], 1);
         }
         mbar_init(&scf[0], 1);
@@ -981,7 +998,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     const int U = min(s_u, C::MAX_U);
     // every expert's slot and pair range (all loads in flight at once), then the
     // prefix of its chunk counts (one warp: contiguous runs per lane, then a scan)
-    for (int u = tid; u < U; u += NTHREADS) {
+    for (int u = tid; u < U; u += C::NTHREADS) {
         const int ui = ordered_index(p.order, u, U);
         int z = __ldg(p.expert_slot + __ldcg(p.uexp + ui));
         const int o0 = __ldcg(p.off + ui), r = __ldcg(p.off + ui + 1) - o0;
@@ -992,7 +1009,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
         umeta[u] = make_uint2((uint32_t)z, (uint32_t)o0 | ((uint32_t)r << 16));
     }
     if (tok != nullptr)  // the block row of every pair (small blocks only)
-        for (int i = tid; i < p.nk && i < C::TOKS; i += NTHREADS) tok[i] = (uint16_t)(__ldcg(p.pair + i) / p.k);
+        for (int i = tid; i < p.nk && i < C::TOKS; i += C::NTHREADS) tok[i] = (uint16_t)(__ldcg(p.pair + i) / p.k);
     __syncthreads();
     if (warp == 1) {
         const int lane = tid & 31, per = (U + 31) / 32, b0 = lane * per, b1 = min(U, b0 + per);
@@ -1021,7 +1038,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
                           tok != nullptr ? nullptr : tokb);
     } else if (warp == 1) {
         if ((tid & 31) == 0) mma_issuer<NBM>(p, smem, tbase, full, empty, sfr, acc_full, acc_empty, done, meta, am);
-    } else if (warp < 6) {
+    } else if (warp < C::EPI_W0) {
         scale_mover<NBM>(p, smem, scbuf, sbs, tbase, mready, scf, sce, sfr, meta, tok, tokb);
     } else {
         epilogue<NBM>(p, tbase, xch, s_tag, acc_full, acc_empty, am);
@@ -1040,8 +1057,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) tc_expert_kernel(const __grid_con
     if (s_last) {
         __threadfence();
         const int V = cp[U];
-        for (int i = tid; i < V; i += NTHREADS) p.gu_done[i] = 0;
-        for (int i = tid; i < V * p.n_gu; i += NTHREADS) p.gu_state[i] = 0;
+        for (int i = tid; i < V; i += C::NTHREADS) p.gu_done[i] = 0;
+        for (int i = tid; i < V * p.n_gu; i += C::NTHREADS) p.gu_state[i] = 0;
         if (tid == 0) {
             p.ctrl[CTRL_WORK_TC] = 0;
             p.ctrl[CTRL_EXIT_TC] = 0;
@@ -1100,7 +1117,7 @@ static int launch(const Params& p, cudaStream_t stream) {
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
         return MOE_ERR_CUDA;
-    if (launch_chained(tc_expert_kernel<NBM>, dim3(sms), dim3(NTHREADS), C::SMEM, stream, p) != cudaSuccess)
+    if (launch_chained(tc_expert_kernel<NBM>, dim3(sms), dim3(C::NTHREADS), C::SMEM, stream, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
