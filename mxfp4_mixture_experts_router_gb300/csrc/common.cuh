@@ -58,8 +58,8 @@ constexpr int SH_K_SPLIT = 8;
 
 struct WsLayout {
     size_t ctrl, uexp, uorder, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
-        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_state, x16s, xexps, gu_done_sh, hmax_sh, h_sh, sh_part, sh_cnt,
-        rbits, rbits2, rbase, total;
+        x_mx, x_sc, h_mx, h_sc, gu_done_tc, gu_part, gu_state, x16s, xexps, gu_done_sh, hmax_sh, h_sh, h_sh_hl, sh_part,
+        sh_cnt, rbits, rbits2, rbase, total;
     int64_t mx_rows_x, mx_rows_h;  // rows of the MX activation buffers (with padding)
     int64_t pairs;   // capacity of the pair-indexed buffers: n_shared*N + N*k
 };
@@ -113,6 +113,9 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     L.gu_done_sh = take(64 * 4);
     L.hmax_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * 4);
     L.h_sh = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
+    // blocks of more than 16 rows: h * 2^-p of every shared pair as f16 hi and lo parts
+    // ([s][N][f] each), split once for all the down projection's row tiles
+    L.h_sh_hl = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
     // the shared experts' gate/up partial sums [s][f/16 tiles][16-row chunks][K slices][2][16][16]
     // and per (s, tile, chunk) the slices finished
     const int64_t sh_units = (int64_t)(n_shared > 0 ? n_shared : 1) * (f / 16) * ((N + 15) / 16);

@@ -51,6 +51,8 @@ struct Params {
     float* part;              // gate/up partials [s][tile][chunk][ks][2][16 rows][16 cols]
     uint32_t* cnt;            // [s][tile][chunk] slices finished
     float* h;                 // [s][N][f]
+    __half* h_hi;             // [s][N][f] f16 parts of h * 2^-p (p from the row's max |h|): hi
+    __half* h_lo;             // and lo = h * 2^-p - hi, rounded to f16
     uint32_t* hmax;           // [s][N] max |h| bits
     float* out;               // [s][N][d]
     uint32_t* ctrl;
@@ -271,10 +273,36 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     if (lane == 0) p.cnt[tu] = 0u;
 }
 
+// h of every (shared expert, row) -> f16 hi + lo parts of h * 2^-p, p from the row's
+// largest |h|: one CTA per (expert, row).  Each value is split once here instead of
+// once per 16-row output tile of the down projection.
+__global__ void __launch_bounds__(256) sh_split_kernel(const Params p) {
+    griddep_wait();  // h and its row maxima come from the gate/up kernel
+    griddep_launch_dependents();
+    const size_t row = blockIdx.x;  // s * n_rows + n
+    const float sc = exp2i(-f16_scale_exponent(__ldcg(p.hmax + row)));
+    const float* h = p.h + row * p.f;
+    for (int c = threadIdx.x * 4; c < p.f; c += 256 * 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(h + c));
+        const float vv[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+            const __half2 h2 = __floats2half2_rn(vv[2 * e], vv[2 * e + 1]);
+            const float2 back = __half22float2(h2);
+            hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            const __half2 l2 = __floats2half2_rn(vv[2 * e] - back.x, vv[2 * e + 1] - back.y);
+            lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+        *reinterpret_cast<uint2*>(p.h_hi + row * p.f + c) = make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2*>(p.h_lo + row * p.f + c) = make_uint2(lo[0], lo[1]);
+    }
+}
+
 struct DnWin {
     uint2 w0[UNROLL], w1[UNROLL];
     uint16_t s0[UNROLL], s1[UNROLL];
-    float4 h[2][UNROLL][2];
+    uint4 hi[2][UNROLL], lo[2][UNROLL];  // 8 f16 of each part per n-tile and group
 };
 
 // down: warp unit = (expert s, 16 output rows, 16-row chunk of the block), full K
@@ -305,8 +333,7 @@ __global__ void __launch_bounds__(THREADS) sh_dn_kernel(const Params p) {
     const int nl = nb + g, nh = nb + 8 + g;
     const bool vl = nl < p.n_rows, vh = nh < p.n_rows;
     const bool two = nb + 8 < p.n_rows;
-    const float* hl = p.h + ((size_t)s * p.n_rows + (vl ? nl : 0)) * f;
-    const float* hh = p.h + ((size_t)s * p.n_rows + (vh ? nh : 0)) * f;
+    const size_t rl = ((size_t)s * p.n_rows + (vl ? nl : 0)) * f, rh = ((size_t)s * p.n_rows + (vh ? nh : 0)) * f;
     auto load_w = [&](DnWin& w, int j0) {
 #pragma unroll
         for (int t = 0; t < UNROLL; t++) {
@@ -327,18 +354,16 @@ __global__ void __launch_bounds__(THREADS) sh_dn_kernel(const Params p) {
 #pragma unroll
             for (int nt = 0; nt < 2; nt++) {
                 const bool v = in && (nt ? (two && vh) : vl);
-                const float* hr = nt ? hh : hl;
-                w.h[nt][t][0] = v ? __ldg(reinterpret_cast<const float4*>(hr + k)) : make_float4(0.f, 0.f, 0.f, 0.f);
-                w.h[nt][t][1] = v ? __ldg(reinterpret_cast<const float4*>(hr + k + 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const size_t r = (nt ? rh : rl) + k;
+                w.hi[nt][t] = v ? __ldg(reinterpret_cast<const uint4*>(p.h_hi + r)) : make_uint4(0, 0, 0, 0);
+                w.lo[nt][t] = v ? __ldg(reinterpret_cast<const uint4*>(p.h_lo + r)) : make_uint4(0, 0, 0, 0);
             }
         }
     };
     DnWin cur, nxt;
     load_w(cur, 0);
-    griddep_wait();  // h and its row maxima come from the gate/up kernel
+    griddep_wait();  // the split parts of h come from the split kernel
     griddep_launch_dependents();
-    const float sl = vl ? exp2i(-f16_scale_exponent(__ldcg(p.hmax + (size_t)s * p.n_rows + nl))) : 0.f;
-    const float shh = vh ? exp2i(-f16_scale_exponent(__ldcg(p.hmax + (size_t)s * p.n_rows + nh))) : 0.f;
     load_h(cur, 0);
     float acc[2][4];
 #pragma unroll
@@ -359,18 +384,8 @@ __global__ void __launch_bounds__(THREADS) sh_dn_kernel(const Params p) {
 #pragma unroll
             for (int nt = 0; nt < 2; nt++) {
                 if (nt == 1 && !two) break;
-                const float sc = nt ? shh : sl;
-                const float4 va = cur.h[nt][t][0], vb = cur.h[nt][t][1];
-                const float vv[8] = {va.x * sc, va.y * sc, va.z * sc, va.w * sc, vb.x * sc, vb.y * sc, vb.z * sc, vb.w * sc};
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const __half2 h2 = __floats2half2_rn(vv[2 * e], vv[2 * e + 1]);
-                    const float2 back = __half22float2(h2);
-                    hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                    const __half2 l2 = __floats2half2_rn(vv[2 * e] - back.x, vv[2 * e + 1] - back.y);
-                    lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
-                }
+                const uint4 hv = cur.hi[nt][t], lv = cur.lo[nt][t];
+                const uint32_t hi[4] = {hv.x, hv.y, hv.z, hv.w}, lo[4] = {lv.x, lv.y, lv.z, lv.w};
                 float pp[4] = {0.f, 0.f, 0.f, 0.f};
                 mma_f16(pp, a1[0], a1[1], a1[2], a1[3], hi[0], hi[1]);
                 mma_f16(pp, a2[0], a2[1], a2[2], a2[3], hi[2], hi[3]);
@@ -427,6 +442,8 @@ int shared_launch(const moe_desc* desc, int n_rows, int n_rows_max, const uint16
     p.part = reinterpret_cast<float*>(base + L.sh_part);
     p.cnt = reinterpret_cast<uint32_t*>(base + L.sh_cnt);
     p.h = reinterpret_cast<float*>(base + L.h_sh);
+    p.h_hi = reinterpret_cast<__half*>(base + L.h_sh_hl);
+    p.h_lo = p.h_hi + (size_t)(n_shared > 0 ? n_shared : 1) * n_rows_max * f;
     p.hmax = reinterpret_cast<uint32_t*>(base + L.hmax_sh);
     p.out = reinterpret_cast<float*>(base + L.shared_y);
     p.ctrl = reinterpret_cast<uint32_t*>(base + L.ctrl);
@@ -450,6 +467,8 @@ int shared_launch(const moe_desc* desc, int n_rows, int n_rows_max, const uint16
     const int64_t dn_units = (int64_t)n_shared * (d / 16) * p.n_chunks;
     if (launch_chained(sh_gu_kernel, dim3((unsigned)((gu_units + WARPS - 1) / WARPS)), dim3(THREADS), 0, s, p) !=
         cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (launch_chained(sh_split_kernel, dim3((unsigned)(n_shared * n_rows)), dim3(256), 0, s, p) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (launch_chained(sh_dn_kernel, dim3((unsigned)((dn_units + WARPS - 1) / WARPS)), dim3(THREADS), 0, s, p) !=
         cudaSuccess)
