@@ -116,10 +116,11 @@ inline WsLayout ws_layout(int d, int f, int E, int k, int n_rows_max, int n_shar
     // blocks of more than 16 rows: h * 2^-p of every shared pair as f16 hi and lo parts
     // ([s][N][f] each), split once for all the down projection's row tiles
     L.h_sh_hl = take((size_t)(n_shared > 0 ? n_shared : 1) * N * f * 4);
-    // the shared experts' gate/up partial sums [s][f/16 tiles][16-row chunks][K slices][2][16][16]
+    // the shared experts' gate/up partial sums [s][f/16 tiles][32-row chunks][K slices][2][16][32]
     // and per (s, tile, chunk) the slices finished
-    const int64_t sh_units = (int64_t)(n_shared > 0 ? n_shared : 1) * (f / 16) * ((N + 15) / 16);
-    L.sh_part = take((size_t)sh_units * SH_K_SPLIT * 512 * 4);
+    // (chunks of 32 block rows: 2 x 16 x 32 sums per unit and slice)
+    const int64_t sh_units = (int64_t)(n_shared > 0 ? n_shared : 1) * (f / 16) * ((N + 31) / 32);
+    L.sh_part = take((size_t)sh_units * SH_K_SPLIT * 1024 * 4);
     L.sh_cnt = take((size_t)sh_units * 4);
     // grouping of blocks of more than 32 rows: per (32-row group, expert) the bitmap
     // of rows that selected it (zeroed again after use), its copy, and the offset of

@@ -9,15 +9,16 @@
 //
 // Design (GB300): the weights stream straight from global memory into the
 // registers of tensor-core fragments (no shared-memory staging, no producer
-// warp); a warp works on 16 block rows at a time, so the weights are read from
-// HBM once and from L2 for every further 16 rows of the block.  Decode blocks
+// warp); a gate/up warp works on 32 block rows at a time and a down warp on 16, so
+// the weights are read from HBM once and from L2 for every further chunk of rows.  Decode blocks
 // (up to 16 rows) use the TMA-fed engine of experts.cu instead, whose deeper
 // staging keeps more bytes in flight per SM.
 //
 //   sh_prep_kernel  f16 copy of the block's rows, each scaled by a power of two
 //                   2^-p chosen from the row's largest magnitude
 //   sh_gu_kernel    gate and up projections: a warp owns 16 rows of gate and the
-//                   same 16 rows of up over one of SH_KS K slices; per 32-wide K
+//                   same 16 rows of up, for 32 block rows, over one of SH_KS K
+//                   slices; per 32-wide K
 //                   group two m16n8k16 MMAs (f16 in, fp32 out) give the group's
 //                   exact partial, scaled by its fp16 scale into the accumulator;
 //                   the last slice of a tile to finish sums the slices in slice
@@ -40,15 +41,19 @@ namespace sh {
 constexpr int WARPS = 4;             // warps per CTA
 constexpr int THREADS = WARPS * 32;
 constexpr int SH_KS = SH_K_SPLIT;    // K slices of the gate/up projection
-constexpr int UNROLL = 4;            // K groups whose loads are in flight together
+constexpr int UNROLL = 4;            // K groups whose loads are in flight together (down)
+constexpr int GU_NT = 4;             // n-tiles (8 block rows each) of a gate/up warp unit
+constexpr int GU_W = 8 * GU_NT;      // block rows of a gate/up warp unit
+constexpr int GU_UNROLL = 2;         // K groups whose loads are in flight together (gate/up)
 
 struct Params {
     const int8_t* q;          // shared pool base (slot s at q + s * slot_bytes)
     int64_t slot_bytes;
-    int d, f, n_rows, n_shared, n_chunks;  // n_chunks = ceil(n_rows / 16)
+    int d, f, n_rows, n_shared, n_chunks;  // n_chunks = ceil(n_rows / 16): the down projection's row chunks
+    int n_gchunks;                          // ceil(n_rows / GU_W): the gate/up projection's
     const __half* x16;        // [N][d] f16 rows (x * 2^-xexp)
     const int* xexp;          // [N]
-    float* part;              // gate/up partials [s][tile][chunk][ks][2][16 rows][16 cols]
+    float* part;              // gate/up partials [s][tile][chunk][ks][2][16 rows][GU_W cols]
     uint32_t* cnt;            // [s][tile][chunk] slices finished
     float* h;                 // [s][N][f]
     __half* h_hi;             // [s][N][f] f16 parts of h * 2^-p (p from the row's max |h|): hi
@@ -122,21 +127,22 @@ __global__ void __launch_bounds__(256) sh_prep_kernel(const Params p) {
     if (p.wait_at_end && tid == 0) griddep_wait();
 }
 
-// The loads of a window of UNROLL K groups (weights, their scales, the activation
+// The loads of a window of GU_UNROLL K groups (weights, their scales, the activation
 // fragments) are issued one window ahead of its MMAs: a warp keeps two windows in
 // registers, so every global load has a window's worth of MMAs to hide behind.
 struct GuWin {
-    uint2 wg0[UNROLL], wg1[UNROLL], wu0[UNROLL], wu1[UNROLL];
-    uint16_t sg0[UNROLL], sg1[UNROLL], su0[UNROLL], su1[UNROLL];
-    uint4 x0[UNROLL], x1[UNROLL];
+    uint2 wg0[GU_UNROLL], wg1[GU_UNROLL], wu0[GU_UNROLL], wu1[GU_UNROLL];
+    uint16_t sg0[GU_UNROLL], sg1[GU_UNROLL], su0[GU_UNROLL], su1[GU_UNROLL];
+    uint4 x[GU_NT][GU_UNROLL];
 };
 
-// gate/up: warp unit = (expert s, 16-row tile, 16-row chunk of the block, K slice)
+// gate/up: warp unit = (expert s, 16-row tile, chunk of GU_W block rows, K slice).  The
+// weights a warp converts to f16 serve all GU_NT n-tiles of its chunk.
 __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, i = lane & 3;
     const int tiles = p.f / 16;
-    const int64_t units = (int64_t)p.n_shared * tiles * p.n_chunks * SH_KS;
+    const int64_t units = (int64_t)p.n_shared * tiles * p.n_gchunks * SH_KS;
     const int64_t u = (int64_t)blockIdx.x * WARPS + warp;
     if (threadIdx.x == 0 && blockIdx.x == 0) tl_begin(p.ctrl, TL_SHARED);
     if (u >= units) {
@@ -145,8 +151,8 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     }
     const int ks = (int)(u % SH_KS);
     const int64_t r1 = u / SH_KS;
-    const int ch = (int)(r1 % p.n_chunks);
-    const int64_t r2 = r1 / p.n_chunks;
+    const int ch = (int)(r1 % p.n_gchunks);
+    const int64_t r2 = r1 / p.n_gchunks;
     const int tile = (int)(r2 % tiles), s = (int)(r2 / tiles);
     const int d = p.d, f = p.f, ksl = d / SH_KS, G = ksl / 32;
     const int8_t* slab = p.q + (size_t)s * p.slot_bytes;
@@ -161,15 +167,19 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     const uint16_t* su0 = reinterpret_cast<const uint16_t*>(reinterpret_cast<const int8_t*>(sg0) + per);
     const uint16_t* su1 = su0 + (size_t)8 * (d / 32);
     const int kbase = ks * ksl;
-    const int nb = ch * 16;
-    const int n_lo = nb + g, n_hi = nb + 8 + g;  // B columns this thread supplies
-    const bool v_lo = n_lo < p.n_rows, v_hi = n_hi < p.n_rows;
-    const bool two = nb + 8 < p.n_rows;  // second n-tile of the chunk in use
-    const __half* x_lo = p.x16 + (size_t)(v_lo ? n_lo : 0) * d;
-    const __half* x_hi = p.x16 + (size_t)(v_hi ? n_hi : 0) * d;
+    const int nb = ch * GU_W;
+    const int ntu = min(GU_NT, (p.n_rows - nb + 7) / 8);  // n-tiles of the chunk in use
+    const __half* xr[GU_NT];  // B column (block row) nb + 8 nt + g of each n-tile
+    bool xv[GU_NT];
+#pragma unroll
+    for (int nt = 0; nt < GU_NT; nt++) {
+        const int n = nb + nt * 8 + g;
+        xv[nt] = n < p.n_rows;
+        xr[nt] = p.x16 + (size_t)(xv[nt] ? n : 0) * d;
+    }
     auto load_w = [&](GuWin& w, int j0) {  // weights and scales of window j0 (independent of the rows)
 #pragma unroll
-        for (int t = 0; t < UNROLL; t++) {
+        for (int t = 0; t < GU_UNROLL; t++) {
             const int j = j0 + t;
             if (j < G) {
                 const int k = kbase + 32 * j;
@@ -182,11 +192,13 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     };
     auto load_x = [&](GuWin& w, int j0) {
 #pragma unroll
-        for (int t = 0; t < UNROLL; t++) {
+        for (int t = 0; t < GU_UNROLL; t++) {
             const int k = kbase + 32 * (j0 + t) + 8 * i;
             const bool in = j0 + t < G;
-            w.x0[t] = (in && v_lo) ? __ldg(reinterpret_cast<const uint4*>(x_lo + k)) : make_uint4(0, 0, 0, 0);
-            w.x1[t] = (in && two && v_hi) ? __ldg(reinterpret_cast<const uint4*>(x_hi + k)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int nt = 0; nt < GU_NT; nt++)
+                w.x[nt][t] = (in && nt < ntu && xv[nt]) ? __ldg(reinterpret_cast<const uint4*>(xr[nt] + k))
+                                                        : make_uint4(0, 0, 0, 0);
         }
     };
     GuWin cur, nxt;
@@ -194,18 +206,18 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     if (p.wait_at_start) griddep_wait();
     griddep_launch_dependents();
     load_x(cur, 0);
-    float ag[2][4], au[2][4];
+    float ag[GU_NT][4], au[GU_NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; nt++)
+    for (int nt = 0; nt < GU_NT; nt++)
 #pragma unroll
         for (int t = 0; t < 4; t++) ag[nt][t] = au[nt][t] = 0.f;
-    for (int j0 = 0; j0 < G; j0 += UNROLL) {
-        if (j0 + UNROLL < G) {
-            load_w(nxt, j0 + UNROLL);
-            load_x(nxt, j0 + UNROLL);
+    for (int j0 = 0; j0 < G; j0 += GU_UNROLL) {
+        if (j0 + GU_UNROLL < G) {
+            load_w(nxt, j0 + GU_UNROLL);
+            load_x(nxt, j0 + GU_UNROLL);
         }
 #pragma unroll
-        for (int t = 0; t < UNROLL; t++) {
+        for (int t = 0; t < GU_UNROLL; t++) {
             if (j0 + t >= G) break;
             uint32_t ga1[4], ga2[4], ua1[4], ua2[4];
             frags(cur.wg0[t], cur.wg1[t], ga1, ga2);
@@ -213,9 +225,9 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
             const float fg0 = __half2float(__ushort_as_half(cur.sg0[t])), fg1 = __half2float(__ushort_as_half(cur.sg1[t]));
             const float fu0 = __half2float(__ushort_as_half(cur.su0[t])), fu1 = __half2float(__ushort_as_half(cur.su1[t]));
 #pragma unroll
-            for (int nt = 0; nt < 2; nt++) {
-                if (nt == 1 && !two) break;
-                const uint4 bx = nt ? cur.x1[t] : cur.x0[t];
+            for (int nt = 0; nt < GU_NT; nt++) {
+                if (nt >= ntu) break;
+                const uint4 bx = cur.x[nt][t];
                 float pg[4] = {0.f, 0.f, 0.f, 0.f}, pu[4] = {0.f, 0.f, 0.f, 0.f};
                 mma_f16(pg, ga1[0], ga1[1], ga1[2], ga1[3], bx.x, bx.y);
                 mma_f16(pg, ga2[0], ga2[1], ga2[2], ga2[3], bx.z, bx.w);
@@ -229,20 +241,21 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
         }
         cur = nxt;
     }
-    // this slice's sums: part[tile unit][ks][gate|up][row][col]
-    const int64_t tu = ((int64_t)s * tiles + tile) * p.n_chunks + ch;
-    float* dst = p.part + (tu * SH_KS + ks) * 2 * 256;
+    // this slice's sums: part[tile unit][ks][gate|up][16 rows][GU_W cols]
+    constexpr int UN = 16 * GU_W;  // sums of one matrix in one unit
+    const int64_t tu = ((int64_t)s * tiles + tile) * p.n_gchunks + ch;
+    float* dst = p.part + (tu * SH_KS + ks) * 2 * UN;
 #pragma unroll
-    for (int nt = 0; nt < 2; nt++) {
+    for (int nt = 0; nt < GU_NT; nt++) {
         const int c = nt * 8 + 2 * i;
-        dst[g * 16 + c] = ag[nt][0];
-        dst[g * 16 + c + 1] = ag[nt][1];
-        dst[(g + 8) * 16 + c] = ag[nt][2];
-        dst[(g + 8) * 16 + c + 1] = ag[nt][3];
-        dst[256 + g * 16 + c] = au[nt][0];
-        dst[256 + g * 16 + c + 1] = au[nt][1];
-        dst[256 + (g + 8) * 16 + c] = au[nt][2];
-        dst[256 + (g + 8) * 16 + c + 1] = au[nt][3];
+        dst[g * GU_W + c] = ag[nt][0];
+        dst[g * GU_W + c + 1] = ag[nt][1];
+        dst[(g + 8) * GU_W + c] = ag[nt][2];
+        dst[(g + 8) * GU_W + c + 1] = ag[nt][3];
+        dst[UN + g * GU_W + c] = au[nt][0];
+        dst[UN + g * GU_W + c + 1] = au[nt][1];
+        dst[UN + (g + 8) * GU_W + c] = au[nt][2];
+        dst[UN + (g + 8) * GU_W + c + 1] = au[nt][3];
     }
     __threadfence();
     __syncwarp();
@@ -252,23 +265,22 @@ __global__ void __launch_bounds__(THREADS) sh_gu_kernel(const Params p) {
     if (!last) return;
     __threadfence();
     // the tile's last slice: sum the slices in slice order, then SwiGLU
-    const float* src = p.part + tu * SH_KS * 2 * 256;
-    for (int e = lane; e < 256; e += 32) {
-        const int row = e >> 4, col = e & 15, n = nb + col;
+    const float* src = p.part + tu * SH_KS * 2 * UN;
+    for (int e = lane; e < UN; e += 32) {
+        const int row = e / GU_W, col = e - row * GU_W, n = nb + col;
+        if (n >= p.n_rows) continue;
         float gs = 0.f, us = 0.f;
 #pragma unroll
         for (int q = 0; q < SH_KS; q++) {
-            gs += __ldcg(src + q * 512 + e);
-            us += __ldcg(src + q * 512 + 256 + e);
+            gs += __ldcg(src + q * 2 * UN + e);
+            us += __ldcg(src + q * 2 * UN + UN + e);
         }
-        if (n < p.n_rows) {
-            const float sc = exp2i(__ldg(p.xexp + n));
-            gs *= sc;
-            us *= sc;
-            const float hv = gs / (1.f + expf(-gs)) * us;
-            p.h[((size_t)s * p.n_rows + n) * f + tile * 16 + row] = hv;
-            atomicMax(p.hmax + (size_t)s * p.n_rows + n, __float_as_uint(hv) & 0x7FFFFFFFu);
-        }
+        const float sc = exp2i(__ldg(p.xexp + n));
+        gs *= sc;
+        us *= sc;
+        const float hv = gs / (1.f + expf(-gs)) * us;
+        p.h[((size_t)s * p.n_rows + n) * f + tile * 16 + row] = hv;
+        atomicMax(p.hmax + (size_t)s * p.n_rows + n, __float_as_uint(hv) & 0x7FFFFFFFu);
     }
     if (lane == 0) p.cnt[tu] = 0u;
 }
@@ -437,6 +449,7 @@ int shared_launch(const moe_desc* desc, int n_rows, int n_rows_max, const uint16
     p.n_rows = n_rows;
     p.n_shared = n_shared;
     p.n_chunks = (n_rows + 15) / 16;
+    p.n_gchunks = (n_rows + GU_W - 1) / GU_W;
     p.x16 = reinterpret_cast<const __half*>(base + (prep ? L.x16s : L.x16));
     p.xexp = reinterpret_cast<const int*>(base + (prep ? L.xexps : L.xexp));
     p.part = reinterpret_cast<float*>(base + L.sh_part);
@@ -463,7 +476,7 @@ int shared_launch(const moe_desc* desc, int n_rows, int n_rows_max, const uint16
         if (cudaMemsetAsync(p.hmax, 0, (size_t)n_shared * n_rows * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
         p.wait_at_start = 1;
     }
-    const int64_t gu_units = (int64_t)n_shared * (f / 16) * p.n_chunks * SH_KS;
+    const int64_t gu_units = (int64_t)n_shared * (f / 16) * p.n_gchunks * SH_KS;
     const int64_t dn_units = (int64_t)n_shared * (d / 16) * p.n_chunks;
     if (launch_chained(sh_gu_kernel, dim3((unsigned)((gu_units + WARPS - 1) / WARPS)), dim3(THREADS), 0, s, p) !=
         cudaSuccess)
