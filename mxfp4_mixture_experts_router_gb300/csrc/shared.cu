@@ -18,13 +18,13 @@
 //                   2^-p chosen from the row's largest magnitude
 //   sh_gu_kernel    gate and up projections: a warp owns 16 rows of gate and the
 //                   same 16 rows of up, for 32 block rows, over one of SH_KS K
-//                   slices; per 32-wide K
-//                   group two m16n8k16 MMAs (f16 in, fp32 out) give the group's
-//                   exact partial, scaled by its fp16 scale into the accumulator;
-//                   the last slice of a tile to finish sums the slices in slice
-//                   order and applies SwiGLU (fp32 h)
-//   sh_dn_kernel    down projection: a warp owns 16 output rows over the full K,
-//                   h split into f16 hi + lo parts (per-row power-of-two scale)
+//                   slices; per 32-wide K group two m16n8k16 MMAs (f16 in, fp32
+//                   out) give the group's exact partial, scaled by its fp16 scale
+//                   into the accumulator; the last slice of a tile to finish sums
+//                   the slices in slice order and applies SwiGLU (fp32 h)
+//   sh_split_kernel h split once into f16 hi + lo parts (per-row power-of-two scale)
+//   sh_dn_kernel    down projection: a warp owns 16 output rows and 16 block rows
+//                   over the full K, on the hi and lo parts of h
 //
 // A thread (g = lane / 4, i = lane % 4) loads 8 consecutive int8 codes of its
 // rows g and g + 8 per group (bytes 8i..8i+7): inside the group, K positions
