@@ -44,7 +44,7 @@ constexpr int SH_KS = SH_K_SPLIT;    // K slices of the gate/up projection
 constexpr int UNROLL = 4;            // K groups whose loads are in flight together (down)
 constexpr int GU_NT = 4;             // n-tiles (8 block rows each) of a gate/up warp unit
 constexpr int GU_W = 8 * GU_NT;      // block rows of a gate/up warp unit
-constexpr int GU_UNROLL = 2;         // K groups whose loads are in flight together (gate/up)
+constexpr int GU_UNROLL = 3;         // K groups whose loads are in flight together (gate/up)
 
 struct Params {
     const int8_t* q;          // shared pool base (slot s at q + s * slot_bytes)
