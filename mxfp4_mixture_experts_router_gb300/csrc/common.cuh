@@ -54,7 +54,7 @@ constexpr int TC_GU_SPLIT = 2;
 // its own E8M0 scale per 32 elements): about 16 significant bits survive
 constexpr int MX_TERMS = 5;
 // K slices of the shared experts' gate/up projection
-constexpr int SH_K_SPLIT = 8;
+constexpr int SH_K_SPLIT = 4;
 
 struct WsLayout {
     size_t ctrl, uexp, uorder, off, pair, x16, xexp, gu_done, hmax, h, dbg_g, dbg_u, shared_y, logits,
